@@ -1,0 +1,254 @@
+/*
+ * replayssm.h -- C ABI of libreplayssm, the GB300 (sm_103a) ReplaySSM decode path.
+ *
+ * The operations follow "ReplaySSM: Cache SSM Inputs, Not State" (Tri Dao's
+ * blog post, as summarised on papercache).  Instead of reading and writing the
+ * fp32 SSM state S (nheads, d, n) every token, each sequence keeps a
+ * checkpoint S_0 plus a ring buffer of its last L inputs; outputs come from
+ * S_0 and the buffer, and a flush folds the buffer into S_0 when it fills.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every call returns an rssm_status (RSSM_OK = 0, negative on error).  On a
+ *    non-zero status nothing was launched.
+ *  - Calls are asynchronous on the caller's stream and never synchronise.
+ *    Pass a cudaStream_t (NULL = the legacy default stream).  The calling
+ *    thread's current CUDA device must own every pointer.
+ *  - The caller owns all memory.  Every pointer is a DEVICE pointer,
+ *    contiguous, row-major in the documented layout.  S, S0, snapshot slots,
+ *    k, q and ring_k must be 16-byte aligned; every other array must be
+ *    aligned to its element size.  The library allocates nothing and keeps
+ *    no state between calls.
+ *  - dtypes: RSSM_F32 (float) or RSSM_BF16 (bfloat16).  The checkpoint and
+ *    state are always float32; the step size Delta, the gate g and beta are
+ *    float32.  Ring entries of v/k use the input dtype.
+ *  - One call handles one layer.  A stack of layers is a loop of calls.
+ *  - Inconsistent per-sequence bookkeeping found ON THE DEVICE (a committed
+ *    count out of range, a draft window that does not fit, an accepted count
+ *    out of range) sets a bit in the caller's sticky int32 error word *err
+ *    (RSSM_EBIT_*) and that sequence is skipped; kernels never trap and never
+ *    spin.  Read *err after synchronising; clear it yourself.
+ *  - Supported shapes (checked on the host, RSSM_ERR_UNSUPPORTED otherwise):
+ *    n (Mamba-2 state size) and dk (GDN key size) in {16, 32, 64, 128};
+ *    d and dv multiples of 4 with 4 <= d <= 256;
+ *    1 <= L <= 32; 1 <= T <= 8 and T <= L; H % G == 0; Hv % Hk == 0; B >= 1.
+ *
+ * Ring buffer and checkpoint layout (HBM)
+ * ---------------------------------------
+ *  Mamba-2 (rssm_m2_replay), per layer:
+ *    S0       float [B][H][d][n]
+ *    ring_v   in_dtype [B][H][L][d]
+ *    ring_k   in_dtype [B][G][L][n]      (k is shared by the H/G heads of a group)
+ *    ring_dt  float [B][H][L]
+ *    start, count, flag, sync   int32 [B]
+ *  Entry j (1-based) of sequence b's window sits in ring slot
+ *  (start[b] + j - 1) mod L; count[b] entries are committed.  Head i uses
+ *  group i / (H/G).  `sync` is a per-sequence arrival counter the kernels use
+ *  to hand the pointer update to the last of a sequence's thread blocks; it
+ *  must be zero before the first call and every call leaves it zero.
+ *
+ *  GDN (rssm_gdn_replay), per layer:
+ *    S0       float [B][Hv][dv][dk]
+ *    ring_u   u_dtype [B][Hv][L][dv]   (cached corrections u)
+ *    ring_k   in_dtype [B][Hk][L][dk]
+ *    ring_g   float [B][Hv][L]         (log decays g)
+ *    start, count, flag, sync   int32 [B]
+ */
+#ifndef REPLAYSSM_H_
+#define REPLAYSSM_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RSSM_API __attribute__((visibility("default")))
+#else
+#define RSSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *rssm_stream_t; /* identical to cudaStream_t */
+typedef int32_t rssm_status;
+
+#define RSSM_OK 0
+#define RSSM_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad dims, T > L ... */
+#define RSSM_ERR_UNSUPPORTED (-2) /* valid but not a supported shape/dtype      */
+#define RSSM_ERR_CUDA (-3)        /* the launch itself failed                     */
+
+#define RSSM_F32 0
+#define RSSM_BF16 1
+
+/* sticky device error bits (OR-ed into *err) */
+#define RSSM_EBIT_COUNT_RANGE 1 /* start/count outside [0, L-1] at a decode step   */
+#define RSSM_EBIT_WINDOW 2      /* count + T > L at a verify round                  */
+#define RSSM_EBIT_ACCEPTED 4    /* accepted outside [0, T] or count + accepted > L  */
+#define RSSM_EBIT_CUR 8         /* snapshot slot index outside [0, T]              */
+
+typedef struct {
+  int32_t B, H, G, d, n, L;
+  int32_t in_dtype; /* dtype of v, k, q and of ring_v, ring_k */
+  int32_t y_dtype;  /* dtype of y */
+} rssm_m2_dims;
+
+typedef struct {
+  float *S0;
+  void *ring_v;
+  void *ring_k;
+  float *ring_dt;
+  int32_t *start, *count, *flag, *sync;
+  int32_t *err; /* one int32 */
+} rssm_m2_replay;
+
+typedef struct {
+  int32_t B, Hv, Hk, dk, dv, L;
+  int32_t in_dtype; /* dtype of q, k, v and of ring_k */
+  int32_t u_dtype;  /* dtype of ring_u (RSSM_F32 recommended) */
+  int32_t y_dtype;
+} rssm_gdn_dims;
+
+typedef struct {
+  float *S0;
+  void *ring_u;
+  void *ring_k;
+  float *ring_g;
+  int32_t *start, *count, *flag, *sync;
+  int32_t *err;
+} rssm_gdn_replay;
+
+/* ------------------------------------------------------------------------ */
+/* Mamba-2                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Baseline decode step ("Background -- memory bound" recurrence; "Algorithm --
+ * Mamba-2 standard decode", baseline): per head a = exp(A_i Delta),
+ * S <- a S + Delta v k^T, y = S q, reading and writing the whole state.
+ *   S   float [B][H][d][n]  (in/out)     v  in_dtype [B][H][d]
+ *   k,q in_dtype [B][G][n]               dt float [B][H]      A float [H]
+ *   y   y_dtype [B][H][d] (out)                                               */
+RSSM_API rssm_status ssm_state_update_baseline(const rssm_m2_dims *dims, float *S, const void *v, const void *k,
+                                      const void *q, const float *dt, const float *A, void *y,
+                                      rssm_stream_t stream);
+
+/* ReplaySSM output-only decode step ("Relaxed requirement: output-only decode";
+ * "Algorithm -- Mamba-2 standard decode"): with h = count[b], append
+ * (v, Delta, k) at slot (start + h) mod L and write
+ *   y = abar (S_0 q) + sum_{j=1}^{h+1} s_j (k_j^T q) v_j,
+ *   abar = prod_{i<=h+1} a_i,  s_j = Delta_j prod_{j<i<=h+1} a_i,  a_i = exp(A Delta_i);
+ * then count <- h+1 and flag <- (count == L).  S_0 is only read.  Inputs as for
+ * the baseline.  A sequence whose start/count is out of range is skipped and
+ * sets RSSM_EBIT_COUNT_RANGE.                                                 */
+RSSM_API rssm_status replay_decode_step(const rssm_m2_dims *dims, const rssm_m2_replay *st, const void *v,
+                               const void *k, const void *q, const float *dt, const float *A, void *y,
+                               rssm_stream_t stream);
+
+/* Flush ("Algorithm -- Mamba-2 standard decode", flush): for every sequence
+ * with flag[b] != 0 and c = count[b] committed entries,
+ *   S_0 <- abar S_0 + sum_{j=1}^{c} s_j v_j k_j^T
+ * then start <- (start + c) mod L, count <- 0, flag <- 0.  Other sequences are
+ * untouched.  The flag array is plain data: setting it from the host flushes
+ * any sequence at any time without changing later outputs.                   */
+RSSM_API rssm_status replay_flush(const rssm_m2_dims *dims, const rssm_m2_replay *st, const float *A,
+                         rssm_stream_t stream);
+
+/* Speculative verify of T drafts ("Algorithm -- speculative decoding"): with
+ * h = count[b] (requires h + T <= L, else RSSM_EBIT_WINDOW and the sequence is
+ * skipped), write the T drafts tentatively at slots (start + h + s - 1) mod L
+ * and, for s = 1..T with p_s = h + s,
+ *   Y_s = abar_s (S_0 q_s) + sum_{j<=p_s} w_{j,s} (k_j^T q_s) v_j.
+ * count is unchanged; flag <- (h + 2T > L) (early flush one window ahead).
+ *   v  in_dtype [B][T][H][d]   k, q in_dtype [B][T][G][n]   dt float [B][T][H]
+ *   y  y_dtype [B][T][H][d]                                                   */
+RSSM_API rssm_status replay_spec_verify(const rssm_m2_dims *dims, const rssm_m2_replay *st, int32_t T,
+                               const void *v, const void *k, const void *q, const float *dt,
+                               const float *A, void *y, rssm_stream_t stream);
+
+/* Device-side commit ("Supplementary design for CUDA Graphs", device commit):
+ * count[b] += accepted[b] for b < B; rejected drafts are rolled back by not
+ * moving the pointer over them.  accepted outside [0, T] or count + accepted > L
+ * sets RSSM_EBIT_ACCEPTED and leaves that sequence unchanged.  Shared by the
+ * Mamba-2 and GDN paths.  accepted, count: int32 [B].                       */
+RSSM_API rssm_status replay_spec_commit(int32_t B, int32_t T, int32_t L, const int32_t *accepted, int32_t *count,
+                               int32_t *err, rssm_stream_t stream);
+
+/* Baseline speculative verify ("Algorithm -- speculative decoding", baseline):
+ * each sequence owns T+1 state slots; starting from slot cur[b], apply the T
+ * drafts serially (baseline recurrence), writing draft s's state to slot
+ * (cur + s) mod (T+1) and its output to y.
+ *   slots float [B][T+1][H][d][n]   cur int32 [B]   inputs/outputs as replay_spec_verify. */
+RSSM_API rssm_status ssm_spec_verify_baseline(const rssm_m2_dims *dims, int32_t T, float *slots, const int32_t *cur,
+                                     const void *v, const void *k, const void *q, const float *dt,
+                                     const float *A, void *y, int32_t *err, rssm_stream_t stream);
+
+/* Baseline commit: cur[b] <- (cur[b] + accepted[b]) mod (T+1). */
+RSSM_API rssm_status ssm_spec_commit_baseline(int32_t B, int32_t T, const int32_t *accepted, int32_t *cur,
+                                     int32_t *err, rssm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Gated DeltaNet                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Baseline GDN decode (appendix "GDN -- standard decode", baseline): per value
+ * head alpha = exp(g), u = beta (v - alpha S k), S <- alpha S + u k^T, y = S q.
+ *   S float [B][Hv][dv][dk] (in/out)   q, k in_dtype [B][Hk][dk]
+ *   v in_dtype [B][Hv][dv]             beta, g float [B][Hv]    y y_dtype [B][Hv][dv] */
+RSSM_API rssm_status gdn_state_update_baseline(const rssm_gdn_dims *dims, float *S, const void *q, const void *k,
+                                      const void *v, const float *beta, const float *g, void *y,
+                                      rssm_stream_t stream);
+
+/* GDN replay decode (appendix "GDN -- standard decode", cache u): with
+ * h = count[b], S_h = (prod alpha_j) S_0 + sum_j (prod_{i>j} alpha_i) u_j k_j^T
+ * (never materialised: S_h k and S_h q are formed from S_0 k, S_0 q and the
+ * buffer), u = beta (v - alpha S_h k), y = alpha S_h q + u (k . q); append
+ * (u, k, g); count <- h+1; flag <- (count == L).                             */
+RSSM_API rssm_status gdn_replay_decode(const rssm_gdn_dims *dims, const rssm_gdn_replay *st, const void *q,
+                              const void *k, const void *v, const float *beta, const float *g, void *y,
+                              rssm_stream_t stream);
+
+/* GDN flush: S_0 <- (prod alpha_j) S_0 + sum_j (prod_{i>j} alpha_i) u_j k_j^T
+ * over the committed entries of flagged sequences; pointer reset as the Mamba-2
+ * flush.                                                                      */
+RSSM_API rssm_status gdn_replay_flush(const rssm_gdn_dims *dims, const rssm_gdn_replay *st, rssm_stream_t stream);
+
+/* GDN chunked speculative verify (appendix "GDN -- speculative decoding"):
+ * with G_s = sum_{r<=s} g_r,
+ *   R_s = beta_s (v_s - e^{G_s} S_h k_s),
+ *   A_{s,s'} = beta_s e^{G_s - G_s'} (k_s . k_s')  (s' < s),
+ *   u_s = R_s - sum_{s'<s} A_{s,s'} u_s'   (T x T lower-triangular solve),
+ *   y_s = e^{G_s} S_h q_s + sum_{s'<=s} e^{G_s - G_s'} (k_s' . q_s) u_s'.
+ * Drafts (u_s, k_s, g_s) are written tentatively; count is unchanged;
+ * flag <- (h + 2T > L).  Commit with replay_spec_commit.
+ *   q, k in_dtype [B][T][Hk][dk]  v in_dtype [B][T][Hv][dv]  beta, g float [B][T][Hv]
+ *   y y_dtype [B][T][Hv][dv]                                                  */
+RSSM_API rssm_status gdn_replay_verify(const rssm_gdn_dims *dims, const rssm_gdn_replay *st, int32_t T, const void *q,
+                              const void *k, const void *v, const float *beta, const float *g, void *y,
+                              rssm_stream_t stream);
+
+/* Baseline GDN speculative verify: serial correction-form updates per draft
+ * with a full snapshot per draft (T+1 slots, as ssm_spec_verify_baseline).
+ *   slots float [B][T+1][Hv][dv][dk]   cur int32 [B].  Commit with
+ *   ssm_spec_commit_baseline.                                                 */
+RSSM_API rssm_status gdn_spec_verify_baseline(const rssm_gdn_dims *dims, int32_t T, float *slots, const int32_t *cur,
+                                     const void *q, const void *k, const void *v, const float *beta,
+                                     const float *g, void *y, int32_t *err, rssm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Utilities                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Library version, e.g. 100 for 0.1.0.  Host-only; never fails. */
+RSSM_API int32_t rssm_version(void);
+
+/* Static description of a status code.  Host-only; never fails. */
+RSSM_API const char *rssm_status_string(rssm_status s);
+
+/* Text of the last CUDA error seen by a call on this thread that returned
+ * RSSM_ERR_CUDA ("" if none).  Host-only. */
+RSSM_API const char *rssm_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REPLAYSSM_H_ */

@@ -1,0 +1,130 @@
+// Device helpers shared by the libreplayssm kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "replayssm.h"
+
+namespace rssm {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kThreads = 256;  // threads per CTA of the per-head kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxL = 32;  // ring capacity limit (one warp lane per entry)
+constexpr int kMaxT = 8;   // verify window limit
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------------------
+// typed loads/stores: 4 consecutive elements as a float4, scalars as float
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+__device__ __forceinline__ float4 load4(const bf16 *p) {
+  // bf16 -> f32 is exact: the bf16 bits are the high half of the f32 bits.
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
+__device__ __forceinline__ float load1(const float *p) { return *p; }
+__device__ __forceinline__ float load1(const bf16 *p) {
+  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(p)) << 16);
+}
+
+__device__ __forceinline__ void store1(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store1(bf16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ void store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+// Copy one element without changing its representation.
+template <typename T>
+__device__ __forceinline__ void copy1(T *dst, const T *src) {
+  *dst = *src;
+}
+
+// Streaming 16-byte load of checkpoint/state data that is read once per launch.
+__device__ __forceinline__ float4 ldg_stream4(const float *p) {
+  return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ void stg_stream4(float *p, float4 v) { __stcs(reinterpret_cast<float4 *>(p), v); }
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+// Sum over an aligned group of LG lanes (LG a power of two <= 32). Every lane
+// of the warp must execute the call.
+template <int LG>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = LG / 2; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Sum of V values over an aligned group of LG lanes with V-1 + log2(LG/V)
+// shuffles instead of V*log2(LG) (recursive halving).  V and LG are powers of
+// two with V <= LG.  On return x[0] of lane l holds the group total of value
+// index (l % LG) / (LG / V).
+template <int LG, int V>
+__device__ __forceinline__ void group_sum_multi(float (&x)[V], int lane) {
+  static_assert(V <= LG, "V must not exceed the group size");
+  int cnt = V;
+#pragma unroll
+  for (int off = LG / 2; off >= LG / V && off > 0; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+    const int half = cnt / 2;
+#pragma unroll
+    for (int m = 0; m < V / 2; ++m) {
+      if (m < half) {
+        const float send = upper ? x[m] : x[m + half];
+        const float keep = upper ? x[m + half] : x[m];
+        x[m] = keep + __shfl_xor_sync(kFull, send, off);
+      }
+    }
+    cnt = half;
+  }
+#pragma unroll
+  for (int off = LG / (2 * V); off > 0; off >>= 1) x[0] += __shfl_xor_sync(kFull, x[0], off);
+}
+
+__device__ __forceinline__ void set_err(int32_t *err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// Arrival counter of a sequence's thread blocks.  Every block of sequence b
+// calls this once, after it has read start/count/flag of b; it returns true
+// in exactly one block, the last to arrive, which may then rewrite the
+// pointers (no other block of this launch reads them afterwards).  The
+// counter is left at zero.
+__device__ __forceinline__ bool last_arrival(int32_t *sync, int b, int blocks_per_seq) {
+  __threadfence();
+  const int old = atomicAdd(sync + b, 1);
+  if (old == blocks_per_seq - 1) {
+    __threadfence();
+    sync[b] = 0;
+    return true;
+  }
+  return false;
+}
+
+// Suffix sums of per-entry log decays over the first p entries, one entry per
+// lane of a warp (p <= 32).  For lane j < p returns the exclusive suffix
+// sum_{m > j, m < p} la_m; `total` receives sum_{m < p} la_m.  Lanes >= p must
+// pass la = 0.
+__device__ __forceinline__ float excl_suffix_sum(float la, int lane, float &total) {
+  float incl = la;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_down_sync(kFull, incl, o);
+    if (lane + o < 32) incl += t;
+  }
+  total = __shfl_sync(kFull, incl, 0);
+  float ex = __shfl_down_sync(kFull, incl, 1);
+  if (lane == 31) ex = 0.f;
+  return ex;
+}
+
+}  // namespace rssm

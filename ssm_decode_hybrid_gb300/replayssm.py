@@ -1,0 +1,346 @@
+"""Python binding of libreplayssm (ctypes).  Argument marshalling only: every
+step of the decode path runs in the library's CUDA kernels.
+
+Tensors must be CUDA tensors on the current device, contiguous, in the
+layouts documented in ``include/replayssm.h``.  Calls are asynchronous on
+torch's current stream.  A missing library raises at import time; a non-zero
+status raises ``ReplaySSMError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libreplayssm.so")
+
+F32, BF16 = 0, 1
+EBIT_COUNT_RANGE, EBIT_WINDOW, EBIT_ACCEPTED, EBIT_CUR = 1, 2, 4, 8
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+
+
+class ReplaySSMError(RuntimeError):
+    pass
+
+
+class M2Dims(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int32) for f in ("B", "H", "G", "d", "n", "L", "in_dtype", "y_dtype")]
+
+
+class M2Replay(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_void_p) for f in
+                ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err")]
+
+
+class GdnDims(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int32) for f in ("B", "Hv", "Hk", "dk", "dv", "L", "in_dtype", "u_dtype", "y_dtype")]
+
+
+class GdnReplay(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_void_p) for f in
+                ("S0", "ring_u", "ring_k", "ring_g", "start", "count", "flag", "sync", "err")]
+
+
+EXPORTS = (
+    "ssm_state_update_baseline", "replay_decode_step", "replay_flush", "replay_spec_verify",
+    "replay_spec_commit", "ssm_spec_verify_baseline", "ssm_spec_commit_baseline",
+    "gdn_state_update_baseline", "gdn_replay_decode", "gdn_replay_flush", "gdn_replay_verify",
+    "gdn_spec_verify_baseline", "rssm_version", "rssm_status_string", "rssm_last_cuda_error",
+)
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python -m ssm_decode_hybrid_gb300.build` "
+                          "(the ReplaySSM path has no fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I = ctypes.c_void_p, ctypes.c_int32
+    sig = {
+        "ssm_state_update_baseline": [ctypes.POINTER(M2Dims), P, P, P, P, P, P, P, P],
+        "replay_decode_step": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), P, P, P, P, P, P, P],
+        "replay_flush": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), P, P],
+        "replay_spec_verify": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), I, P, P, P, P, P, P, P],
+        "replay_spec_commit": [I, I, I, P, P, P, P],
+        "ssm_spec_verify_baseline": [ctypes.POINTER(M2Dims), I, P, P, P, P, P, P, P, P, P, P],
+        "ssm_spec_commit_baseline": [I, I, P, P, P, P],
+        "gdn_state_update_baseline": [ctypes.POINTER(GdnDims), P, P, P, P, P, P, P, P],
+        "gdn_replay_decode": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), P, P, P, P, P, P, P],
+        "gdn_replay_flush": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), P],
+        "gdn_replay_verify": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), I, P, P, P, P, P, P, P],
+        "gdn_spec_verify_baseline": [ctypes.POINTER(GdnDims), I, P, P, P, P, P, P, P, P, P, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int32
+    lib.rssm_version.restype = ctypes.c_int32
+    lib.rssm_version.argtypes = []
+    lib.rssm_status_string.restype = ctypes.c_char_p
+    lib.rssm_status_string.argtypes = [ctypes.c_int32]
+    lib.rssm_last_cuda_error.restype = ctypes.c_char_p
+    lib.rssm_last_cuda_error.argtypes = []
+    return lib
+
+
+LIB = _load()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = LIB.rssm_status_string(status).decode()
+        if status == -3:
+            msg += ": " + LIB.rssm_last_cuda_error().decode()
+        raise ReplaySSMError(f"{what} failed ({status}): {msg}")
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _f32(t: torch.Tensor, name: str):
+    if t.dtype != torch.float32:
+        raise ValueError(f"{name} must be float32")
+
+
+def _i32(t: torch.Tensor, name: str):
+    if t.dtype != torch.int32:
+        raise ValueError(f"{name} must be int32")
+
+
+# ---------------------------------------------------------------------------
+# state containers
+# ---------------------------------------------------------------------------
+
+
+@dataclasses.dataclass
+class Mamba2State:
+    """Checkpoint + ring buffer of one Mamba-2 layer (device tensors)."""
+
+    S0: torch.Tensor  # [B,H,d,n] f32
+    ring_v: torch.Tensor  # [B,H,L,d] in dtype
+    ring_k: torch.Tensor  # [B,G,L,n] in dtype
+    ring_dt: torch.Tensor  # [B,H,L] f32
+    start: torch.Tensor  # [B] i32
+    count: torch.Tensor  # [B] i32
+    flag: torch.Tensor  # [B] i32
+    sync: torch.Tensor  # [B] i32, zero
+    err: torch.Tensor  # [1] i32
+
+    @classmethod
+    def empty(cls, B, H, G, d, n, L, dtype=torch.bfloat16, device="cuda"):
+        z = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt, device=device)  # noqa: E731
+        return cls(z(B, H, d, n), z(B, H, L, d, dt=dtype), z(B, G, L, n, dt=dtype), z(B, H, L),
+                   z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32),
+                   z(1, dt=torch.int32))
+
+    @property
+    def shape(self):
+        B, H, d, n = self.S0.shape
+        return B, H, self.ring_k.shape[1], d, n, self.ring_v.shape[2]
+
+    def dims(self, y_dtype=torch.float32) -> M2Dims:
+        B, H, G, d, n, L = self.shape
+        return M2Dims(B, H, G, d, n, L, _dt(self.ring_v), _DT[y_dtype])
+
+    def struct(self) -> M2Replay:
+        _f32(self.S0, "S0")
+        _f32(self.ring_dt, "ring_dt")
+        for name in ("start", "count", "flag", "sync", "err"):
+            _i32(getattr(self, name), name)
+        return M2Replay(*(_ptr(getattr(self, f)) for f in
+                          ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err")))
+
+
+@dataclasses.dataclass
+class GdnState:
+    """Checkpoint + ring buffer of cached corrections of one GDN layer."""
+
+    S0: torch.Tensor  # [B,Hv,dv,dk] f32
+    ring_u: torch.Tensor  # [B,Hv,L,dv] u dtype
+    ring_k: torch.Tensor  # [B,Hk,L,dk] in dtype
+    ring_g: torch.Tensor  # [B,Hv,L] f32
+    start: torch.Tensor
+    count: torch.Tensor
+    flag: torch.Tensor
+    sync: torch.Tensor
+    err: torch.Tensor
+
+    @classmethod
+    def empty(cls, B, Hv, Hk, dk, dv, L, dtype=torch.bfloat16, u_dtype=torch.float32, device="cuda"):
+        z = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt, device=device)  # noqa: E731
+        return cls(z(B, Hv, dv, dk), z(B, Hv, L, dv, dt=u_dtype), z(B, Hk, L, dk, dt=dtype), z(B, Hv, L),
+                   z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32),
+                   z(1, dt=torch.int32))
+
+    @property
+    def shape(self):
+        B, Hv, dv, dk = self.S0.shape
+        return B, Hv, self.ring_k.shape[1], dk, dv, self.ring_u.shape[2]
+
+    def dims(self, y_dtype=torch.float32) -> GdnDims:
+        B, Hv, Hk, dk, dv, L = self.shape
+        return GdnDims(B, Hv, Hk, dk, dv, L, _dt(self.ring_k), _dt(self.ring_u), _DT[y_dtype])
+
+    def struct(self) -> GdnReplay:
+        _f32(self.S0, "S0")
+        _f32(self.ring_g, "ring_g")
+        for name in ("start", "count", "flag", "sync", "err"):
+            _i32(getattr(self, name), name)
+        return GdnReplay(*(_ptr(getattr(self, f)) for f in
+                           ("S0", "ring_u", "ring_k", "ring_g", "start", "count", "flag", "sync", "err")))
+
+
+# ---------------------------------------------------------------------------
+# Mamba-2 calls
+# ---------------------------------------------------------------------------
+
+
+def _out(y, shape, dtype, device):
+    if y is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return y
+
+
+def ssm_state_update_baseline(S, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+    """Baseline decode step: S <- a S + dt v k^T in place, returns y = S q."""
+    _f32(S, "S")
+    B, H, d, n = S.shape
+    G = k.shape[1]
+    y = _out(y, (B, H, d), y_dtype, S.device)
+    dims = M2Dims(B, H, G, d, n, 1, _dt(v), _dt(y))
+    _check(LIB.ssm_state_update_baseline(ctypes.byref(dims), _ptr(S), _ptr(v), _ptr(k), _ptr(q), _ptr(dt), _ptr(A),
+                                         _ptr(y), _stream()), "ssm_state_update_baseline")
+    return y
+
+
+def replay_decode_step(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+    B, H, G, d, n, L = state.shape
+    y = _out(y, (B, H, d), y_dtype, state.S0.device)
+    dims = state.dims(y.dtype)
+    st = state.struct()
+    _check(LIB.replay_decode_step(ctypes.byref(dims), ctypes.byref(st), _ptr(v), _ptr(k), _ptr(q), _ptr(dt), _ptr(A),
+                                  _ptr(y), _stream()), "replay_decode_step")
+    return y
+
+
+def replay_flush(state: Mamba2State, A):
+    dims = state.dims()
+    st = state.struct()
+    _check(LIB.replay_flush(ctypes.byref(dims), ctypes.byref(st), _ptr(A), _stream()), "replay_flush")
+
+
+def replay_spec_verify(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+    """v [B,T,H,d]; k, q [B,T,G,n]; dt [B,T,H]; returns y [B,T,H,d]."""
+    B, H, G, d, n, L = state.shape
+    T = v.shape[1]
+    y = _out(y, (B, T, H, d), y_dtype, state.S0.device)
+    dims = state.dims(y.dtype)
+    st = state.struct()
+    _check(LIB.replay_spec_verify(ctypes.byref(dims), ctypes.byref(st), T, _ptr(v), _ptr(k), _ptr(q), _ptr(dt),
+                                  _ptr(A), _ptr(y), _stream()), "replay_spec_verify")
+    return y
+
+
+def replay_spec_commit(accepted, count, T: int, L: int, err=None):
+    _i32(accepted, "accepted")
+    _i32(count, "count")
+    _check(LIB.replay_spec_commit(count.shape[0], T, L, _ptr(accepted), _ptr(count), _ptr(err), _stream()),
+           "replay_spec_commit")
+
+
+def ssm_spec_verify_baseline(slots, cur, v, k, q, dt, A, y=None, err=None, y_dtype=torch.float32):
+    """slots [B,T+1,H,d,n] f32; cur [B] i32; inputs as replay_spec_verify."""
+    _f32(slots, "slots")
+    B, T1, H, d, n = slots.shape
+    T = T1 - 1
+    G = k.shape[2]
+    y = _out(y, (B, T, H, d), y_dtype, slots.device)
+    dims = M2Dims(B, H, G, d, n, 1, _dt(v), _dt(y))
+    _check(LIB.ssm_spec_verify_baseline(ctypes.byref(dims), T, _ptr(slots), _ptr(cur), _ptr(v), _ptr(k), _ptr(q),
+                                        _ptr(dt), _ptr(A), _ptr(y), _ptr(err), _stream()), "ssm_spec_verify_baseline")
+    return y
+
+
+def ssm_spec_commit_baseline(accepted, cur, T: int, err=None):
+    _check(LIB.ssm_spec_commit_baseline(cur.shape[0], T, _ptr(accepted), _ptr(cur), _ptr(err), _stream()),
+           "ssm_spec_commit_baseline")
+
+
+# ---------------------------------------------------------------------------
+# GDN calls
+# ---------------------------------------------------------------------------
+
+
+def gdn_state_update_baseline(S, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+    _f32(S, "S")
+    B, Hv, dv, dk = S.shape
+    Hk = k.shape[1]
+    y = _out(y, (B, Hv, dv), y_dtype, S.device)
+    dims = GdnDims(B, Hv, Hk, dk, dv, 1, _dt(k), F32, _dt(y))
+    _check(LIB.gdn_state_update_baseline(ctypes.byref(dims), _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                         _ptr(y), _stream()), "gdn_state_update_baseline")
+    return y
+
+
+def gdn_replay_decode(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+    B, Hv, Hk, dk, dv, L = state.shape
+    y = _out(y, (B, Hv, dv), y_dtype, state.S0.device)
+    dims = state.dims(y.dtype)
+    st = state.struct()
+    _check(LIB.gdn_replay_decode(ctypes.byref(dims), ctypes.byref(st), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                 _ptr(y), _stream()), "gdn_replay_decode")
+    return y
+
+
+def gdn_replay_flush(state: GdnState):
+    dims = state.dims()
+    st = state.struct()
+    _check(LIB.gdn_replay_flush(ctypes.byref(dims), ctypes.byref(st), _stream()), "gdn_replay_flush")
+
+
+def gdn_replay_verify(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+    """q, k [B,T,Hk,dk]; v [B,T,Hv,dv]; beta, g [B,T,Hv]; returns y [B,T,Hv,dv]."""
+    B, Hv, Hk, dk, dv, L = state.shape
+    T = v.shape[1]
+    y = _out(y, (B, T, Hv, dv), y_dtype, state.S0.device)
+    dims = state.dims(y.dtype)
+    st = state.struct()
+    _check(LIB.gdn_replay_verify(ctypes.byref(dims), ctypes.byref(st), T, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                 _ptr(g), _ptr(y), _stream()), "gdn_replay_verify")
+    return y
+
+
+def gdn_spec_verify_baseline(slots, cur, q, k, v, beta, g, y=None, err=None, y_dtype=torch.float32):
+    _f32(slots, "slots")
+    B, T1, Hv, dv, dk = slots.shape
+    T = T1 - 1
+    Hk = k.shape[2]
+    y = _out(y, (B, T, Hv, dv), y_dtype, slots.device)
+    dims = GdnDims(B, Hv, Hk, dk, dv, 1, _dt(k), F32, _dt(y))
+    _check(LIB.gdn_spec_verify_baseline(ctypes.byref(dims), T, _ptr(slots), _ptr(cur), _ptr(q), _ptr(k), _ptr(v),
+                                        _ptr(beta), _ptr(g), _ptr(y), _ptr(err), _stream()),
+           "gdn_spec_verify_baseline")
+    return y
+
+
+def version() -> int:
+    return int(LIB.rssm_version())

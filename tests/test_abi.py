@@ -1,0 +1,99 @@
+"""The C-ABI library loads, exports every symbol its header declares, and
+rejects bad arguments on the host before any launch (CPU only: no kernel runs)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "replayssm.h")
+
+
+def _lib_path():
+    from ssm_decode_hybrid_gb300 import build
+
+    if not os.path.exists(build.LIB):
+        build.build()
+    return build.LIB
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"^RSSM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_symbols())
+    for required in ("ssm_state_update_baseline", "replay_decode_step", "replay_flush", "replay_spec_verify",
+                     "replay_spec_commit", "gdn_replay_decode", "gdn_replay_flush", "gdn_replay_verify"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(_lib_path())
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"missing export {name}"
+
+
+def test_binding_covers_exports():
+    _lib_path()
+    from ssm_decode_hybrid_gb300 import replayssm as R
+
+    assert set(declared_symbols()) == set(R.EXPORTS)
+    assert R.version() == 100
+    assert R.LIB.rssm_status_string(-1) == b"invalid argument"
+    assert R.LIB.rssm_status_string(-2) == b"unsupported shape or dtype"
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-validation test uses fake device pointers; CPU only")
+def test_host_validation_rejects_bad_arguments():
+    _lib_path()
+    from ssm_decode_hybrid_gb300 import replayssm as R
+
+    L = R.LIB
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # aligned, never dereferenced: every call below fails validation first
+    mis = P(0x10004)  # 4-byte but not 16-byte aligned
+
+    def dims(**kw):
+        base = dict(B=2, H=4, G=2, d=64, n=128, L=16, in_dtype=R.BF16, y_dtype=R.F32)
+        base.update(kw)
+        return R.M2Dims(*base.values())
+
+    rep = R.M2Replay(*([fake] * 9))
+    args = [fake, fake, fake, fake, fake, fake, None]
+    assert L.replay_decode_step(None, ctypes.byref(rep), *args) == -1
+    assert L.replay_decode_step(ctypes.byref(dims(H=3)), ctypes.byref(rep), *args) == -1  # H % G
+    assert L.replay_decode_step(ctypes.byref(dims(n=96)), ctypes.byref(rep), *args) == -2
+    assert L.replay_decode_step(ctypes.byref(dims(d=66)), ctypes.byref(rep), *args) == -2
+    assert L.replay_decode_step(ctypes.byref(dims(L=33)), ctypes.byref(rep), *args) == -2
+    assert L.replay_decode_step(ctypes.byref(dims(in_dtype=7)), ctypes.byref(rep), *args) == -1
+    assert L.replay_decode_step(ctypes.byref(dims(B=0)), ctypes.byref(rep), *args) == -1
+    assert L.replay_decode_step(ctypes.byref(dims()), None, *args) == -1
+    bad = R.M2Replay(mis, *([fake] * 8))  # misaligned S0
+    assert L.replay_decode_step(ctypes.byref(dims()), ctypes.byref(bad), *args) == -1
+    nosync = R.M2Replay(*([fake] * 7), None, fake)
+    assert L.replay_decode_step(ctypes.byref(dims()), ctypes.byref(nosync), *args) == -1
+    assert L.replay_flush(ctypes.byref(dims()), ctypes.byref(nosync), fake, None) == -1
+    # verify: T out of range
+    vargs = [fake, fake, fake, fake, fake, fake, None]
+    assert L.replay_spec_verify(ctypes.byref(dims()), ctypes.byref(rep), 0, *vargs) == -1
+    assert L.replay_spec_verify(ctypes.byref(dims(L=4)), ctypes.byref(rep), 5, *vargs) == -1
+    assert L.replay_spec_verify(ctypes.byref(dims()), ctypes.byref(rep), 9, *vargs) == -2
+    assert L.replay_spec_commit(2, 5, 4, fake, fake, None, None) == -1  # T > L
+    assert L.replay_spec_commit(0, 1, 4, fake, fake, None, None) == -1
+    assert L.ssm_spec_commit_baseline(2, 0, fake, fake, None, None) == -1
+    # baseline: misaligned k
+    assert L.ssm_state_update_baseline(ctypes.byref(dims()), fake, fake, mis, fake, fake, fake, fake, None) == -1
+
+    gd = R.GdnDims(2, 4, 2, 128, 128, 16, R.BF16, R.F32, R.F32)
+    grep = R.GdnReplay(*([fake] * 9))
+    gargs = [fake, fake, fake, fake, fake, fake, None]
+    bad_g = R.GdnDims(2, 4, 3, 128, 128, 16, R.BF16, R.F32, R.F32)  # Hv % Hk
+    assert L.gdn_replay_decode(ctypes.byref(bad_g), ctypes.byref(grep), *gargs) == -1
+    bad_g = R.GdnDims(2, 4, 2, 256, 128, 16, R.BF16, R.F32, R.F32)  # dk unsupported
+    assert L.gdn_replay_decode(ctypes.byref(bad_g), ctypes.byref(grep), *gargs) == -2
+    assert L.gdn_replay_verify(ctypes.byref(gd), ctypes.byref(grep), 17, *gargs) == -1
+    assert L.gdn_replay_flush(ctypes.byref(gd), None, None) == -1

@@ -1,0 +1,161 @@
+"""GPU parity of the Gated DeltaNet kernels against the fp64 oracle (through the C ABI).
+
+Outputs: |gpu - ref| <= max(1e-3 |ref|, 1e-4) with the buffer's u in fp32,
+max(1e-2 |ref|, 1e-3) with bf16 u or bf16 outputs.  Bookkeeping bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_close, dev, gdn_state, gdn_step_dev, host, take, tol_for
+from oracle import gdn as og
+from ssm_decode_hybrid_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def rs():
+    from ssm_decode_hybrid_gb300 import replayssm
+
+    return replayssm
+
+
+def oracle_replay(init, idx):
+    return og.GdnReplay(take(init.S0, idx), take(init.ring_u, idx), take(init.ring_k, idx), take(init.ring_g, idx),
+                        take(init.start, idx), take(init.count, idx), u_dtype=init.shape.u_dtype)
+
+
+def check_pointers(state, orc, idx, what):
+    np.testing.assert_array_equal(host(state.start)[idx], orc.start, err_msg=f"{what}: start")
+    np.testing.assert_array_equal(host(state.count)[idx], orc.count, err_msg=f"{what}: count")
+    np.testing.assert_array_equal(host(state.flag)[idx], orc.flag, err_msg=f"{what}: flag")
+
+
+def run_decode(shape, seed, steps, sample=None, y_dtype=torch.float32):
+    R = rs()
+    init = wl.gdn_init(shape, seed)
+    idx = np.arange(shape.B) if sample is None else np.asarray(sample)
+    state = gdn_state(init)
+    orc = oracle_replay(init, idx)
+    rtol, atol = tol_for(y_dtype)
+    if shape.u_dtype == wl.BF16:
+        rtol, atol = max(rtol, 1e-2), max(atol, 1e-3)
+    for t in range(steps):
+        st = wl.gdn_step(shape, seed, t)
+        y = R.gdn_replay_decode(state, *gdn_step_dev(st, shape.in_dtype), y_dtype=y_dtype)
+        flags = host(state.flag)
+        R.gdn_replay_flush(state)
+        y_ref = orc.decode_step(take(st.q, idx), take(st.k, idx), take(st.v, idx), take(st.beta, idx),
+                                take(st.g, idx))
+        np.testing.assert_array_equal(flags[idx], orc.flag, err_msg=f"step {t}: flag")
+        orc.flush()
+        assert_close(y[idx], y_ref, rtol, atol, what=f"step {t}: y")
+        check_pointers(state, orc, idx, f"step {t}")
+    assert_close(state.S0[idx], orc.S0, rtol, atol, what="final S0")
+    assert int(host(state.err)[0]) == 0
+    assert int(host(state.sync).sum()) == 0
+
+
+SHAPES = [
+    wl.GdnShape(B=3, Hv=4, Hk=2, dk=16, dv=16, L=4, in_dtype=wl.F32),
+    wl.GdnShape(B=4, Hv=6, Hk=3, dk=32, dv=20, L=5, in_dtype=wl.BF16),
+    wl.GdnShape(B=3, Hv=4, Hk=4, dk=64, dv=68, L=7, in_dtype=wl.BF16),
+    wl.GdnShape(B=4, Hv=8, Hk=4, dk=128, dv=128, L=16, in_dtype=wl.BF16),  # the GDN layer, small batch
+    wl.GdnShape(B=2, Hv=2, Hk=1, dk=128, dv=136, L=1, in_dtype=wl.F32),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{s.B}Hv{s.Hv}Hk{s.Hk}dk{s.dk}dv{s.dv}L{s.L}{s.in_dtype}")
+def test_decode_parity(shape):
+    run_decode(shape, 200, steps=2 * shape.L + 3)
+
+
+def test_decode_bf16_u_and_bf16_y():
+    shape = wl.GdnShape(B=4, Hv=8, Hk=4, dk=128, dv=128, L=8, in_dtype=wl.BF16, u_dtype=wl.BF16)
+    run_decode(shape, 201, steps=12, y_dtype=torch.bfloat16)
+
+
+def test_gdn_layer_full_batch_sampled():
+    """Batch 256, 32 value heads over 16 key heads, d_k = d_v = 128, L = 16."""
+    run_decode(wl.GDN_LAYER, wl.SEED_GDN, steps=40, sample=[0, 77, 200, 255])
+
+
+def test_baseline_parity():
+    shape = wl.GdnShape(B=8, Hv=8, Hk=4, dk=128, dv=128, L=16, in_dtype=wl.BF16)
+    R = rs()
+    init = wl.gdn_init(shape, 202, fill_max=0)
+    S = dev(init.S0)
+    S_ref = init.S0.astype(np.float64)
+    state = gdn_state(init)
+    for t in range(24):
+        st = wl.gdn_step(shape, 202, t)
+        inp = gdn_step_dev(st, shape.in_dtype)
+        y = R.gdn_state_update_baseline(S, *inp)
+        y_rep = R.gdn_replay_decode(state, *inp)
+        R.gdn_replay_flush(state)
+        S_ref, y_ref, _ = og.rank1_step(S_ref, st.q, st.k, st.v, st.beta, st.g)
+        assert_close(y, y_ref, what=f"baseline step {t}")
+        assert_close(y_rep, y_ref, what=f"replay step {t}")
+    assert_close(S, S_ref, what="baseline state")
+
+
+def run_verify(shape, T, rounds, seed, sample=None):
+    R = rs()
+    init = wl.gdn_init(shape, seed, fill_max=shape.L - T)
+    idx = np.arange(shape.B) if sample is None else np.asarray(sample)
+    state = gdn_state(init)
+    orc = oracle_replay(init, idx)
+    for r in range(rounds):
+        st = wl.gdn_step(shape, seed, r, T=T)
+        acc = wl.accepted_counts(shape.B, T, seed, r)
+        y = R.gdn_replay_verify(state, *gdn_step_dev(st, shape.in_dtype))
+        Y_ref = orc.verify(take(st.q, idx), take(st.k, idx), take(st.v, idx), take(st.beta, idx), take(st.g, idx))
+        np.testing.assert_array_equal(host(state.flag)[idx], orc.flag, err_msg=f"round {r}: flag")
+        assert_close(y[idx], Y_ref, what=f"round {r}: y")
+        R.replay_spec_commit(dev(acc, torch.int32), state.count, T, shape.L, state.err)
+        orc.commit(take(acc, idx), T)
+        R.gdn_replay_flush(state)
+        orc.flush()
+        check_pointers(state, orc, idx, f"round {r}")
+    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 6, 8])
+def test_chunked_verify_parity(T):
+    shape = wl.GdnShape(B=8, Hv=8, Hk=4, dk=128, dv=128, L=16, in_dtype=wl.BF16)
+    run_verify(shape, T, rounds=10, seed=300 + T)
+
+
+def test_chunked_verify_small_shapes():
+    run_verify(wl.GdnShape(B=4, Hv=4, Hk=2, dk=16, dv=16, L=6, in_dtype=wl.F32), 3, rounds=10, seed=310)
+    run_verify(wl.GdnShape(B=4, Hv=6, Hk=3, dk=64, dv=36, L=9, in_dtype=wl.BF16), 4, rounds=10, seed=311)
+
+
+def test_chunked_verify_full_batch_sampled():
+    """Batch 256, T = 4, accepted ~ U{0..4}: sampled sequences."""
+    run_verify(wl.GDN_LAYER, 4, rounds=16, seed=wl.SEED_GDN + 50, sample=[1, 99, 254])
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_snapshot_baseline_parity(T):
+    shape = wl.GdnShape(B=4, Hv=8, Hk=4, dk=128, dv=128, L=16, in_dtype=wl.BF16)
+    R = rs()
+    init = wl.gdn_init(shape, 320 + T, fill_max=0)
+    slots = torch.zeros(shape.B, T + 1, shape.Hv, shape.dv, shape.dk, device="cuda")
+    slots[:, 0] = dev(init.S0)
+    cur = torch.zeros(shape.B, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    base = og.GdnSnapshotBaseline(init.S0, T)
+    for r in range(6):
+        st = wl.gdn_step(shape, 320 + T, r, T=T)
+        y = R.gdn_spec_verify_baseline(slots, cur, *gdn_step_dev(st, shape.in_dtype), err=err)
+        Y_ref = base.verify(st.q, st.k, st.v, st.beta, st.g)
+        assert_close(y, Y_ref, what=f"round {r}")
+        acc = wl.accepted_counts(shape.B, T, 320 + T, r)
+        R.ssm_spec_commit_baseline(dev(acc, torch.int32), cur, T, err)
+        base.commit(acc)
+        np.testing.assert_array_equal(host(cur), base.cur)
+    for b in range(shape.B):
+        assert_close(slots[b, int(base.cur[b])], base.state(b), what=f"state {b}")
+    assert int(host(err)[0]) == 0

@@ -1,0 +1,285 @@
+"""GPU parity of the Mamba-2 kernels against the fp64 oracle (through the C ABI).
+
+Outputs: |gpu - ref| <= max(1e-3 |ref|, 1e-4) (fp32 y), max(1e-2 |ref|, 1e-3)
+(bf16 y).  start/count/flag and the error word: bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import (assert_close, dev, host, m2_state, m2_step_dev, take, tol_for)
+from oracle import mamba2 as om
+from ssm_decode_hybrid_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def rs():
+    from ssm_decode_hybrid_gb300 import replayssm
+
+    return replayssm
+
+
+def oracle_replay(init, idx):
+    return om.Mamba2Replay(take(init.S0, idx), init.A, take(init.ring_v, idx), take(init.ring_k, idx),
+                           take(init.ring_dt, idx), take(init.start, idx), take(init.count, idx))
+
+
+def check_pointers(state, orc, idx, what):
+    np.testing.assert_array_equal(host(state.start)[idx], orc.start, err_msg=f"{what}: start")
+    np.testing.assert_array_equal(host(state.count)[idx], orc.count, err_msg=f"{what}: count")
+    np.testing.assert_array_equal(host(state.flag)[idx], orc.flag, err_msg=f"{what}: flag")
+
+
+def run_decode(shape, seed, steps, sample=None, y_dtype=torch.float32, check_every=1):
+    R = rs()
+    init = wl.mamba2_init(shape, seed)
+    idx = np.arange(shape.B) if sample is None else np.asarray(sample)
+    state = m2_state(init)
+    orc = oracle_replay(init, idx)
+    A = dev(init.A)
+    rtol, atol = tol_for(y_dtype)
+    for t in range(steps):
+        st = wl.mamba2_step(shape, seed, t)
+        v, k, q, dt = m2_step_dev(st, shape.in_dtype)
+        y = R.replay_decode_step(state, v, k, q, dt, A, y_dtype=y_dtype)
+        flags_after_decode = host(state.flag)
+        R.replay_flush(state, A)
+        y_ref = orc.decode_step(take(st.v, idx), take(st.k, idx), take(st.q, idx), take(st.dt, idx))
+        np.testing.assert_array_equal(flags_after_decode[idx], orc.flag, err_msg=f"step {t}: flag")
+        orc.flush()
+        if t % check_every == 0 or t == steps - 1:
+            assert_close(y[idx], y_ref, rtol, atol, what=f"step {t}: y")
+            check_pointers(state, orc, idx, f"step {t}")
+    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0
+    assert int(host(state.sync).sum()) == 0
+    return state, orc
+
+
+def test_tiny_config_parity():
+    """Tiny Mamba-2 decode (batch 1, 4 heads, d = n = 16, L = 4, fp32), 32 steps."""
+    run_decode(wl.TINY_MAMBA2, wl.SEED_TINY, steps=32)
+
+
+SHAPES = [
+    wl.Mamba2Shape(B=3, H=4, G=2, d=16, n=16, L=4, in_dtype=wl.F32),
+    wl.Mamba2Shape(B=5, H=6, G=3, d=20, n=32, L=3, in_dtype=wl.BF16),
+    wl.Mamba2Shape(B=4, H=8, G=2, d=68, n=64, L=7, in_dtype=wl.BF16),  # ragged rows
+    wl.Mamba2Shape(B=3, H=4, G=1, d=136, n=128, L=32, in_dtype=wl.BF16),  # two row chunks + tail
+    wl.Mamba2Shape(B=2, H=2, G=2, d=4, n=128, L=1, in_dtype=wl.F32),  # flush every step
+    wl.Mamba2Shape(B=6, H=32, G=8, d=64, n=128, L=16, in_dtype=wl.BF16),  # the Nemotron-H layer, small batch
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{s.B}H{s.H}G{s.G}d{s.d}n{s.n}L{s.L}{s.in_dtype}")
+def test_decode_parity(shape):
+    run_decode(shape, seed=123, steps=2 * shape.L + 3)
+
+
+def test_decode_bf16_output():
+    run_decode(wl.Mamba2Shape(B=4, H=8, G=2, d=64, n=128, L=8, in_dtype=wl.BF16), 77, steps=12,
+               y_dtype=torch.bfloat16)
+
+
+def test_nemotron_layer_full_batch_sampled():
+    """Batch 256, 32 heads, d=64, n=128, G=8, L=16, random fill levels: 48 steps
+    (three flush cycles per sequence); sampled sequences against the oracle,
+    bookkeeping of every sequence against its closed form."""
+    shape = wl.NEMOTRON_H_MAMBA2
+    R = rs()
+    init = wl.mamba2_init(shape, wl.SEED_NEMOTRON)
+    idx = np.array([0, 37, 128, 255])
+    state = m2_state(init)
+    orc = oracle_replay(init, idx)
+    A = dev(init.A)
+    start0, count0 = init.start.astype(np.int64), init.count.astype(np.int64)
+    for t in range(48):
+        st = wl.mamba2_step(shape, wl.SEED_NEMOTRON, t)
+        y = R.replay_decode_step(state, *m2_step_dev(st, shape.in_dtype), A)
+        R.replay_flush(state, A)
+        y_ref = orc.decode_step(take(st.v, idx), take(st.k, idx), take(st.q, idx), take(st.dt, idx))
+        orc.flush()
+        assert_close(y[idx], y_ref, what=f"step {t}")
+        # every sequence: after t+1 steps, total = count0 + t + 1 entries went through
+        tot = count0 + t + 1
+        np.testing.assert_array_equal(host(state.count), tot % shape.L)
+        np.testing.assert_array_equal(host(state.start), (start0 + (tot // shape.L) * shape.L) % shape.L)
+    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0
+
+
+def test_replay_matches_baseline_kernel():
+    """The replay path and the baseline kernel agree on the same inputs, and
+    the baseline matches the plain recurrence."""
+    shape = wl.Mamba2Shape(B=16, H=32, G=8, d=64, n=128, L=16, in_dtype=wl.BF16)
+    R = rs()
+    init = wl.mamba2_init(shape, 9, fill_max=0)
+    state = m2_state(init)
+    S = dev(init.S0)
+    A = dev(init.A)
+    S_ref = init.S0.astype(np.float64)
+    for t in range(40):
+        st = wl.mamba2_step(shape, 9, t)
+        inp = m2_step_dev(st, shape.in_dtype)
+        y_rep = R.replay_decode_step(state, *inp, A)
+        R.replay_flush(state, A)
+        y_base = R.ssm_state_update_baseline(S, *inp, A)
+        S_ref, y_ref = om.recurrence_step(S_ref, st.v, st.k, st.q, st.dt, init.A)
+        assert_close(y_base, y_ref, what=f"baseline step {t}")
+        assert_close(y_rep, y_ref, what=f"replay step {t}")
+    assert_close(S, S_ref, what="baseline state")
+
+
+def test_baseline_tiny_and_bf16_out():
+    shape = wl.TINY_MAMBA2
+    R = rs()
+    init = wl.mamba2_init(shape, 5, fill_max=0)
+    S = dev(init.S0)
+    S_ref = init.S0.astype(np.float64)
+    for t in range(32):
+        st = wl.mamba2_step(shape, 5, t)
+        y = R.ssm_state_update_baseline(S, *m2_step_dev(st, shape.in_dtype), dev(init.A),
+                                        y_dtype=torch.bfloat16 if t % 2 else torch.float32)
+        S_ref, y_ref = om.recurrence_step(S_ref, st.v, st.k, st.q, st.dt, init.A)
+        assert_close(y, y_ref, *tol_for(y.dtype), what=f"step {t}")
+
+
+def test_flush_anywhere_gpu():
+    """Forcing flushes at random steps (flag written from the host) leaves every
+    output unchanged."""
+    shape = wl.Mamba2Shape(B=8, H=8, G=2, d=32, n=64, L=8, in_dtype=wl.BF16)
+    R = rs()
+    init = wl.mamba2_init(shape, 31)
+    s1, s2 = m2_state(init), m2_state(init)
+    A = dev(init.A)
+    rng = np.random.default_rng(31)
+    for t in range(20):
+        inp = m2_step_dev(wl.mamba2_step(shape, 31, t), shape.in_dtype)
+        y1 = R.replay_decode_step(s1, *inp, A)
+        R.replay_flush(s1, A)
+        y2 = R.replay_decode_step(s2, *inp, A)
+        force = torch.from_numpy((rng.random(shape.B) < 0.4).astype(np.int32)).cuda()
+        s2.flag.copy_(torch.maximum(s2.flag, force))
+        R.replay_flush(s2, A)
+        assert_close(y2, host(y1), what=f"step {t}")
+
+
+def run_spec(shape, T, rounds, seed, sample=None):
+    R = rs()
+    init = wl.mamba2_init(shape, seed, fill_max=shape.L - T)
+    idx = np.arange(shape.B) if sample is None else np.asarray(sample)
+    state = m2_state(init)
+    orc = oracle_replay(init, idx)
+    A = dev(init.A)
+    for r in range(rounds):
+        st = wl.mamba2_step(shape, seed, r, T=T)
+        acc = wl.accepted_counts(shape.B, T, seed, r)
+        y = R.replay_spec_verify(state, *m2_step_dev(st, shape.in_dtype), A)
+        Y_ref = orc.spec_verify(take(st.v, idx), take(st.k, idx), take(st.q, idx), take(st.dt, idx))
+        np.testing.assert_array_equal(host(state.flag)[idx], orc.flag, err_msg=f"round {r}: flag")
+        assert_close(y[idx], Y_ref, what=f"round {r}: y")
+        R.replay_spec_commit(dev(acc, torch.int32), state.count, T, shape.L, state.err)
+        orc.commit(take(acc, idx), T)
+        R.replay_flush(state, A)
+        orc.flush()
+        check_pointers(state, orc, idx, f"round {r}")
+    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8])
+def test_spec_verify_parity(T):
+    shape = wl.Mamba2Shape(B=12, H=8, G=2, d=64, n=128, L=16, in_dtype=wl.BF16)
+    run_spec(shape, T, rounds=12, seed=40 + T)
+
+
+def test_spec_verify_small_shapes():
+    run_spec(wl.Mamba2Shape(B=5, H=4, G=1, d=16, n=16, L=6, in_dtype=wl.F32), 3, rounds=10, seed=3)
+    run_spec(wl.Mamba2Shape(B=5, H=6, G=3, d=36, n=32, L=9, in_dtype=wl.BF16), 4, rounds=10, seed=4)
+
+
+def test_spec_full_batch_sampled():
+    """Batch 512, T = 4, L = 16, accepted ~ U{0..4}: sampled sequences."""
+    run_spec(wl.SPEC_MAMBA2, 4, rounds=24, seed=wl.SEED_SPEC, sample=[0, 100, 311, 511])
+
+
+@pytest.mark.parametrize("T", [1, 4, 6])
+def test_snapshot_baseline_parity(T):
+    shape = wl.Mamba2Shape(B=6, H=8, G=2, d=64, n=128, L=16, in_dtype=wl.BF16)
+    R = rs()
+    init = wl.mamba2_init(shape, 60 + T, fill_max=0)
+    slots = torch.zeros(shape.B, T + 1, shape.H, shape.d, shape.n, device="cuda")
+    slots[:, 0] = dev(init.S0)
+    cur = torch.zeros(shape.B, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    base = om.Mamba2SnapshotBaseline(init.S0, init.A, T)
+    A = dev(init.A)
+    for r in range(8):
+        st = wl.mamba2_step(shape, 60 + T, r, T=T)
+        y = R.ssm_spec_verify_baseline(slots, cur, *m2_step_dev(st, shape.in_dtype), A, err=err)
+        Y_ref = base.verify(st.v, st.k, st.q, st.dt)
+        assert_close(y, Y_ref, what=f"round {r}")
+        acc = wl.accepted_counts(shape.B, T, 60 + T, r)
+        R.ssm_spec_commit_baseline(dev(acc, torch.int32), cur, T, err)
+        base.commit(acc)
+        np.testing.assert_array_equal(host(cur), base.cur)
+    for b in range(shape.B):
+        assert_close(slots[b, int(base.cur[b])], base.state(b), what=f"state {b}")
+    assert int(host(err)[0]) == 0
+
+
+def test_device_error_bits():
+    """Out-of-range bookkeeping sets the sticky error word and skips only the
+    offending sequence; nothing faults."""
+    shape = wl.Mamba2Shape(B=4, H=4, G=2, d=32, n=64, L=8, in_dtype=wl.BF16)
+    R = rs()
+    init = wl.mamba2_init(shape, 70)
+    init.count[:] = [8, 2, -1, 3]  # 8 == L and -1 are out of range
+    state = m2_state(init)
+    A = dev(init.A)
+    st = wl.mamba2_step(shape, 70, 0)
+    y = torch.full((shape.B, shape.H, shape.d), float("nan"), device="cuda")
+    R.replay_decode_step(state, *m2_step_dev(st, shape.in_dtype), A, y=y)
+    torch.cuda.synchronize()
+    assert int(host(state.err)[0]) == R.EBIT_COUNT_RANGE
+    np.testing.assert_array_equal(host(state.count), [8, 3, -1, 4])
+    yh = host(y)
+    assert np.all(np.isnan(yh[[0, 2]])) and np.all(np.isfinite(yh[[1, 3]]))
+    assert int(host(state.sync).sum()) == 0
+    # verify window that does not fit, then an accepted count out of range
+    state.err.zero_()
+    state.count.copy_(dev(np.array([7, 1, 2, 0]), torch.int32))
+    st4 = wl.mamba2_step(shape, 70, 1, T=2)
+    R.replay_spec_verify(state, *m2_step_dev(st4, shape.in_dtype), A)
+    torch.cuda.synchronize()
+    assert int(host(state.err)[0]) == R.EBIT_WINDOW
+    state.err.zero_()
+    R.replay_spec_commit(dev(np.array([0, 3, 1, -1]), torch.int32), state.count, 2, shape.L, state.err)
+    torch.cuda.synchronize()
+    assert int(host(state.err)[0]) == R.EBIT_ACCEPTED
+    np.testing.assert_array_equal(host(state.count), [7, 1, 3, 0])
+
+
+def test_checkpoint_resume_bit_identical():
+    """Copy the caller-owned state to the host mid-run, restore it into fresh
+    buffers, continue: outputs are bit-identical to the uninterrupted run."""
+    shape = wl.Mamba2Shape(B=8, H=8, G=2, d=64, n=128, L=8, in_dtype=wl.BF16)
+    R = rs()
+    init = wl.mamba2_init(shape, 80)
+    state = m2_state(init)
+    A = dev(init.A)
+    steps = [m2_step_dev(wl.mamba2_step(shape, 80, t), shape.in_dtype) for t in range(14)]
+    snap = None
+    ys = []
+    for t, inp in enumerate(steps):
+        if t == 5:
+            snap = {f: getattr(state, f).cpu().clone() for f in state.__dataclass_fields__}
+        ys.append(R.replay_decode_step(state, *inp, A).clone())
+        R.replay_flush(state, A)
+    restored = R.Mamba2State(**{f: v.cuda() for f, v in snap.items()})
+    for t, inp in enumerate(steps[5:], start=5):
+        y = R.replay_decode_step(restored, *inp, A)
+        R.replay_flush(restored, A)
+        assert torch.equal(y, ys[t])
+    assert torch.equal(restored.S0, state.S0)
