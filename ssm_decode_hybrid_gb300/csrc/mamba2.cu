@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) m2_replay_kernel(M2Launch a) {
   }
 
   // 3. decay weights: warp s handles query s; lane j < p_s is entry j+1
-  for (int qs = warp; qs < Q; qs += kWarps) {
+  for (int qs = warp; qs < T; qs += kWarps) {
     const int p = h + (kVerify ? qs + 1 : 1);
     float dtj = 0.f;
     if (lane < p) dtj = (lane < h) ? ring_dt[(st + lane) % L] : a.dt[in_h + static_cast<size_t>(lane - h) * a.H];
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) m2_replay_kernel(M2Launch a) {
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < Q * kMaxL; idx += kThreads) {
+  for (int idx = tid; idx < T * kMaxL; idx += kThreads) {
     const int qs = idx / kMaxL, j = idx - qs * kMaxL;
     const int p = h + (kVerify ? qs + 1 : 1);
     s_coef[qs][j] = (j < p) ? s_wt[qs][j] * s_M[qs][j] : 0.f;
