@@ -85,6 +85,7 @@ typedef int32_t rssm_status;
 #define RSSM_EBIT_WINDOW 2      /* count + T > L at a verify round                  */
 #define RSSM_EBIT_ACCEPTED 4    /* accepted outside [0, T] or count + accepted > L  */
 #define RSSM_EBIT_CUR 8         /* snapshot slot index outside [0, T]              */
+#define RSSM_EBIT_TIMEOUT 16    /* a bounded wait inside a pipelined kernel ran out */
 
 typedef struct {
   int32_t B, H, G, d, n, L;
@@ -151,6 +152,21 @@ RSSM_API rssm_status replay_decode_step(const rssm_m2_dims *dims, const rssm_m2_
  * any sequence at any time without changing later outputs.                   */
 RSSM_API rssm_status replay_flush(const rssm_m2_dims *dims, const rssm_m2_replay *st, const float *A,
                          rssm_stream_t stream);
+
+/* Decode step with the flush fused in ("Algorithm -- Mamba-2 standard decode":
+ * append, output, and if the buffer is full, flush): the same outputs as
+ * replay_decode_step followed by replay_flush, in one launch.  A sequence
+ * whose buffer fills with this token (count reaches L) has all L entries
+ * folded into S_0 from the tile this launch already holds, using this step's
+ * decay weights; it ends with count = 0 and flag = 0 (start is unchanged,
+ * since start + L = start mod L).  Other sequences end as after
+ * replay_decode_step.  Like replay_decode_step, the call overwrites every
+ * valid sequence's flag, so an early flush requested through the flag array
+ * must be carried out with replay_flush before this call.
+ * Arguments as replay_decode_step.                                            */
+RSSM_API rssm_status replay_decode_step_fused(const rssm_m2_dims *dims, const rssm_m2_replay *st, const void *v,
+                                              const void *k, const void *q, const float *dt, const float *A,
+                                              void *y, rssm_stream_t stream);
 
 /* Speculative verify of T drafts ("Algorithm -- speculative decoding"): with
  * h = count[b] (requires h + T <= L, else RSSM_EBIT_WINDOW and the sequence is

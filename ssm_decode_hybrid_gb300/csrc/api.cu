@@ -164,11 +164,43 @@ rssm_status replay_decode_step(const rssm_m2_dims *dims, const rssm_m2_replay *s
   return cuda_status(launch_m2(M2Kind::Decode, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-rssm_status replay_flush(const rssm_m2_dims *dims, const rssm_m2_replay *s, const float *A, rssm_stream_t stream) {
+static FlushLaunch m2_flush_launch(const rssm_m2_dims &d, const rssm_m2_replay *s, const float *A);
+
+rssm_status replay_decode_step_fused(const rssm_m2_dims *dims, const rssm_m2_replay *s, const void *v,
+                                     const void *k, const void *q, const float *dt, const float *A, void *y,
+                                     rssm_stream_t stream) {
   rssm_status st = check_m2_dims(dims);
   if (st) return st;
   const rssm_m2_dims &d = *dims;
-  if (!m2_replay_ok(d, s, true) || !ok4(A)) return RSSM_ERR_INVALID_ARG;
+  if (!m2_replay_ok(d, s, true) || !ok_elem(v, d.in_dtype) || !ok16(k) || !ok16(q) || !ok4(dt) || !ok4(A) ||
+      !ok_elem(y, d.y_dtype))
+    return RSSM_ERR_INVALID_ARG;
+  M2Launch a = m2_launch(d);
+  a.S = s->S0;
+  a.ring_v = s->ring_v;
+  a.ring_k = s->ring_k;
+  a.ring_dt = s->ring_dt;
+  a.start = s->start;
+  a.count = s->count;
+  a.flag = s->flag;
+  a.sync = s->sync;
+  a.err = s->err;
+  a.v = v;
+  a.k = k;
+  a.q = q;
+  a.dt = dt;
+  a.A = A;
+  a.y = y;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_m2(M2Kind::DecodeFused, a, cs);
+  if (e != cudaErrorNotSupported) return cuda_status(e);
+  // shapes outside the pipelined kernel: the decode step, then the flush
+  e = launch_m2(M2Kind::Decode, a, cs);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_flush(m2_flush_launch(d, s, A), cs));
+}
+
+static FlushLaunch m2_flush_launch(const rssm_m2_dims &d, const rssm_m2_replay *s, const float *A) {
   FlushLaunch a;
   std::memset(&a, 0, sizeof(a));
   a.B = d.B;
@@ -191,7 +223,15 @@ rssm_status replay_flush(const rssm_m2_dims *dims, const rssm_m2_replay *s, cons
   a.sync = s->sync;
   a.err = s->err;
   a.num_sms = device_sm_count();
-  return cuda_status(launch_flush(a, reinterpret_cast<cudaStream_t>(stream)));
+  return a;
+}
+
+rssm_status replay_flush(const rssm_m2_dims *dims, const rssm_m2_replay *s, const float *A, rssm_stream_t stream) {
+  rssm_status st = check_m2_dims(dims);
+  if (st) return st;
+  const rssm_m2_dims &d = *dims;
+  if (!m2_replay_ok(d, s, true) || !ok4(A)) return RSSM_ERR_INVALID_ARG;
+  return cuda_status(launch_flush(m2_flush_launch(d, s, A), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 rssm_status replay_spec_verify(const rssm_m2_dims *dims, const rssm_m2_replay *s, int32_t T, const void *v,

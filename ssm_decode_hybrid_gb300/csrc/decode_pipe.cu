@@ -1,0 +1,408 @@
+// Pipelined ReplaySSM decode step for Mamba-2 (sm_103a): a persistent kernel
+// that streams each (sequence, head) work item's checkpoint tile and ring
+// entries into shared memory with bulk asynchronous copies (TMA engine,
+// cp.async.bulk) through a multi-stage mbarrier pipeline.
+//
+// "ReplaySSM: Cache SSM Inputs, Not State" -- "Algorithm: Mamba-2 standard
+// decode" (output-only decode) and "Kernel design details" (ring buffer with
+// in-kernel indexing).
+//
+// Roles.  Warp 0 is the producer: one lane waits for a free stage, then issues
+// the copies of one item -- the d x n fp32 block of S_0 (one contiguous
+// copy), the committed ring slots of v and k (one or two contiguous segments,
+// copied into the same slot positions of a shared-memory ring), the item's
+// Delta ring, and this step's v, k, q.  This step's Delta and A are read by
+// the whole producer warp for 32 items at a time and the pointers once per
+// sequence, so no per-item load sits on the copy path.  Two consumer groups of four warps
+// take alternate items: decay weights (suffix scan over <= 32 entries in one
+// warp), k_j^T q (one lane group per entry), the buffer term, S_0 q from the
+// shared-memory tile, then y and the appended ring entry go back to HBM.
+//
+// Work split.  Items (b, head) are numbered b*H + i, which is also the order
+// of S_0 in HBM; CTA c takes a contiguous run of items, so each SM streams a
+// contiguous region.  The pointer update of a sequence whose heads span
+// several CTAs is handed to the last arrival on the per-sequence counter; a
+// CTA reads the pointers of its sequences once and adds all of its items of a
+// sequence to the counter in one atomic.
+#include "kernels.cuh"
+
+namespace rssm {
+
+namespace {
+
+constexpr int kGroups = 2;
+constexpr int kGroupWarps = 4;
+constexpr int kGroupThreads = 32 * kGroupWarps;
+constexpr int kPipeThreads = 32 + kGroups * kGroupThreads;
+constexpr int kMaxStages = 8;
+constexpr int kMaxRows = 256;
+constexpr int kSeqMax = 256;  // sequences one CTA's run of items may touch
+
+struct alignas(16) StageHdr {
+  int h, st, valid, b;
+  int i, pad0, pad1, pad2;
+  float dt_in, A, pad3, pad4;
+};
+
+struct GroupScratch {
+  float wt[kMaxL];
+  float M[kMaxL];
+  float abar, pad[3];
+  float dot[kMaxRows];
+  float buf[kMaxRows];
+};
+
+struct PipeGeom {
+  int stages, items_per_cta;
+  uint32_t stage_bytes;
+  uint32_t off_vring, off_kring, off_dtring, off_vin, off_kin, off_qin, off_hdr;
+};
+
+template <int N, bool kFuse, typename TI, typename TO>
+__global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launch a, PipeGeom geo) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int NS = geo.stages;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(NS) * geo.stage_bytes);
+  uint64_t *empty = full + kMaxStages;
+  GroupScratch *scratch = reinterpret_cast<GroupScratch *>(empty + kMaxStages);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = a.H, d = a.d, L = a.L;
+  const int HpG = H / a.G;
+  const int total = a.B * H;
+  const int it0 = blockIdx.x * geo.items_per_cta;
+  const int it1 = min(total, it0 + geo.items_per_cta);
+  const int n_items = max(0, it1 - it0);
+  constexpr uint32_t es = sizeof(TI);
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kGroupWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    // Pointers of the chunk's sequences are read once, then this CTA's
+    // arrivals are counted per sequence (one atomic per sequence, not per
+    // item); the last arrival of a sequence advances its pointers.
+    int *s_h = reinterpret_cast<int *>(scratch + kGroups);
+    int *s_st = s_h + kSeqMax;
+    const int b_first = n_items > 0 ? it0 / H : 0;
+    const int nseq = n_items > 0 ? (it1 - 1) / H - b_first + 1 : 0;
+    for (int sq = lane; sq < nseq; sq += 32) {
+      const int b = b_first + sq;
+      const int h = a.count[b], st = a.start[b];
+      s_h[sq] = h;
+      s_st[sq] = st;
+      if (h >= 0 && h < L && st >= 0 && st < L) {
+        const int kb = min(it1, (b + 1) * H) - max(it0, b * H);
+        __threadfence();
+        const int old = atomicAdd(a.sync + b, kb);
+        if (old + kb == H) {
+          __threadfence();
+          a.sync[b] = 0;
+          // fused: a buffer that fills is folded by this launch
+          a.count[b] = (kFuse && h + 1 == L) ? 0 : h + 1;
+          a.flag[b] = (!kFuse && h + 1 == L) ? 1 : 0;
+        }
+      }
+    }
+    __syncwarp();
+    float r_dt = 0.f, r_A = 0.f;
+    for (int it = 0; it < n_items; ++it) {
+      const int item = it0 + it;
+      if ((it & 31) == 0) {
+        const int my = item + lane;
+        if (my < it1) {
+          r_dt = a.dt[my];
+          r_A = a.A[my % H];
+        }
+      }
+      const int src = it & 31;
+      const int sq = item / H - b_first;
+      const int h = s_h[sq];
+      const int st = s_st[sq];
+      const float dti = __shfl_sync(kFull, r_dt, src);
+      const float Ai = __shfl_sync(kFull, r_A, src);
+      const int stage = it % NS;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(empty + stage, ((it / NS) & 1) ^ 1) ? 1 : 0;
+      ok = __shfl_sync(kFull, ok, 0);
+      if (!ok) {
+        if (lane == 0) set_err(a.err, RSSM_EBIT_TIMEOUT);
+        break;
+      }
+      if (lane == 0) {
+        const int b = item / H, i = item - b * H, g = i / HpG;
+        unsigned char *sb = smem + static_cast<size_t>(stage) * geo.stage_bytes;
+        StageHdr *hdr = reinterpret_cast<StageHdr *>(sb + geo.off_hdr);
+        const bool valid = h >= 0 && h < L && st >= 0 && st < L;
+        hdr->h = h;
+        hdr->st = st;
+        hdr->valid = valid ? 1 : 0;
+        hdr->b = b;
+        hdr->i = i;
+        hdr->dt_in = dti;
+        hdr->A = Ai;
+        if (valid) {
+          const size_t bh = static_cast<size_t>(b) * H + i;
+          const size_t bg = static_cast<size_t>(b) * a.G + g;
+          const uint32_t bytes = static_cast<uint32_t>(d) * N * 4u + static_cast<uint32_t>(h) * (d + N) * es +
+                                 static_cast<uint32_t>(L) * 4u + static_cast<uint32_t>(d + 2 * N) * es;
+          uint64_t *bar = full + stage;
+          mbar_arrive_expect_tx(bar, bytes);
+          bulk_g2s(sb, a.S + bh * d * N, static_cast<uint32_t>(d) * N * 4u, bar);
+          const TI *rv = static_cast<const TI *>(a.ring_v) + bh * L * d;
+          const TI *rk = static_cast<const TI *>(a.ring_k) + bg * L * N;
+          const int seg1 = min(h, L - st);
+          if (seg1 > 0) {
+            bulk_g2s(sb + geo.off_vring + static_cast<size_t>(st) * d * es, rv + static_cast<size_t>(st) * d,
+                     static_cast<uint32_t>(seg1) * d * es, bar);
+            bulk_g2s(sb + geo.off_kring + static_cast<size_t>(st) * N * es, rk + static_cast<size_t>(st) * N,
+                     static_cast<uint32_t>(seg1) * N * es, bar);
+          }
+          if (h > seg1) {
+            const uint32_t seg2 = static_cast<uint32_t>(h - seg1);
+            bulk_g2s(sb + geo.off_vring, rv, seg2 * d * es, bar);
+            bulk_g2s(sb + geo.off_kring, rk, seg2 * N * es, bar);
+          }
+          bulk_g2s(sb + geo.off_dtring, a.ring_dt + bh * L, static_cast<uint32_t>(L) * 4u, bar);
+          bulk_g2s(sb + geo.off_vin, static_cast<const TI *>(a.v) + bh * d, static_cast<uint32_t>(d) * es, bar);
+          bulk_g2s(sb + geo.off_kin, static_cast<const TI *>(a.k) + bg * N, static_cast<uint32_t>(N) * es, bar);
+          bulk_g2s(sb + geo.off_qin, static_cast<const TI *>(a.q) + bg * N, static_cast<uint32_t>(N) * es, bar);
+        } else {
+          set_err(a.err, RSSM_EBIT_COUNT_RANGE);
+          mbar_arrive(full + stage);
+        }
+      }
+      __syncwarp();
+    }
+    return;
+  }
+
+  // ------------------------------ consumers -------------------------------
+  constexpr int LPR = N / 4;
+  constexpr int RPW = 32 / LPR;
+  constexpr int RPP = kGroupWarps * RPW;
+  const int gi = (warp - 1) / kGroupWarps;
+  const int wg = (warp - 1) - gi * kGroupWarps;
+  const int gtid = tid - 32 - gi * kGroupThreads;
+  GroupScratch &sc = scratch[gi];
+  const int col = (lane % LPR) * 4;
+
+  for (int it = gi; it < n_items; it += kGroups) {
+    const int stage = it % NS;
+    if (!mbar_wait(full + stage, (it / NS) & 1)) {
+      if (gtid == 0) set_err(a.err, RSSM_EBIT_TIMEOUT);
+      break;
+    }
+    const unsigned char *sb = smem + static_cast<size_t>(stage) * geo.stage_bytes;
+    const StageHdr hdr = *reinterpret_cast<const StageHdr *>(sb + geo.off_hdr);
+    if (hdr.valid) {
+      const int h = hdr.h, st = hdr.st, p = h + 1, b = hdr.b, i = hdr.i, g = i / HpG;
+      const float *s0 = reinterpret_cast<const float *>(sb);
+      const TI *vring = reinterpret_cast<const TI *>(sb + geo.off_vring);
+      const TI *kring = reinterpret_cast<const TI *>(sb + geo.off_kring);
+      const float *dtring = reinterpret_cast<const float *>(sb + geo.off_dtring);
+      const TI *vin = reinterpret_cast<const TI *>(sb + geo.off_vin);
+      const TI *kin = reinterpret_cast<const TI *>(sb + geo.off_kin);
+      const TI *qin = reinterpret_cast<const TI *>(sb + geo.off_qin);
+
+      // phase A: decay weights (warp 0 of the group), k_j^T q (all warps)
+      const float4 q4 = load4(qin + col);
+      if (wg == 0) {
+        const float dtj = (lane < h) ? dtring[(st + lane) % L] : (lane == h ? hdr.dt_in : 0.f);
+        float tot;
+        const float ex = excl_suffix_sum(hdr.A * dtj, lane, tot);
+        sc.wt[lane] = (lane < p) ? dtj * expf(ex) : 0.f;
+        if (lane == 0) sc.abar = expf(tot);
+      }
+      for (int jb = wg * RPW; jb < p; jb += RPP) {
+        const int j = jb + lane / LPR;
+        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < p) kv = load4((j < h ? kring + static_cast<size_t>((st + j) % L) * N : kin) + col);
+        const float m = group_sum<LPR>(dot4(kv, q4));
+        if (j < p && (lane % LPR) == 0) sc.M[j] = m;
+      }
+      named_bar(1 + gi, kGroupThreads);
+
+      // phase B: buffer term per row, S_0 q per row
+      const float abar = sc.abar;
+      for (int r = gtid; r < d; r += kGroupThreads) {
+        float acc = 0.f;
+        for (int j = 0; j < p; ++j) {
+          const TI *vj = (j < h) ? vring + static_cast<size_t>((st + j) % L) * d : vin;
+          acc = fmaf(sc.wt[j] * sc.M[j], load1(vj + r), acc);
+        }
+        sc.buf[r] = acc;
+      }
+      for (int base = 0; base < d; base += 8 * RPP) {
+        float x[8];
+#pragma unroll
+        for (int pp = 0; pp < 8; ++pp) {
+          const int r = base + wg * RPW + lane / LPR + pp * RPP;
+          x[pp] = (r < d) ? dot4(*reinterpret_cast<const float4 *>(s0 + static_cast<size_t>(r) * N + col), q4) : 0.f;
+        }
+        if constexpr (8 <= LPR) {
+          group_sum_multi<LPR, 8>(x, lane);
+          constexpr int SPAN = LPR / 8;
+          const int pp = (lane % LPR) / SPAN;
+          const int r = base + wg * RPW + lane / LPR + pp * RPP;
+          if ((lane % SPAN) == 0 && r < d) sc.dot[r] = x[0];
+        } else {
+#pragma unroll
+          for (int pp = 0; pp < 8; ++pp) {
+            const float t = group_sum<LPR>(x[pp]);
+            const int r = base + wg * RPW + lane / LPR + pp * RPP;
+            if ((lane % LPR) == 0 && r < d) sc.dot[r] = t;
+          }
+        }
+      }
+      named_bar(1 + gi, kGroupThreads);
+
+      // phase C: y, appended ring entry
+      const size_t bh = static_cast<size_t>(b) * H + i;
+      const int slot = (st + h) % L;
+      TO *y = static_cast<TO *>(a.y) + bh * d;
+      TI *rv_out = static_cast<TI *>(a.ring_v) + (bh * L + slot) * d;
+      for (int r = gtid; r < d; r += kGroupThreads) {
+        store1(y + r, fmaf(abar, sc.dot[r], sc.buf[r]));
+        rv_out[r] = vin[r];
+      }
+      if (gtid == 0) a.ring_dt[bh * L + slot] = hdr.dt_in;
+      if (i % HpG == 0) {
+        TI *rk_out = static_cast<TI *>(a.ring_k) + ((static_cast<size_t>(b) * a.G + g) * L + slot) * N;
+        for (int c = gtid; c < N; c += kGroupThreads) rk_out[c] = kin[c];
+      }
+      if (kFuse && p == L) {
+        // The buffer is full after this append: fold all L entries into S_0
+        // with the weights of this step, S_0 <- abar S_0 + sum_j s_j v_j k_j^T,
+        // reading S_0 and the entries from the stage already in shared memory.
+        float *S0g = a.S + bh * d * N;
+        constexpr int CG = N / 4;                // column groups of 4
+        constexpr int RSTEP = kGroupThreads / CG;  // rows covered per pass
+        const int c4 = (gtid % CG) * 4;
+        for (int r0 = gtid / CG; r0 < d; r0 += 4 * RSTEP) {
+          float4 acc[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = r0 + u * RSTEP;
+            const float4 sv = (r < d) ? *reinterpret_cast<const float4 *>(s0 + static_cast<size_t>(r) * N + c4)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            acc[u] = make_float4(abar * sv.x, abar * sv.y, abar * sv.z, abar * sv.w);
+          }
+          for (int j = 0; j < L; ++j) {
+            const bool cur = j == h;
+            const size_t sl = static_cast<size_t>((st + j) % L);
+            const float4 kv = load4((cur ? kin : kring + sl * N) + c4);
+            const TI *vj = cur ? vin : vring + sl * d;
+            const float w = sc.wt[j];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int r = r0 + u * RSTEP;
+              const float wv = (r < d) ? w * load1(vj + r) : 0.f;
+              acc[u].x = fmaf(wv, kv.x, acc[u].x);
+              acc[u].y = fmaf(wv, kv.y, acc[u].y);
+              acc[u].z = fmaf(wv, kv.z, acc[u].z);
+              acc[u].w = fmaf(wv, kv.w, acc[u].w);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = r0 + u * RSTEP;
+            if (r < d) stg_stream4(S0g + static_cast<size_t>(r) * N + c4, acc[u]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + stage);
+  }
+}
+
+template <int N, bool kFuse, typename TI, typename TO>
+cudaError_t launch_pipe_n(const M2Launch &a, cudaStream_t stream, bool *launched) {
+  *launched = false;
+  int dev = 0, sms = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+  const uint32_t es = sizeof(TI);
+  auto al = [](uint32_t x) { return (x + 127u) & ~127u; };
+  PipeGeom geo;
+  uint32_t off = al(static_cast<uint32_t>(a.d) * N * 4u);
+  geo.off_vring = off;
+  off = al(off + static_cast<uint32_t>(a.L) * a.d * es);
+  geo.off_kring = off;
+  off = al(off + static_cast<uint32_t>(a.L) * N * es);
+  geo.off_dtring = off;
+  off = al(off + static_cast<uint32_t>(a.L) * 4u);
+  geo.off_vin = off;
+  off = al(off + static_cast<uint32_t>(a.d) * es);
+  geo.off_kin = off;
+  off = al(off + N * es);
+  geo.off_qin = off;
+  off = al(off + N * es);
+  geo.off_hdr = off;
+  geo.stage_bytes = al(off + sizeof(StageHdr));
+  const uint32_t fixed = 2u * kMaxStages * 8u + kGroups * sizeof(GroupScratch) + 2u * kSeqMax * sizeof(int);
+  const int stages = static_cast<int>((static_cast<uint32_t>(optin) - fixed) / geo.stage_bytes);
+  if (stages < 2) return cudaSuccess;  // not launched: the caller uses the per-head kernel
+  geo.stages = stages < kMaxStages ? stages : kMaxStages;
+  const int total = a.B * a.H;
+  int grid = total < sms ? total : sms;
+  geo.items_per_cta = (total + grid - 1) / grid;
+  const int cap = (kSeqMax - 2) * a.H;  // keeps a run within kSeqMax sequences
+  if (geo.items_per_cta > cap) geo.items_per_cta = cap;
+  grid = (total + geo.items_per_cta - 1) / geo.items_per_cta;
+  const size_t smem = static_cast<size_t>(geo.stages) * geo.stage_bytes + fixed;
+  auto kern = m2_decode_pipe_kernel<N, kFuse, TI, TO>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
+      cudaSuccess)
+    return e;
+  kern<<<grid, kPipeThreads, smem, stream>>>(a, geo);
+  *launched = true;
+  return cudaGetLastError();
+}
+
+template <bool kFuse, typename TI, typename TO>
+cudaError_t launch_pipe_t(const M2Launch &a, cudaStream_t stream, bool *launched) {
+  switch (a.n) {
+    case 16: return launch_pipe_n<16, kFuse, TI, TO>(a, stream, launched);
+    case 32: return launch_pipe_n<32, kFuse, TI, TO>(a, stream, launched);
+    case 64: return launch_pipe_n<64, kFuse, TI, TO>(a, stream, launched);
+    case 128: return launch_pipe_n<128, kFuse, TI, TO>(a, stream, launched);
+  }
+  *launched = false;
+  return cudaSuccess;
+}
+
+template <bool kFuse>
+cudaError_t launch_pipe_f(const M2Launch &a, cudaStream_t stream, bool *launched) {
+  if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_F32) return launch_pipe_t<kFuse, bf16, float>(a, stream, launched);
+  if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_BF16) return launch_pipe_t<kFuse, bf16, bf16>(a, stream, launched);
+  if (a.in_dtype == RSSM_F32 && a.y_dtype == RSSM_F32) return launch_pipe_t<kFuse, float, float>(a, stream, launched);
+  if (a.in_dtype == RSSM_F32 && a.y_dtype == RSSM_BF16) return launch_pipe_t<kFuse, float, bf16>(a, stream, launched);
+  *launched = false;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+bool m2_decode_pipe_eligible(const M2Launch &a) {
+  const int es = a.in_dtype == RSSM_BF16 ? 2 : 4;
+  auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  return a.L % 4 == 0 && (a.d * es) % 16 == 0 && a.d <= kMaxRows && a.d * a.n * 4 <= 96 * 1024 && a16(a.S) &&
+         a16(a.ring_v) && a16(a.ring_k) && a16(a.ring_dt) && a16(a.v) && a16(a.k) && a16(a.q);
+}
+
+cudaError_t launch_m2_decode_pipe(const M2Launch &a, bool fuse_flush, cudaStream_t stream, bool *launched) {
+  return fuse_flush ? launch_pipe_f<true>(a, stream, launched) : launch_pipe_f<false>(a, stream, launched);
+}
+
+}  // namespace rssm

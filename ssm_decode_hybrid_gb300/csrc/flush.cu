@@ -1,14 +1,19 @@
 // Flush: fold the committed ring entries of flagged sequences into S_0.
 //
 // "ReplaySSM: Cache SSM Inputs, Not State" -- "Algorithm: Mamba-2 standard
-// decode" (flush: S_0 <- abar S_0 + sum_j s_j v_j k_j^T, clear the buffer) and
-// the GDN appendix (same history form with the cached corrections u_j).
+// decode" (flush: S_0 <- abar S_0 + sum_j s_j v_j k_j^T, then clear the
+// buffer) and the GDN appendix (same history form with the cached
+// corrections u_j and the gates g_j).
 //
-// CUDA-core version: a persistent grid walks the (sequence, head) items; items
-// of unflagged sequences cost one flag read.  For a flagged item the c
-// weighted vectors (d floats each) and c keys (n floats each) are staged in
-// shared memory, and every thread updates the 16-byte column slices of S_0
-// it owns: acc = abar * S_0 + sum_j (w_j v_j[r]) k_j[col..col+3].
+// Two launches.  The first is a persistent grid: every CTA compacts the
+// flagged sequences (in sequence order, so all CTAs build the same list) and
+// takes every grid-th (sequence, head) item of that list.  For an item, the
+// c committed entries (c x d vectors, c x n keys) are staged in shared memory;
+// each thread owns one 16-byte column slice of up to 8 rows of S_0, loads it,
+// and accumulates abar * S_0 + sum_j (w_j v_j[r]) k_j[col..col+3] with the
+// key slice read once per entry.  The last of a sequence's items to arrive
+// resets start and count.  The flags themselves are cleared by the second,
+// one-thread-per-sequence launch, because every CTA of the first reads them.
 #include "kernels.cuh"
 
 namespace rssm {
@@ -21,98 +26,127 @@ template <int N, typename TV, typename TK>
 __global__ void __launch_bounds__(kThreads) flush_kernel(FlushLaunch a) {
   constexpr int LPR = N / 4, RPW = 32 / LPR, RPP = kWarps * RPW;
   extern __shared__ float smem[];  // [L][d] vectors, then [L][N] keys (f32)
+  __shared__ int s_list[kThreads];
+  __shared__ int s_wsum[kWarps + 1];
   __shared__ float s_wt[kMaxL];
   __shared__ float s_abar;
-  __shared__ int s_ptr[3];
+  __shared__ int s_ptr[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int d = a.d, L = a.L;
-  const int HpG = a.H / a.G;
+  const int B = a.B, H = a.H, d = a.d, L = a.L;
+  const int HpG = H / a.G;
+  const int grid = gridDim.x;
   float *s_vec = smem;
   float *s_key = smem + static_cast<size_t>(L) * d;
   const int col = (lane % LPR) * 4;
   const int row0 = warp * RPW + lane / LPR;
-  const int items = a.B * a.H;
 
-  for (int w = blockIdx.x; w < items; w += gridDim.x) {
-    const int b = w / a.H, i = w - b * a.H;
+  int done = 0;  // flagged sequences in earlier chunks
+  for (int base = 0; base < B; base += kThreads) {
+    // ordered compaction of the flagged sequences of this chunk
+    const int bq = base + tid;
+    const bool f = bq < B && a.flag[bq] != 0;
+    const unsigned m = __ballot_sync(kFull, f);
+    if (lane == 0) s_wsum[warp] = __popc(m);
+    __syncthreads();
     if (tid == 0) {
-      s_ptr[0] = a.flag[b];
-      s_ptr[1] = a.count[b];
-      s_ptr[2] = a.start[b];
+      int acc = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        const int c = s_wsum[w];
+        s_wsum[w] = acc;
+        acc += c;
+      }
+      s_wsum[kWarps] = acc;
     }
     __syncthreads();
-    const int f = s_ptr[0], c = s_ptr[1], st = s_ptr[2];
+    if (f) s_list[s_wsum[warp] + __popc(m & ((1u << lane) - 1u))] = bq;
     __syncthreads();
-    if (f == 0) continue;
-    if (c < 0 || c > L || st < 0 || st >= L) {
-      if (tid == 0) set_err(a.err, RSSM_EBIT_COUNT_RANGE);
-      continue;
-    }
-    if (tid == 0 && last_arrival(a.sync, b, a.H)) {
-      a.start[b] = (st + c) % L;
-      a.count[b] = 0;
-      a.flag[b] = 0;
-    }
-    const size_t bh = static_cast<size_t>(b) * a.H + i;
-    const size_t bg = static_cast<size_t>(b) * a.G + i / HpG;
-    float *S0 = a.S0 + bh * d * N;
-
-    // checkpoint loads for the first chunk go out first
-    float4 s[kPass];
-#pragma unroll
-    for (int p = 0; p < kPass; ++p) {
-      const int r = row0 + p * RPP;
-      s[p] = (r < d) ? ldg_stream4(S0 + static_cast<size_t>(r) * N + col) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    // weights: lane j < c holds entry j+1
-    if (warp == 0) {
-      float ld = 0.f;
-      if (lane < c) ld = a.ring_ld[bh * L + (st + lane) % L];
-      const float la = a.mamba2 ? a.A[i] * ld : ld;
-      float total;
-      const float ex = excl_suffix_sum(lane < c ? la : 0.f, lane, total);
-      if (lane < c) s_wt[lane] = (a.mamba2 ? ld : 1.f) * expf(ex);
-      if (lane == 0) s_abar = expf(total);
-    }
-    const TV *vec = static_cast<const TV *>(a.ring_vec) + bh * L * d;
-    for (int idx = tid; idx < c * d; idx += kThreads) {
-      const int j = idx / d, r = idx - j * d;
-      s_vec[idx] = load1(vec + static_cast<size_t>((st + j) % L) * d + r);
-    }
-    const TK *key = static_cast<const TK *>(a.ring_key) + bg * L * N;
-    for (int idx = tid; idx < c * (N / 4); idx += kThreads) {
-      const int j = idx / (N / 4), c4 = (idx - j * (N / 4)) * 4;
-      store4(s_key + j * N + c4, load4(key + static_cast<size_t>((st + j) % L) * N + c4));
-    }
-    __syncthreads();
-    const float abar = s_abar;
-    for (int base = 0; base < d; base += kPass * RPP) {
-      if (base > 0) {
+    const int nf = s_wsum[kWarps];
+    const long first = static_cast<long>(done) * H;  // global index of this chunk's first item
+    int k = static_cast<int>(((static_cast<long>(blockIdx.x) - first) % grid + grid) % grid);
+    for (; k < nf * H; k += grid) {
+      const int b = s_list[k / H], i = k % H;
+      if (tid == 0) {
+        s_ptr[0] = a.count[b];
+        s_ptr[1] = a.start[b];
+      }
+      __syncthreads();
+      const int c = s_ptr[0], st = s_ptr[1];
+      __syncthreads();
+      if (c < 0 || c > L || st < 0 || st >= L) {
+        if (tid == 0) set_err(a.err, RSSM_EBIT_COUNT_RANGE);
+        continue;
+      }
+      if (tid == 0 && last_arrival(a.sync, b, H)) {
+        a.start[b] = (st + c) % L;
+        a.count[b] = 0;
+      }
+      const size_t bh = static_cast<size_t>(b) * H + i;
+      const size_t bg = static_cast<size_t>(b) * a.G + i / HpG;
+      float *S0 = a.S0 + bh * d * N;
+      const TV *vec = static_cast<const TV *>(a.ring_vec) + bh * L * d;
+      const TK *key = static_cast<const TK *>(a.ring_key) + bg * L * N;
+      if (warp == 0) {
+        float ld = 0.f;
+        if (lane < c) ld = a.ring_ld[bh * L + (st + lane) % L];
+        const float la = a.mamba2 ? a.A[i] * ld : ld;
+        float total;
+        const float ex = excl_suffix_sum(lane < c ? la : 0.f, lane, total);
+        if (lane < c) s_wt[lane] = (a.mamba2 ? ld : 1.f) * expf(ex);
+        if (lane == 0) s_abar = expf(total);
+      }
+      for (int idx = tid; idx < c * d; idx += kThreads) {
+        const int j = idx / d, r = idx - j * d;
+        s_vec[idx] = load1(vec + static_cast<size_t>((st + j) % L) * d + r);
+      }
+      for (int idx = tid; idx < c * (N / 4); idx += kThreads) {
+        const int j = idx / (N / 4), c4 = (idx - j * (N / 4)) * 4;
+        store4(s_key + j * N + c4, load4(key + static_cast<size_t>((st + j) % L) * N + c4));
+      }
+      for (int rb = 0; rb < d; rb += kPass * RPP) {
+        float4 acc[kPass];
 #pragma unroll
         for (int p = 0; p < kPass; ++p) {
-          const int r = base + row0 + p * RPP;
-          s[p] = (r < d) ? ldg_stream4(S0 + static_cast<size_t>(r) * N + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const int r = rb + row0 + p * RPP;
+          acc[p] = (r < d) ? ldg_stream4(S0 + static_cast<size_t>(r) * N + col) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      }
+        __syncthreads();  // s_vec, s_key, s_wt, s_abar ready (first pass); loads in flight
+        const float abar = s_abar;
 #pragma unroll
-      for (int p = 0; p < kPass; ++p) {
-        const int r = base + row0 + p * RPP;
-        if (r < d) {
-          float4 acc = make_float4(abar * s[p].x, abar * s[p].y, abar * s[p].z, abar * s[p].w);
-          for (int j = 0; j < c; ++j) {
-            const float wv = s_wt[j] * s_vec[j * d + r];
-            const float4 kv = *reinterpret_cast<const float4 *>(s_key + j * N + col);
-            acc.x = fmaf(wv, kv.x, acc.x);
-            acc.y = fmaf(wv, kv.y, acc.y);
-            acc.z = fmaf(wv, kv.z, acc.z);
-            acc.w = fmaf(wv, kv.w, acc.w);
+        for (int p = 0; p < kPass; ++p) {
+          acc[p].x *= abar;
+          acc[p].y *= abar;
+          acc[p].z *= abar;
+          acc[p].w *= abar;
+        }
+        for (int j = 0; j < c; ++j) {
+          const float4 kv = *reinterpret_cast<const float4 *>(s_key + j * N + col);
+          const float w = s_wt[j];
+#pragma unroll
+          for (int p = 0; p < kPass; ++p) {
+            const int r = rb + row0 + p * RPP;
+            const float wv = (r < d) ? w * s_vec[j * d + r] : 0.f;
+            acc[p].x = fmaf(wv, kv.x, acc[p].x);
+            acc[p].y = fmaf(wv, kv.y, acc[p].y);
+            acc[p].z = fmaf(wv, kv.z, acc[p].z);
+            acc[p].w = fmaf(wv, kv.w, acc[p].w);
           }
-          stg_stream4(S0 + static_cast<size_t>(r) * N + col, acc);
+        }
+#pragma unroll
+        for (int p = 0; p < kPass; ++p) {
+          const int r = rb + row0 + p * RPP;
+          if (r < d) stg_stream4(S0 + static_cast<size_t>(r) * N + col, acc[p]);
         }
       }
+      __syncthreads();  // shared staging is reused by the next item
     }
-    __syncthreads();
+    done += nf;
+    __syncthreads();  // s_list / s_wsum are rebuilt for the next chunk
   }
+}
+
+__global__ void clear_flags_kernel(int B, int32_t *flag) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) flag[b] = 0;
 }
 
 template <int N, typename TV, typename TK>
@@ -124,9 +158,12 @@ cudaError_t launch_flush_n(const FlushLaunch &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   const long items = static_cast<long>(a.B) * a.H;
-  const long cap = static_cast<long>(a.num_sms > 0 ? a.num_sms : 148) * 8;
+  const long cap = static_cast<long>(a.num_sms > 0 ? a.num_sms : 148) * 4;
   const unsigned grid = static_cast<unsigned>(items < cap ? items : cap);
   kern<<<grid, kThreads, sm, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  clear_flags_kernel<<<(a.B + 255) / 256, 256, 0, stream>>>(a.B, a.flag);
   return cudaGetLastError();
 }
 

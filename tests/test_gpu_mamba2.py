@@ -77,6 +77,35 @@ def test_decode_parity(shape):
     run_decode(shape, seed=123, steps=2 * shape.L + 3)
 
 
+FUSED_SHAPES = [
+    wl.Mamba2Shape(B=6, H=32, G=8, d=64, n=128, L=16, in_dtype=wl.BF16),
+    wl.Mamba2Shape(B=5, H=8, G=4, d=32, n=64, L=8, in_dtype=wl.F32),
+    wl.Mamba2Shape(B=3, H=4, G=2, d=16, n=16, L=4, in_dtype=wl.BF16),
+    wl.Mamba2Shape(B=4, H=6, G=3, d=20, n=32, L=3, in_dtype=wl.BF16),  # outside the pipelined kernel
+]
+
+
+@pytest.mark.parametrize("shape", FUSED_SHAPES, ids=lambda s: f"B{s.B}H{s.H}d{s.d}n{s.n}L{s.L}{s.in_dtype}")
+def test_decode_fused_parity(shape):
+    """replay_decode_step_fused == decode step followed by the flush."""
+    R = rs()
+    seed = 321
+    init = wl.mamba2_init(shape, seed)
+    state = m2_state(init)
+    orc = oracle_replay(init, np.arange(shape.B))
+    A = dev(init.A)
+    for t in range(2 * shape.L + 3):
+        st = wl.mamba2_step(shape, seed, t)
+        y = R.replay_decode_step_fused(state, *m2_step_dev(st, shape.in_dtype), A)
+        y_ref = orc.decode_step(st.v, st.k, st.q, st.dt)
+        orc.flush()
+        assert_close(y, y_ref, what=f"step {t}")
+        check_pointers(state, orc, np.arange(shape.B), f"step {t}")
+    assert_close(state.S0, orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0
+    assert int(host(state.sync).sum()) == 0
+
+
 def test_decode_bf16_output():
     run_decode(wl.Mamba2Shape(B=4, H=8, G=2, d=64, n=128, L=8, in_dtype=wl.BF16), 77, steps=12,
                y_dtype=torch.bfloat16)
