@@ -4,39 +4,42 @@
 // cp.async.bulk) through a multi-stage mbarrier pipeline.
 //
 // "ReplaySSM: Cache SSM Inputs, Not State" -- "Algorithm: Mamba-2 standard
-// decode" (output-only decode) and "Kernel design details" (ring buffer with
-// in-kernel indexing).
+// decode" (output-only decode; "if the buffer is full, flush") and "Kernel
+// design details" (ring buffer with in-kernel indexing).
 //
-// Roles.  Warp 0 is the producer: one lane waits for a free stage, then issues
-// the copies of one item -- the d x n fp32 block of S_0 (one contiguous
-// copy), the committed ring slots of v and k (one or two contiguous segments,
-// copied into the same slot positions of a shared-memory ring), the item's
-// Delta ring, and this step's v, k, q.  This step's Delta and A are read by
-// the whole producer warp for 32 items at a time and the pointers once per
-// sequence, so no per-item load sits on the copy path.  Two consumer groups of four warps
-// take alternate items: decay weights (suffix scan over <= 32 entries in one
-// warp), k_j^T q (one lane group per entry), the buffer term, S_0 q from the
-// shared-memory tile, then y and the appended ring entry go back to HBM.
+// Roles.  Warp 0 is the producer.  Per item, one lane waits for a free stage
+// and issues the copies: the d x n fp32 block of S_0 (one contiguous copy),
+// the committed ring slots of v and k (one or two contiguous segments, copied
+// into the same slot positions of a shared-memory ring), the item's Delta
+// ring, and this step's v, k, q.  The whole producer warp reads the per-item
+// metadata (start, count, this step's Delta, A) 32 items at a time, one batch
+// ahead of the copies, and counts the items' arrivals for the pointer update,
+// so no dependent load sits on the copy path.  kGroups consumer groups of four
+// warps take items in turn: decay weights (suffix scan over <= 32 entries in
+// one warp), k_j^T q (one lane group per entry), the buffer term, S_0 q from
+// the shared-memory tile; then y and the appended ring entry go to HBM.  With
+// the flush fused, an item whose buffer fills is folded into S_0 from the
+// same shared-memory stage.
 //
-// Work split.  Items (b, head) are numbered b*H + i, which is also the order
-// of S_0 in HBM; CTA c takes a contiguous run of items, so each SM streams a
-// contiguous region.  The pointer update of a sequence whose heads span
-// several CTAs is handed to the last arrival on the per-sequence counter; a
-// CTA reads the pointers of its sequences once and adds all of its items of a
-// sequence to the counter in one atomic.
+// Work split.  Items are numbered head-major, item = i * B + b, and CTA c
+// takes a contiguous run of them.  Each item's S_0 block is one contiguous
+// 16-byte aligned region, so the order costs no DRAM efficiency, and the
+// items of a sequence (which share its fill level, hence its flush) spread
+// over many CTAs.  The pointer update of a sequence is handed to the last of
+// its items to arrive on the per-sequence counter.
 #include "kernels.cuh"
 
 namespace rssm {
 
 namespace {
 
-constexpr int kGroups = 2;
+constexpr int kGroups = 3;
 constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = 32 * kGroupWarps;
 constexpr int kPipeThreads = 32 + kGroups * kGroupThreads;
 constexpr int kMaxStages = 8;
 constexpr int kMaxRows = 256;
-constexpr int kSeqMax = 256;  // sequences one CTA's run of items may touch
+constexpr int kItemMax = 512;  // items per CTA (metadata table size)
 
 struct alignas(16) StageHdr {
   int h, st, valid, b;
@@ -44,9 +47,15 @@ struct alignas(16) StageHdr {
   float dt_in, A, pad3, pad4;
 };
 
+struct ItemMeta {
+  int h, st;
+  float dt, A;
+};
+
 struct GroupScratch {
   float wt[kMaxL];
   float M[kMaxL];
+  int slot[kMaxL];
   float abar, pad[3];
   float dot[kMaxRows];
   float buf[kMaxRows];
@@ -58,6 +67,8 @@ struct PipeGeom {
   uint32_t off_vring, off_kring, off_dtring, off_vin, off_kin, off_qin, off_hdr;
 };
 
+__device__ __forceinline__ int wrap(int s, int L) { return s >= L ? s - L : s; }
+
 template <int N, bool kFuse, typename TI, typename TO>
 __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launch a, PipeGeom geo) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -65,11 +76,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(NS) * geo.stage_bytes);
   uint64_t *empty = full + kMaxStages;
   GroupScratch *scratch = reinterpret_cast<GroupScratch *>(empty + kMaxStages);
+  ItemMeta *meta = reinterpret_cast<ItemMeta *>(scratch + kGroups);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.H, d = a.d, L = a.L;
+  const int B = a.B, H = a.H, d = a.d, L = a.L;
   const int HpG = H / a.G;
-  const int total = a.B * H;
+  const int total = B * H;
   const int it0 = blockIdx.x * geo.items_per_cta;
   const int it1 = min(total, it0 + geo.items_per_cta);
   const int n_items = max(0, it1 - it0);
@@ -86,48 +98,31 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
-    // Pointers of the chunk's sequences are read once, then this CTA's
-    // arrivals are counted per sequence (one atomic per sequence, not per
-    // item); the last arrival of a sequence advances its pointers.
-    int *s_h = reinterpret_cast<int *>(scratch + kGroups);
-    int *s_st = s_h + kSeqMax;
-    const int b_first = n_items > 0 ? it0 / H : 0;
-    const int nseq = n_items > 0 ? (it1 - 1) / H - b_first + 1 : 0;
-    for (int sq = lane; sq < nseq; sq += 32) {
-      const int b = b_first + sq;
-      const int h = a.count[b], st = a.start[b];
-      s_h[sq] = h;
-      s_st[sq] = st;
-      if (h >= 0 && h < L && st >= 0 && st < L) {
-        const int kb = min(it1, (b + 1) * H) - max(it0, b * H);
-        __threadfence();
-        const int old = atomicAdd(a.sync + b, kb);
-        if (old + kb == H) {
-          __threadfence();
-          a.sync[b] = 0;
-          // fused: a buffer that fills is folded by this launch
-          a.count[b] = (kFuse && h + 1 == L) ? 0 : h + 1;
-          a.flag[b] = (!kFuse && h + 1 == L) ? 1 : 0;
+    // Metadata of items [32k, 32k+32): one lane per item reads the pointers of
+    // its sequence, this step's Delta and A, then counts the item's arrival;
+    // the last arrival of a sequence advances its pointers (it runs after
+    // every item of the sequence, in every CTA, has read them).
+    auto meta_batch = [&](int k) {
+      const int it = 32 * k + lane;
+      if (it < n_items) {
+        const int item = it0 + it;
+        const int i = item / B, b = item - i * B;
+        ItemMeta m;
+        m.h = a.count[b];
+        m.st = a.start[b];
+        m.dt = a.dt[static_cast<size_t>(b) * H + i];
+        m.A = a.A[i];
+        meta[it] = m;
+        if (m.h >= 0 && m.h < L && m.st >= 0 && m.st < L && last_arrival(a.sync, b, H)) {
+          a.count[b] = (kFuse && m.h + 1 == L) ? 0 : m.h + 1;  // fused: a filled buffer is folded now
+          a.flag[b] = (!kFuse && m.h + 1 == L) ? 1 : 0;
         }
       }
-    }
-    __syncwarp();
-    float r_dt = 0.f, r_A = 0.f;
+      __syncwarp();
+    };
+    meta_batch(0);
     for (int it = 0; it < n_items; ++it) {
-      const int item = it0 + it;
-      if ((it & 31) == 0) {
-        const int my = item + lane;
-        if (my < it1) {
-          r_dt = a.dt[my];
-          r_A = a.A[my % H];
-        }
-      }
-      const int src = it & 31;
-      const int sq = item / H - b_first;
-      const int h = s_h[sq];
-      const int st = s_st[sq];
-      const float dti = __shfl_sync(kFull, r_dt, src);
-      const float Ai = __shfl_sync(kFull, r_A, src);
+      if ((it & 31) == 0 && it + 32 < n_items) meta_batch(it / 32 + 1);
       const int stage = it % NS;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(empty + stage, ((it / NS) & 1) ^ 1) ? 1 : 0;
@@ -137,7 +132,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
         break;
       }
       if (lane == 0) {
-        const int b = item / H, i = item - b * H, g = i / HpG;
+        const ItemMeta m = meta[it];
+        const int h = m.h, st = m.st;
+        const int item = it0 + it;
+        const int i = item / B, b = item - i * B, g = i / HpG;
         unsigned char *sb = smem + static_cast<size_t>(stage) * geo.stage_bytes;
         StageHdr *hdr = reinterpret_cast<StageHdr *>(sb + geo.off_hdr);
         const bool valid = h >= 0 && h < L && st >= 0 && st < L;
@@ -146,8 +144,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
         hdr->valid = valid ? 1 : 0;
         hdr->b = b;
         hdr->i = i;
-        hdr->dt_in = dti;
-        hdr->A = Ai;
+        hdr->dt_in = m.dt;
+        hdr->A = m.A;
         if (valid) {
           const size_t bh = static_cast<size_t>(b) * H + i;
           const size_t bg = static_cast<size_t>(b) * a.G + g;
@@ -212,33 +210,39 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
       const TI *kin = reinterpret_cast<const TI *>(sb + geo.off_kin);
       const TI *qin = reinterpret_cast<const TI *>(sb + geo.off_qin);
 
-      // phase A: decay weights (warp 0 of the group), k_j^T q (all warps)
+      // phase A: decay weights and ring slots (warp 0), k_j^T q (all warps)
       const float4 q4 = load4(qin + col);
       if (wg == 0) {
-        const float dtj = (lane < h) ? dtring[(st + lane) % L] : (lane == h ? hdr.dt_in : 0.f);
+        const int slot = wrap(st + lane, L);
+        const float dtj = (lane < h) ? dtring[slot] : (lane == h ? hdr.dt_in : 0.f);
         float tot;
         const float ex = excl_suffix_sum(hdr.A * dtj, lane, tot);
         sc.wt[lane] = (lane < p) ? dtj * expf(ex) : 0.f;
+        sc.slot[lane] = slot;
         if (lane == 0) sc.abar = expf(tot);
       }
       for (int jb = wg * RPW; jb < p; jb += RPP) {
         const int j = jb + lane / LPR;
         float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < p) kv = load4((j < h ? kring + static_cast<size_t>((st + j) % L) * N : kin) + col);
+        if (j < p) kv = load4((j < h ? kring + static_cast<size_t>(wrap(st + j, L)) * N : kin) + col);
         const float m = group_sum<LPR>(dot4(kv, q4));
         if (j < p && (lane % LPR) == 0) sc.M[j] = m;
       }
       named_bar(1 + gi, kGroupThreads);
 
-      // phase B: buffer term per row, S_0 q per row
+      // phase B: buffer term per row (four independent partial sums), S_0 q per row
       const float abar = sc.abar;
       for (int r = gtid; r < d; r += kGroupThreads) {
-        float acc = 0.f;
-        for (int j = 0; j < p; ++j) {
-          const TI *vj = (j < h) ? vring + static_cast<size_t>((st + j) % L) * d : vin;
-          acc = fmaf(sc.wt[j] * sc.M[j], load1(vj + r), acc);
+        float acc0 = sc.wt[h] * sc.M[h] * load1(vin + r), acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        int j = 0;
+        for (; j + 4 <= h; j += 4) {
+          acc0 = fmaf(sc.wt[j] * sc.M[j], load1(vring + static_cast<size_t>(sc.slot[j]) * d + r), acc0);
+          acc1 = fmaf(sc.wt[j + 1] * sc.M[j + 1], load1(vring + static_cast<size_t>(sc.slot[j + 1]) * d + r), acc1);
+          acc2 = fmaf(sc.wt[j + 2] * sc.M[j + 2], load1(vring + static_cast<size_t>(sc.slot[j + 2]) * d + r), acc2);
+          acc3 = fmaf(sc.wt[j + 3] * sc.M[j + 3], load1(vring + static_cast<size_t>(sc.slot[j + 3]) * d + r), acc3);
         }
-        sc.buf[r] = acc;
+        for (; j < h; ++j) acc0 = fmaf(sc.wt[j] * sc.M[j], load1(vring + static_cast<size_t>(sc.slot[j]) * d + r), acc0);
+        sc.buf[r] = (acc0 + acc1) + (acc2 + acc3);
       }
       for (int base = 0; base < d; base += 8 * RPP) {
         float x[8];
@@ -264,9 +268,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
       }
       named_bar(1 + gi, kGroupThreads);
 
-      // phase C: y, appended ring entry
+      // phase C: y, the appended ring entry
       const size_t bh = static_cast<size_t>(b) * H + i;
-      const int slot = (st + h) % L;
+      const int slot = wrap(st + h, L);
       TO *y = static_cast<TO *>(a.y) + bh * d;
       TI *rv_out = static_cast<TI *>(a.ring_v) + (bh * L + slot) * d;
       for (int r = gtid; r < d; r += kGroupThreads) {
@@ -280,10 +284,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
       }
       if (kFuse && p == L) {
         // The buffer is full after this append: fold all L entries into S_0
-        // with the weights of this step, S_0 <- abar S_0 + sum_j s_j v_j k_j^T,
-        // reading S_0 and the entries from the stage already in shared memory.
+        // with this step's weights, S_0 <- abar S_0 + sum_j s_j v_j k_j^T,
+        // reading S_0 and the entries from the stage in shared memory.
         float *S0g = a.S + bh * d * N;
-        constexpr int CG = N / 4;                // column groups of 4
+        constexpr int CG = N / 4;                  // column groups of 4
         constexpr int RSTEP = kGroupThreads / CG;  // rows covered per pass
         const int c4 = (gtid % CG) * 4;
         for (int r0 = gtid / CG; r0 < d; r0 += 4 * RSTEP) {
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
           }
           for (int j = 0; j < L; ++j) {
             const bool cur = j == h;
-            const size_t sl = static_cast<size_t>((st + j) % L);
+            const size_t sl = static_cast<size_t>(sc.slot[j]);
             const float4 kv = load4((cur ? kin : kring + sl * N) + c4);
             const TI *vj = cur ? vin : vring + sl * d;
             const float w = sc.wt[j];
@@ -350,15 +354,14 @@ cudaError_t launch_pipe_n(const M2Launch &a, cudaStream_t stream, bool *launched
   off = al(off + N * es);
   geo.off_hdr = off;
   geo.stage_bytes = al(off + sizeof(StageHdr));
-  const uint32_t fixed = 2u * kMaxStages * 8u + kGroups * sizeof(GroupScratch) + 2u * kSeqMax * sizeof(int);
+  const uint32_t fixed = 2u * kMaxStages * 8u + kGroups * sizeof(GroupScratch) + kItemMax * sizeof(ItemMeta);
   const int stages = static_cast<int>((static_cast<uint32_t>(optin) - fixed) / geo.stage_bytes);
   if (stages < 2) return cudaSuccess;  // not launched: the caller uses the per-head kernel
   geo.stages = stages < kMaxStages ? stages : kMaxStages;
   const int total = a.B * a.H;
   int grid = total < sms ? total : sms;
   geo.items_per_cta = (total + grid - 1) / grid;
-  const int cap = (kSeqMax - 2) * a.H;  // keeps a run within kSeqMax sequences
-  if (geo.items_per_cta > cap) geo.items_per_cta = cap;
+  if (geo.items_per_cta > kItemMax) geo.items_per_cta = kItemMax;
   grid = (total + geo.items_per_cta - 1) / geo.items_per_cta;
   const size_t smem = static_cast<size_t>(geo.stages) * geo.stage_bytes + fixed;
   auto kern = m2_decode_pipe_kernel<N, kFuse, TI, TO>;
