@@ -134,10 +134,17 @@ __device__ __forceinline__ float excl_suffix_sum(float la, int lane, float &tota
 // ---------------------------------------------------------------------------
 namespace rssm {
 
-// Spin limit of every mbarrier wait.  A wait that runs out sets
+// Time limit of every wait inside a kernel (mbarrier phases, the fold-unit
+// lock): about one second of GPU global time.  A wait that runs out sets
 // RSSM_EBIT_TIMEOUT in the error word and the kernel winds down instead of
 // hanging the GPU.
-constexpr uint32_t kSpinLimit = 1u << 24;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -170,11 +177,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase of the given parity; false if the limit ran out.
+// Bounded wait for the phase of the given parity; false if the time limit
+// ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kSpinLimit; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
 }
 
 // Bulk (non-tensor) asynchronous copy global -> shared; completion is counted
@@ -186,9 +196,28 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                : "memory");
 }
 
+// Volatile shared/global int access (a flag other threads poll).
+__device__ __forceinline__ int ld_volatile(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
+__device__ __forceinline__ void st_volatile(int *p, int v) { *reinterpret_cast<volatile int *>(p) = v; }
+
 // Barrier over a subset of warps (ids 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads, so
+// that a decision (e.g. a wait that ran out) is the same in all of them.
+__device__ __forceinline__ bool named_bar_or(int id, int threads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(out)
+      : "r"(id), "r"(threads), "r"(pred ? 1u : 0u)
+      : "memory");
+  return out != 0;
 }
 
 }  // namespace rssm

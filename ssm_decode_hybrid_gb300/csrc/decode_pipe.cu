@@ -28,6 +28,7 @@
 // over many CTAs.  The pointer update of a sequence is handed to the last of
 // its items to arrive on the per-sequence counter.
 #include "kernels.cuh"
+#include "tc05.cuh"
 
 namespace rssm {
 
@@ -65,17 +66,145 @@ struct PipeGeom {
   int stages, items_per_cta;
   uint32_t stage_bytes;
   uint32_t off_vring, off_kring, off_dtring, off_vin, off_kin, off_qin, off_hdr;
+  // tensor-core fold unit (fused flush): offsets from the end of the stages
+  uint32_t off_fold, off_opA, off_opB, ke, ncols;
+};
+
+// One tensor-core fold unit per CTA, shared by the consumer groups under a
+// lock (a fold touches one item in L): TMEM accumulator, its mbarrier, the
+// operand buffers.
+struct FoldUnit {
+  uint64_t bar;
+  uint32_t tmem;
+  int lock;
+  uint32_t phase;
+  int pad[3];
 };
 
 __device__ __forceinline__ int wrap(int s, int L) { return s >= L ? s - L : s; }
 
-template <int N, bool kFuse, typename TI, typename TO>
+// Tensor-core fold of one full buffer (n = 128, bf16 entries), by the 128
+// threads of one consumer group holding the CTA's fold unit.  Transposed
+// form: D^T[c][r] = sum_s k_s[c] (w_s v_s[r]) with M = n = 128 state columns
+// (TMEM lanes), N = d rows of S_0, K = the L ring slots (every slot holds a
+// committed entry when the buffer is full; the order over slots is irrelevant
+// to the sum).  The weighted vectors are split into three bf16 terms
+// (hi + mid + lo, about 2^-25 relative) and accumulated by three MMAs over the
+// same key operand, so the fold keeps fp32 accuracy.  Thread (warp w, lane l)
+// owns state column c = 32 (w % 4) + l, the TMEM lane its warp may access,
+// and writes S_0[r][c] = abar S_0[r][c] + D^T[c][r] row by row, coalesced.
+template <int N, typename TI>
+__device__ __forceinline__ void fold_tc(const M2Launch &a, const PipeGeom &geo, FoldUnit *fu,
+                                        const GroupScratch &sc, int gi, int gtid, int warp, int lane,
+                                        const float *s0, const TI *kring, const TI *vring, const TI *kin,
+                                        const TI *vin, int st, int h, float abar, float *S0g) {
+  static_assert(N == 128, "the tensor-core fold maps the 128 state columns to TMEM lanes");
+  const int d = a.d, L = a.L, KE = static_cast<int>(geo.ke);
+  unsigned char *base = reinterpret_cast<unsigned char *>(fu);
+  unsigned char *opA = base + (geo.off_opA - geo.off_fold);
+  unsigned char *opB = base + (geo.off_opB - geo.off_fold);
+  const int c = 32 * (warp & 3) + lane;
+  const int cur = (st + h) % L;
+
+  // acquire the unit (bounded)
+  int got = 1;
+  if (gtid == 0) {
+    const uint64_t t0 = global_ns();
+    while (atomicCAS(&fu->lock, 0, 1) != 0) {
+      if (global_ns() - t0 > kWaitLimitNs) {
+        got = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  if (named_bar_or(1 + gi, kGroupThreads, gtid == 0 && !got)) {
+    if (gtid == 0) set_err(a.err, RSSM_EBIT_TIMEOUT);
+    return;
+  }
+  tc05::fence_after_sync();
+  const uint32_t phase = fu->phase;
+
+  // A: row c = state column, K = slot (keys are exact in bf16)
+  for (int sl = 0; sl < KE; sl += 2) {
+    __nv_bfloat162 pr;
+    pr.x = (sl < L) ? (sl == cur ? kin[c] : kring[static_cast<size_t>(sl) * N + c]) : __float2bfloat16_rn(0.f);
+    pr.y = (sl + 1 < L) ? (sl + 1 == cur ? kin[c] : kring[static_cast<size_t>(sl + 1) * N + c])
+                        : __float2bfloat16_rn(0.f);
+    *reinterpret_cast<__nv_bfloat162 *>(opA + tc05::kmajor_offset(N, c, sl)) = pr;
+  }
+  // B: three terms of w_s v_s[r], row r of S_0, K = slot
+  const uint32_t term_bytes = static_cast<uint32_t>(d) * KE * 2u;
+  for (int idx = gtid; idx < d * (KE / 2); idx += kGroupThreads) {
+    const int sp = idx / d, r = idx - sp * d, s_0 = 2 * sp;
+    float w[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int sl = s_0 + u;
+      w[u] = 0.f;
+      if (sl < L) {
+        int e = sl - st;
+        if (e < 0) e += L;
+        const float vv = (sl == cur) ? load1(vin + r) : load1(vring + static_cast<size_t>(sl) * d + r);
+        w[u] = sc.wt[e] * vv;
+      }
+    }
+    __nv_bfloat162 t3[3];
+    tc05::split3_bf16(w[0], t3[0].x, t3[1].x, t3[2].x);
+    tc05::split3_bf16(w[1], t3[0].y, t3[1].y, t3[2].y);
+#pragma unroll
+    for (int t = 0; t < 3; ++t)
+      *reinterpret_cast<__nv_bfloat162 *>(opB + t * term_bytes + tc05::kmajor_offset(d, r, s_0)) = t3[t];
+  }
+  tc05::fence_proxy_async_smem();
+  named_bar(1 + gi, kGroupThreads);
+  if (gtid == 0) {
+    tc05::fence_after_sync();
+    const uint32_t idesc = tc05::idesc_bf16_f32(N, d);
+    bool acc = false;
+    for (int t = 0; t < 3; ++t)
+      for (int ks = 0; ks < KE / 16; ++ks) {
+        tc05::mma_bf16(fu->tmem, tc05::smem_desc(opA + ks * N * 32, tc05::kLBO, tc05::kSBO),
+                       tc05::smem_desc(opB + t * term_bytes + ks * d * 32, tc05::kLBO, tc05::kSBO), idesc, acc);
+        acc = true;
+      }
+    tc05::commit(&fu->bar);
+  }
+  const bool timed_out = !mbar_wait(&fu->bar, phase);
+  const bool fail = named_bar_or(1 + gi, kGroupThreads, timed_out);
+  if (!fail) {
+    tc05::fence_after_sync();
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    for (int r0 = 0; r0 < d; r0 += 32) {
+      float dv[32];
+      tc05::ld_32x32b_x32(fu->tmem + lane_base + static_cast<uint32_t>(r0), dv);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        const int r = r0 + u;
+        __stcs(S0g + static_cast<size_t>(r) * N + c, fmaf(abar, s0[static_cast<size_t>(r) * N + c], dv[u]));
+      }
+    }
+  } else if (gtid == 0) {
+    set_err(a.err, RSSM_EBIT_TIMEOUT);
+  }
+  // release the unit
+  tc05::fence_before_sync();
+  named_bar(1 + gi, kGroupThreads);
+  if (gtid == 0) {
+    fu->phase = phase ^ 1u;
+    __threadfence_block();
+    atomicExch(&fu->lock, 0);
+  }
+}
+
+template <int N, bool kFuse, bool kTc, typename TI, typename TO>
 __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launch a, PipeGeom geo) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int NS = geo.stages;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(NS) * geo.stage_bytes);
   uint64_t *empty = full + kMaxStages;
-  GroupScratch *scratch = reinterpret_cast<GroupScratch *>(empty + kMaxStages);
+  int *ticket = reinterpret_cast<int *>(empty + kMaxStages);  // next item to start
+  GroupScratch *scratch = reinterpret_cast<GroupScratch *>(ticket + 4);
   ItemMeta *meta = reinterpret_cast<ItemMeta *>(scratch + kGroups);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -87,14 +216,27 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
   const int n_items = max(0, it1 - it0);
   constexpr uint32_t es = sizeof(TI);
 
+  FoldUnit *fu = reinterpret_cast<FoldUnit *>(smem + geo.off_fold);
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, kGroupWarps);
     }
+    if (kTc) {
+      mbar_init(&fu->bar, 1);
+      fu->lock = 0;
+      fu->phase = 0;
+    }
+    *ticket = 0;
     fence_mbar_init();
   }
+  if (kTc && warp == 1) {
+    tc05::alloc(&fu->tmem, geo.ncols);
+    tc05::relinquish();
+  }
+  tc05::fence_before_sync();
   __syncthreads();
+  tc05::fence_after_sync();
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
@@ -131,14 +273,17 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
         if (lane == 0) set_err(a.err, RSSM_EBIT_TIMEOUT);
         break;
       }
+      // lane 0 posts the expected bytes and issues every copy of the item (the
+      // small copies issued from several lanes at once measured slower)
       if (lane == 0) {
         const ItemMeta m = meta[it];
         const int h = m.h, st = m.st;
         const int item = it0 + it;
         const int i = item / B, b = item - i * B, g = i / HpG;
         unsigned char *sb = smem + static_cast<size_t>(stage) * geo.stage_bytes;
-        StageHdr *hdr = reinterpret_cast<StageHdr *>(sb + geo.off_hdr);
         const bool valid = h >= 0 && h < L && st >= 0 && st < L;
+        uint64_t *bar = full + stage;
+        StageHdr *hdr = reinterpret_cast<StageHdr *>(sb + geo.off_hdr);
         hdr->h = h;
         hdr->st = st;
         hdr->valid = valid ? 1 : 0;
@@ -151,22 +296,20 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
           const size_t bg = static_cast<size_t>(b) * a.G + g;
           const uint32_t bytes = static_cast<uint32_t>(d) * N * 4u + static_cast<uint32_t>(h) * (d + N) * es +
                                  static_cast<uint32_t>(L) * 4u + static_cast<uint32_t>(d + 2 * N) * es;
-          uint64_t *bar = full + stage;
           mbar_arrive_expect_tx(bar, bytes);
           bulk_g2s(sb, a.S + bh * d * N, static_cast<uint32_t>(d) * N * 4u, bar);
           const TI *rv = static_cast<const TI *>(a.ring_v) + bh * L * d;
           const TI *rk = static_cast<const TI *>(a.ring_k) + bg * L * N;
-          const int seg1 = min(h, L - st);
+          const int seg1 = min(h, L - st), seg2 = h - seg1;
           if (seg1 > 0) {
             bulk_g2s(sb + geo.off_vring + static_cast<size_t>(st) * d * es, rv + static_cast<size_t>(st) * d,
                      static_cast<uint32_t>(seg1) * d * es, bar);
             bulk_g2s(sb + geo.off_kring + static_cast<size_t>(st) * N * es, rk + static_cast<size_t>(st) * N,
                      static_cast<uint32_t>(seg1) * N * es, bar);
           }
-          if (h > seg1) {
-            const uint32_t seg2 = static_cast<uint32_t>(h - seg1);
-            bulk_g2s(sb + geo.off_vring, rv, seg2 * d * es, bar);
-            bulk_g2s(sb + geo.off_kring, rk, seg2 * N * es, bar);
+          if (seg2 > 0) {
+            bulk_g2s(sb + geo.off_vring, rv, static_cast<uint32_t>(seg2) * d * es, bar);
+            bulk_g2s(sb + geo.off_kring, rk, static_cast<uint32_t>(seg2) * N * es, bar);
           }
           bulk_g2s(sb + geo.off_dtring, a.ring_dt + bh * L, static_cast<uint32_t>(L) * 4u, bar);
           bulk_g2s(sb + geo.off_vin, static_cast<const TI *>(a.v) + bh * d, static_cast<uint32_t>(d) * es, bar);
@@ -174,7 +317,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
           bulk_g2s(sb + geo.off_qin, static_cast<const TI *>(a.q) + bg * N, static_cast<uint32_t>(N) * es, bar);
         } else {
           set_err(a.err, RSSM_EBIT_COUNT_RANGE);
-          mbar_arrive(full + stage);
+          mbar_arrive(bar);
         }
       }
       __syncwarp();
@@ -194,10 +337,30 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
 
   for (int it = gi; it < n_items; it += kGroups) {
     const int stage = it % NS;
-    if (!mbar_wait(full + stage, (it / NS) & 1)) {
+    // Items are started in order: a group waits for this item's stage only
+    // after the previous item's fill has been observed (ticket == it).  Then
+    // the previous use of this stage has landed, the barrier sits in this
+    // use's phase or the one after it, and one parity wait is exact.  (Without
+    // the ticket a group running ahead could meet the stage one phase early,
+    // where a parity wait passes at once.)
+    bool timed_out = false;
+    if (gtid == 0) {
+      const uint64_t t0 = global_ns();
+      while (ld_volatile(ticket) != it)
+        if (global_ns() - t0 > kWaitLimitNs) {
+          timed_out = true;
+          break;
+        }
+    }
+    if (!named_bar_or(1 + gi, kGroupThreads, timed_out))
+      timed_out = !mbar_wait(full + stage, static_cast<uint32_t>(it / NS) & 1u);
+    else
+      timed_out = true;
+    if (named_bar_or(1 + gi, kGroupThreads, timed_out)) {  // same decision in the whole group
       if (gtid == 0) set_err(a.err, RSSM_EBIT_TIMEOUT);
       break;
     }
+    if (gtid == 0) st_volatile(ticket, it + 1);
     const unsigned char *sb = smem + static_cast<size_t>(stage) * geo.stage_bytes;
     const StageHdr hdr = *reinterpret_cast<const StageHdr *>(sb + geo.off_hdr);
     if (hdr.valid) {
@@ -282,7 +445,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
         TI *rk_out = static_cast<TI *>(a.ring_k) + ((static_cast<size_t>(b) * a.G + g) * L + slot) * N;
         for (int c = gtid; c < N; c += kGroupThreads) rk_out[c] = kin[c];
       }
-      if (kFuse && p == L) {
+      if constexpr (kTc) {
+        if (p == L) {
+          // The buffer is full after this append: fold all L entries into S_0
+          // with this step's weights on the tensor core (see fold_tc).
+          fold_tc<N, TI>(a, geo, fu, sc, gi, gtid, warp, lane, s0, kring, vring, kin, vin, st, h, abar,
+                         a.S + bh * d * N);
+        }
+      } else if (kFuse && p == L) {
         // The buffer is full after this append: fold all L entries into S_0
         // with this step's weights, S_0 <- abar S_0 + sum_j s_j v_j k_j^T,
         // reading S_0 and the entries from the stage in shared memory.
@@ -326,6 +496,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + stage);
   }
+  if (kTc) {
+    // every consumer warp is done with TMEM before warp 1 releases it
+    tc05::fence_before_sync();
+    named_bar(15, kGroups * kGroupThreads);
+    tc05::fence_after_sync();
+    if (warp == 1) tc05::dealloc(fu->tmem, geo.ncols);
+  }
 }
 
 template <int N, bool kFuse, typename TI, typename TO>
@@ -354,17 +531,32 @@ cudaError_t launch_pipe_n(const M2Launch &a, cudaStream_t stream, bool *launched
   off = al(off + N * es);
   geo.off_hdr = off;
   geo.stage_bytes = al(off + sizeof(StageHdr));
-  const uint32_t fixed = 2u * kMaxStages * 8u + kGroups * sizeof(GroupScratch) + kItemMax * sizeof(ItemMeta);
+  constexpr bool tc = kFuse && N == 128 && sizeof(TI) == 2;
+  const bool use_tc = tc && a.d % 32 == 0 && a.d <= 256 && a.L <= kMaxL;
+  geo.ke = a.L <= 16 ? 16u : 32u;
+  geo.ncols = 32;
+  while (geo.ncols < static_cast<uint32_t>(a.d)) geo.ncols <<= 1;
+  const uint32_t fold_bytes =
+      use_tc ? al(sizeof(FoldUnit)) + 128u * geo.ke * 2u + 3u * static_cast<uint32_t>(a.d) * geo.ke * 2u : 0u;
+  const uint32_t fixed =
+      2u * kMaxStages * 8u + 16u + kGroups * sizeof(GroupScratch) + kItemMax * sizeof(ItemMeta) + fold_bytes + 128u;
   const int stages = static_cast<int>((static_cast<uint32_t>(optin) - fixed) / geo.stage_bytes);
-  if (stages < 2) return cudaSuccess;  // not launched: the caller uses the per-head kernel
+  if (stages < kGroups) return cudaSuccess;  // not launched: the caller uses the per-head kernel
   geo.stages = stages < kMaxStages ? stages : kMaxStages;
+  {
+    const uint32_t head = static_cast<uint32_t>(geo.stages) * geo.stage_bytes + 2u * kMaxStages * 8u + 16u +
+                          kGroups * sizeof(GroupScratch) + kItemMax * sizeof(ItemMeta);
+    geo.off_fold = al(head);
+    geo.off_opA = geo.off_fold + al(sizeof(FoldUnit));
+    geo.off_opB = geo.off_opA + 128u * geo.ke * 2u;
+  }
   const int total = a.B * a.H;
   int grid = total < sms ? total : sms;
   geo.items_per_cta = (total + grid - 1) / grid;
   if (geo.items_per_cta > kItemMax) geo.items_per_cta = kItemMax;
   grid = (total + geo.items_per_cta - 1) / geo.items_per_cta;
   const size_t smem = static_cast<size_t>(geo.stages) * geo.stage_bytes + fixed;
-  auto kern = m2_decode_pipe_kernel<N, kFuse, TI, TO>;
+  auto kern = use_tc ? m2_decode_pipe_kernel<N, kFuse, tc, TI, TO> : m2_decode_pipe_kernel<N, kFuse, false, TI, TO>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
       cudaSuccess)
     return e;

@@ -71,5 +71,7 @@ struct FlushLaunch {
 };
 
 cudaError_t launch_flush(const FlushLaunch &a, cudaStream_t stream);
+// The tensor-core flush applies (n = 128, bf16 keys, d a multiple of 32).
+bool flush_tc_eligible(const FlushLaunch &a);
 
 }  // namespace rssm

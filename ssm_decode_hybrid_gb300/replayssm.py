@@ -15,7 +15,8 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libreplayssm.so")
+# REPLAYSSM_LIB points the binding at another build of the same library.
+LIB_PATH = os.environ.get("REPLAYSSM_LIB") or os.path.join(_HERE, "libreplayssm.so")
 
 F32, BF16 = 0, 1
 EBIT_COUNT_RANGE, EBIT_WINDOW, EBIT_ACCEPTED, EBIT_CUR = 1, 2, 4, 8

@@ -62,10 +62,13 @@ SHAPES = [
     wl.GdnShape(B=3, Hv=4, Hk=4, dk=64, dv=68, L=7, in_dtype=wl.BF16),
     wl.GdnShape(B=4, Hv=8, Hk=4, dk=128, dv=128, L=16, in_dtype=wl.BF16),  # the GDN layer, small batch
     wl.GdnShape(B=2, Hv=2, Hk=1, dk=128, dv=136, L=1, in_dtype=wl.F32),
+    wl.GdnShape(B=2, Hv=4, Hk=2, dk=128, dv=128, L=32, in_dtype=wl.BF16),  # tensor-core flush, K extent 64
+    wl.GdnShape(B=3, Hv=2, Hk=2, dk=128, dv=64, L=3, in_dtype=wl.BF16, u_dtype=wl.BF16),  # bf16 u, padded K
 ]
 
 
-@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{s.B}Hv{s.Hv}Hk{s.Hk}dk{s.dk}dv{s.dv}L{s.L}{s.in_dtype}")
+@pytest.mark.parametrize("shape", SHAPES,
+                         ids=lambda s: f"B{s.B}Hv{s.Hv}Hk{s.Hk}dk{s.dk}dv{s.dv}L{s.L}{s.in_dtype}u{s.u_dtype}")
 def test_decode_parity(shape):
     run_decode(shape, 200, steps=2 * shape.L + 3)
 

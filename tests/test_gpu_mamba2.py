@@ -69,6 +69,8 @@ SHAPES = [
     wl.Mamba2Shape(B=3, H=4, G=1, d=136, n=128, L=32, in_dtype=wl.BF16),  # two row chunks + tail
     wl.Mamba2Shape(B=2, H=2, G=2, d=4, n=128, L=1, in_dtype=wl.F32),  # flush every step
     wl.Mamba2Shape(B=6, H=32, G=8, d=64, n=128, L=16, in_dtype=wl.BF16),  # the Nemotron-H layer, small batch
+    wl.Mamba2Shape(B=3, H=4, G=2, d=96, n=128, L=32, in_dtype=wl.BF16),  # tensor-core flush, K extent 64
+    wl.Mamba2Shape(B=2, H=2, G=1, d=32, n=128, L=5, in_dtype=wl.BF16),  # tensor-core flush, zero-padded K
 ]
 
 
