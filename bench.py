@@ -275,7 +275,7 @@ def run_gpu(args):
                           to(init.ring_dt), to(init.start, torch.int32), to(init.count, torch.int32),
                           torch.zeros(shape.B, dtype=torch.int32, device=dev),
                           torch.zeros(shape.B, dtype=torch.int32, device=dev),
-                          torch.zeros(1, dtype=torch.int32, device=dev))
+                          torch.zeros(1, dtype=torch.int32, device=dev)).add_workspace()
     A = to(init.A)
     host_in = []
     for p in range(POOL):

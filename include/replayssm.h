@@ -100,6 +100,8 @@ typedef struct {
   float *ring_dt;
   int32_t *start, *count, *flag, *sync;
   int32_t *err; /* one int32 */
+  float *work;  /* optional decode workspace of replay_decode_workspace_bytes()
+                   bytes, 16-byte aligned, or NULL (see replay_decode_step) */
 } rssm_m2_replay;
 
 typedef struct {
@@ -139,10 +141,20 @@ RSSM_API rssm_status ssm_state_update_baseline(const rssm_m2_dims *dims, float *
  *   abar = prod_{i<=h+1} a_i,  s_j = Delta_j prod_{j<i<=h+1} a_i,  a_i = exp(A Delta_i);
  * then count <- h+1 and flag <- (count == L).  S_0 is only read.  Inputs as for
  * the baseline.  A sequence whose start/count is out of range is skipped and
- * sets RSSM_EBIT_COUNT_RANGE.                                                 */
+ * sets RSSM_EBIT_COUNT_RANGE.
+ * With st->work non-NULL the step runs as two launches ("Kernel design
+ * details": a small precompute kernel for the ring-dependent terms, then a
+ * main kernel streaming S_0); the workspace holds per (sequence, head) the
+ * precomputed terms between them and carries nothing from one call to the
+ * next.  With st->work NULL one launch does both (same results).             */
 RSSM_API rssm_status replay_decode_step(const rssm_m2_dims *dims, const rssm_m2_replay *st, const void *v,
                                const void *k, const void *q, const float *dt, const float *A, void *y,
                                rssm_stream_t stream);
+
+/* Bytes of the optional decode workspace (rssm_m2_replay.work) for dims:
+ * B * H * 4 * ceil((d + L + 4) / 4) floats.  Returns 0 for invalid dims.
+ * Host only; launches nothing.                                                */
+RSSM_API int64_t replay_decode_workspace_bytes(const rssm_m2_dims *dims);
 
 /* Flush ("Algorithm -- Mamba-2 standard decode", flush): for every sequence
  * with flag[b] != 0 and c = count[b] committed entries,

@@ -82,7 +82,7 @@ GdnLaunch gdn_launch(const rssm_gdn_dims &d) {
 bool m2_replay_ok(const rssm_m2_dims &d, const rssm_m2_replay *s, bool need_sync) {
   return s != nullptr && ok16(s->S0) && ok_elem(s->ring_v, d.in_dtype) && ok16(s->ring_k) && ok4(s->ring_dt) &&
          ok4(s->start) && ok4(s->count) && ok4(s->flag) && (!need_sync || ok4(s->sync)) &&
-         (s->err == nullptr || aligned(s->err, 4));
+         (s->err == nullptr || aligned(s->err, 4)) && (s->work == nullptr || aligned(s->work, 16));
 }
 
 bool gdn_replay_ok(const rssm_gdn_dims &d, const rssm_gdn_replay *s, bool need_sync) {
@@ -117,6 +117,11 @@ const char *rssm_status_string(rssm_status s) {
 const char *rssm_last_cuda_error(void) { return g_last_cuda_error; }
 
 // ------------------------------- Mamba-2 ---------------------------------
+
+int64_t replay_decode_workspace_bytes(const rssm_m2_dims *dims) {
+  if (check_m2_dims(dims) != RSSM_OK) return 0;
+  return static_cast<int64_t>(dims->B) * dims->H * work_stride_floats(dims->d, dims->L) * 4;
+}
 
 rssm_status ssm_state_update_baseline(const rssm_m2_dims *dims, float *S, const void *v, const void *k,
                                       const void *q, const float *dt, const float *A, void *y,
@@ -161,6 +166,7 @@ rssm_status replay_decode_step(const rssm_m2_dims *dims, const rssm_m2_replay *s
   a.dt = dt;
   a.A = A;
   a.y = y;
+  a.work = s->work;
   return cuda_status(launch_m2(M2Kind::Decode, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -191,6 +197,7 @@ rssm_status replay_decode_step_fused(const rssm_m2_dims *dims, const rssm_m2_rep
   a.dt = dt;
   a.A = A;
   a.y = y;
+  a.work = s->work;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_m2(M2Kind::DecodeFused, a, cs);
   if (e != cudaErrorNotSupported) return cuda_status(e);

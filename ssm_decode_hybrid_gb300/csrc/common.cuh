@@ -221,3 +221,15 @@ __device__ __forceinline__ bool named_bar_or(int id, int threads, bool pred) {
 }
 
 }  // namespace rssm
+
+namespace rssm {
+
+// Per-thread 16-byte asynchronous copy global -> shared (L1 bypassed); the
+// thread waits for its own copies with cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+}  // namespace rssm

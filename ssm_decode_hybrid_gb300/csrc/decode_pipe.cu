@@ -7,19 +7,20 @@
 // decode" (output-only decode; "if the buffer is full, flush") and "Kernel
 // design details" (ring buffer with in-kernel indexing).
 //
-// Roles.  Warp 0 is the producer.  Per item, one lane waits for a free stage
-// and issues the copies: the d x n fp32 block of S_0 (one contiguous copy),
-// the committed ring slots of v and k (one or two contiguous segments, copied
-// into the same slot positions of a shared-memory ring), the item's Delta
-// ring, and this step's v, k, q.  The whole producer warp reads the per-item
-// metadata (start, count, this step's Delta, A) 32 items at a time, one batch
-// ahead of the copies, and counts the items' arrivals for the pointer update,
-// so no dependent load sits on the copy path.  kGroups consumer groups of four
-// warps take items in turn: decay weights (suffix scan over <= 32 entries in
-// one warp), k_j^T q (one lane group per entry), the buffer term, S_0 q from
-// the shared-memory tile; then y and the appended ring entry go to HBM.  With
-// the flush fused, an item whose buffer fills is folded into S_0 from the
-// same shared-memory stage.
+// Roles.  Warp 0 is the producer: per item, one lane waits for a free stage
+// and issues a single bulk copy, the item's d x n fp32 block of S_0 (one
+// contiguous region).  One request per item keeps the TMA engine streaming;
+// every other byte of the item -- the committed ring slots of v and k, the
+// Delta ring, this step's v, k, q -- is fetched by the consumer group itself
+// with 16-byte cp.async copies into its private double buffer, one item
+// ahead (while it computes the current item).  The producer warp also reads
+// the per-item metadata (start, count, this step's Delta, A) 32 items at a
+// time and counts the items' arrivals for the pointer update.  kGroups
+// consumer groups of four warps take items in turn: decay weights (suffix
+// scan over <= 32 entries in one warp), k_j^T q (one lane group per entry),
+// the buffer term, S_0 q from the shared-memory tile; then y and the appended
+// ring entry go to HBM.  With the flush fused, an item whose buffer fills is
+// folded into S_0 from the same shared-memory data.
 //
 // Work split.  Items are numbered head-major, item = i * B + b, and CTA c
 // takes a contiguous run of them.  Each item's S_0 block is one contiguous
@@ -40,13 +41,7 @@ constexpr int kGroupThreads = 32 * kGroupWarps;
 constexpr int kPipeThreads = 32 + kGroups * kGroupThreads;
 constexpr int kMaxStages = 8;
 constexpr int kMaxRows = 256;
-constexpr int kItemMax = 512;  // items per CTA (metadata table size)
-
-struct alignas(16) StageHdr {
-  int h, st, valid, b;
-  int i, pad0, pad1, pad2;
-  float dt_in, A, pad3, pad4;
-};
+constexpr int kItemMax = 256;  // items per CTA (metadata table size)
 
 struct ItemMeta {
   int h, st;
@@ -64,8 +59,10 @@ struct GroupScratch {
 
 struct PipeGeom {
   int stages, items_per_cta;
-  uint32_t stage_bytes;
-  uint32_t off_vring, off_kring, off_dtring, off_vin, off_kin, off_qin, off_hdr;
+  uint32_t stage_bytes;  // S_0 tile of one item
+  // per-group double buffer of the item's small data: offsets inside one buffer
+  uint32_t pbuf_bytes, off_vring, off_kring, off_dtring, off_vin, off_kin, off_qin;
+  uint32_t off_pbufs, off_meta;
   // tensor-core fold unit (fused flush): offsets from the end of the stages
   uint32_t off_fold, off_opA, off_opB, ke, ncols;
 };
@@ -197,6 +194,61 @@ __device__ __forceinline__ void fold_tc(const M2Launch &a, const PipeGeom &geo, 
   }
 }
 
+// Consumer-side fetch of one item's small data into a group buffer: the
+// committed ring slots of v and k (at their slot positions), the Delta ring,
+// and this step's v, k, q, as 16-byte cp.async copies spread over the group.
+template <int N, typename TI>
+__device__ __forceinline__ void prefetch_item(const M2Launch &a, const PipeGeom &geo, const ItemMeta &m, int item,
+                                              unsigned char *pb, int gtid) {
+  const int B = a.B, H = a.H, d = a.d, L = a.L;
+  if (!(m.h >= 0 && m.h < L && m.st >= 0 && m.st < L)) return;
+  constexpr int es = sizeof(TI);
+  constexpr int kc = N * es / 16;  // 16-byte chunks per key slot (a power of two)
+  const int i = item / B, b = item - i * B, g = i / (H / a.G);
+  const size_t bh = static_cast<size_t>(b) * H + i, bg = static_cast<size_t>(b) * a.G + g;
+  const int h = m.h, st = m.st;
+  const int vc = d * es / 16;
+  const unsigned char *rv = static_cast<const unsigned char *>(a.ring_v) + bh * L * d * es;
+  const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + bg * L * N * es;
+  // keys: thread t takes chunk t % kc of entries t / kc, t / kc + 128 / kc, ...
+  {
+    const int c = gtid % kc;
+    for (int j = gtid / kc; j < h; j += kGroupThreads / kc) {
+      const int off = (wrap(st + j, L) * kc + c) * 16;
+      cp_async16(pb + geo.off_kring + off, rk + off);
+    }
+  }
+  // values: rows of vc chunks, walked with a running (entry, chunk) pair
+  {
+    int j = gtid / vc, c = gtid - (gtid / vc) * vc;
+    const int jstep = kGroupThreads / vc, cstep = kGroupThreads - jstep * vc;
+    for (; j < h;) {
+      const int off = (wrap(st + j, L) * vc + c) * 16;
+      cp_async16(pb + geo.off_vring + off, rv + off);
+      j += jstep;
+      c += cstep;
+      if (c >= vc) {
+        c -= vc;
+        ++j;
+      }
+    }
+  }
+  // Delta ring, this step's v, k, q
+  const int dc = L / 4;
+  if (gtid < dc) {
+    cp_async16(pb + geo.off_dtring + gtid * 16, reinterpret_cast<const unsigned char *>(a.ring_dt + bh * L) + gtid * 16);
+  } else if (gtid < dc + vc) {
+    const int c = gtid - dc;
+    cp_async16(pb + geo.off_vin + c * 16, static_cast<const unsigned char *>(a.v) + bh * d * es + c * 16);
+  } else if (gtid < dc + vc + kc) {
+    const int c = gtid - dc - vc;
+    cp_async16(pb + geo.off_kin + c * 16, static_cast<const unsigned char *>(a.k) + bg * N * es + c * 16);
+  } else if (gtid < dc + vc + 2 * kc) {
+    const int c = gtid - dc - vc - kc;
+    cp_async16(pb + geo.off_qin + c * 16, static_cast<const unsigned char *>(a.q) + bg * N * es + c * 16);
+  }
+}
+
 template <int N, bool kFuse, bool kTc, typename TI, typename TO>
 __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launch a, PipeGeom geo) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -205,7 +257,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
   uint64_t *empty = full + kMaxStages;
   int *ticket = reinterpret_cast<int *>(empty + kMaxStages);  // next item to start
   GroupScratch *scratch = reinterpret_cast<GroupScratch *>(ticket + 4);
-  ItemMeta *meta = reinterpret_cast<ItemMeta *>(scratch + kGroups);
+  unsigned char *pbufs = smem + geo.off_pbufs;
+  ItemMeta *meta = reinterpret_cast<ItemMeta *>(smem + geo.off_meta);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = a.B, H = a.H, d = a.d, L = a.L;
@@ -214,7 +267,6 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
   const int it0 = blockIdx.x * geo.items_per_cta;
   const int it1 = min(total, it0 + geo.items_per_cta);
   const int n_items = max(0, it1 - it0);
-  constexpr uint32_t es = sizeof(TI);
 
   FoldUnit *fu = reinterpret_cast<FoldUnit *>(smem + geo.off_fold);
   if (tid == 0) {
@@ -273,48 +325,16 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
         if (lane == 0) set_err(a.err, RSSM_EBIT_TIMEOUT);
         break;
       }
-      // lane 0 posts the expected bytes and issues every copy of the item (the
-      // small copies issued from several lanes at once measured slower)
       if (lane == 0) {
         const ItemMeta m = meta[it];
-        const int h = m.h, st = m.st;
         const int item = it0 + it;
-        const int i = item / B, b = item - i * B, g = i / HpG;
-        unsigned char *sb = smem + static_cast<size_t>(stage) * geo.stage_bytes;
-        const bool valid = h >= 0 && h < L && st >= 0 && st < L;
+        const int i = item / B, b = item - i * B;
         uint64_t *bar = full + stage;
-        StageHdr *hdr = reinterpret_cast<StageHdr *>(sb + geo.off_hdr);
-        hdr->h = h;
-        hdr->st = st;
-        hdr->valid = valid ? 1 : 0;
-        hdr->b = b;
-        hdr->i = i;
-        hdr->dt_in = m.dt;
-        hdr->A = m.A;
-        if (valid) {
+        if (m.h >= 0 && m.h < L && m.st >= 0 && m.st < L) {
           const size_t bh = static_cast<size_t>(b) * H + i;
-          const size_t bg = static_cast<size_t>(b) * a.G + g;
-          const uint32_t bytes = static_cast<uint32_t>(d) * N * 4u + static_cast<uint32_t>(h) * (d + N) * es +
-                                 static_cast<uint32_t>(L) * 4u + static_cast<uint32_t>(d + 2 * N) * es;
-          mbar_arrive_expect_tx(bar, bytes);
-          bulk_g2s(sb, a.S + bh * d * N, static_cast<uint32_t>(d) * N * 4u, bar);
-          const TI *rv = static_cast<const TI *>(a.ring_v) + bh * L * d;
-          const TI *rk = static_cast<const TI *>(a.ring_k) + bg * L * N;
-          const int seg1 = min(h, L - st), seg2 = h - seg1;
-          if (seg1 > 0) {
-            bulk_g2s(sb + geo.off_vring + static_cast<size_t>(st) * d * es, rv + static_cast<size_t>(st) * d,
-                     static_cast<uint32_t>(seg1) * d * es, bar);
-            bulk_g2s(sb + geo.off_kring + static_cast<size_t>(st) * N * es, rk + static_cast<size_t>(st) * N,
-                     static_cast<uint32_t>(seg1) * N * es, bar);
-          }
-          if (seg2 > 0) {
-            bulk_g2s(sb + geo.off_vring, rv, static_cast<uint32_t>(seg2) * d * es, bar);
-            bulk_g2s(sb + geo.off_kring, rk, static_cast<uint32_t>(seg2) * N * es, bar);
-          }
-          bulk_g2s(sb + geo.off_dtring, a.ring_dt + bh * L, static_cast<uint32_t>(L) * 4u, bar);
-          bulk_g2s(sb + geo.off_vin, static_cast<const TI *>(a.v) + bh * d, static_cast<uint32_t>(d) * es, bar);
-          bulk_g2s(sb + geo.off_kin, static_cast<const TI *>(a.k) + bg * N, static_cast<uint32_t>(N) * es, bar);
-          bulk_g2s(sb + geo.off_qin, static_cast<const TI *>(a.q) + bg * N, static_cast<uint32_t>(N) * es, bar);
+          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(d) * N * 4u);
+          bulk_g2s(smem + static_cast<size_t>(stage) * geo.stage_bytes, a.S + bh * d * N,
+                   static_cast<uint32_t>(d) * N * 4u, bar);
         } else {
           set_err(a.err, RSSM_EBIT_COUNT_RANGE);
           mbar_arrive(bar);
@@ -335,16 +355,17 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
   GroupScratch &sc = scratch[gi];
   const int col = (lane % LPR) * 4;
 
-  for (int it = gi; it < n_items; it += kGroups) {
+  int j_iter = 0;
+  for (int it = gi; it < n_items; it += kGroups, ++j_iter) {
     const int stage = it % NS;
-    // Items are started in order: a group waits for this item's stage only
-    // after the previous item's fill has been observed (ticket == it).  Then
-    // the previous use of this stage has landed, the barrier sits in this
-    // use's phase or the one after it, and one parity wait is exact.  (Without
-    // the ticket a group running ahead could meet the stage one phase early,
-    // where a parity wait passes at once.)
+    // Items are started in order: every thread of the group waits for this
+    // item's stage only after the previous item's fill has been observed
+    // (ticket == it).  Then the previous use of this stage has landed, the
+    // barrier sits in this use's phase or the one after it, and one parity
+    // wait is exact.  (Without the ticket a group running ahead could meet the
+    // stage one phase early, where a parity wait passes at once.)
     bool timed_out = false;
-    if (gtid == 0) {
+    {
       const uint64_t t0 = global_ns();
       while (ld_volatile(ticket) != it)
         if (global_ns() - t0 > kWaitLimitNs) {
@@ -352,110 +373,156 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
           break;
         }
     }
-    if (!named_bar_or(1 + gi, kGroupThreads, timed_out))
-      timed_out = !mbar_wait(full + stage, static_cast<uint32_t>(it / NS) & 1u);
-    else
-      timed_out = true;
+    if (!timed_out) timed_out = !mbar_wait(full + stage, static_cast<uint32_t>(it / NS) & 1u);
+    // this item's small data: fetched during the previous item (or now, for
+    // the group's first item)
+    unsigned char *pb = pbufs + static_cast<size_t>(2 * gi + (j_iter & 1)) * geo.pbuf_bytes;
+    unsigned char *pb_next = pbufs + static_cast<size_t>(2 * gi + ((j_iter + 1) & 1)) * geo.pbuf_bytes;
+    const ItemMeta m = meta[it];  // written before the producer released this item
+    if (j_iter == 0 && !timed_out) {
+      prefetch_item<N, TI>(a, geo, m, it0 + it, pb, gtid);
+      cp_async_commit();
+    }
+    cp_async_wait_all();
     if (named_bar_or(1 + gi, kGroupThreads, timed_out)) {  // same decision in the whole group
       if (gtid == 0) set_err(a.err, RSSM_EBIT_TIMEOUT);
       break;
     }
     if (gtid == 0) st_volatile(ticket, it + 1);
+
     const unsigned char *sb = smem + static_cast<size_t>(stage) * geo.stage_bytes;
-    const StageHdr hdr = *reinterpret_cast<const StageHdr *>(sb + geo.off_hdr);
-    if (hdr.valid) {
-      const int h = hdr.h, st = hdr.st, p = h + 1, b = hdr.b, i = hdr.i, g = i / HpG;
+    bool released = false;
+    if (m.h >= 0 && m.h < L && m.st >= 0 && m.st < L) {
+      const int item = it0 + it;
+      const int i = item / B, b = item - i * B, g = i / HpG;
+      const int h = m.h, st = m.st, p = h + 1;
       const float *s0 = reinterpret_cast<const float *>(sb);
-      const TI *vring = reinterpret_cast<const TI *>(sb + geo.off_vring);
-      const TI *kring = reinterpret_cast<const TI *>(sb + geo.off_kring);
-      const float *dtring = reinterpret_cast<const float *>(sb + geo.off_dtring);
-      const TI *vin = reinterpret_cast<const TI *>(sb + geo.off_vin);
-      const TI *kin = reinterpret_cast<const TI *>(sb + geo.off_kin);
-      const TI *qin = reinterpret_cast<const TI *>(sb + geo.off_qin);
+      const TI *vring = reinterpret_cast<const TI *>(pb + geo.off_vring);
+      const TI *kring = reinterpret_cast<const TI *>(pb + geo.off_kring);
+      const float *dtring = reinterpret_cast<const float *>(pb + geo.off_dtring);
+      const TI *vin = reinterpret_cast<const TI *>(pb + geo.off_vin);
+      const TI *kin = reinterpret_cast<const TI *>(pb + geo.off_kin);
+      const TI *qin = reinterpret_cast<const TI *>(pb + geo.off_qin);
+      const bool fold = kFuse && p == L;
 
-      // phase A: decay weights and ring slots (warp 0), k_j^T q (all warps)
+      // phase 1: S_0 q per row first (all warps) so that each warp can hand
+      // its share of the stage back at once, then k_j^T q (all warps) and the
+      // decay weights and ring slots (warp 0) -- independent of each other
       const float4 q4 = load4(qin + col);
-      if (wg == 0) {
-        const int slot = wrap(st + lane, L);
-        const float dtj = (lane < h) ? dtring[slot] : (lane == h ? hdr.dt_in : 0.f);
-        float tot;
-        const float ex = excl_suffix_sum(hdr.A * dtj, lane, tot);
-        sc.wt[lane] = (lane < p) ? dtj * expf(ex) : 0.f;
-        sc.slot[lane] = slot;
-        if (lane == 0) sc.abar = expf(tot);
-      }
-      for (int jb = wg * RPW; jb < p; jb += RPP) {
-        const int j = jb + lane / LPR;
-        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < p) kv = load4((j < h ? kring + static_cast<size_t>(wrap(st + j, L)) * N : kin) + col);
-        const float m = group_sum<LPR>(dot4(kv, q4));
-        if (j < p && (lane % LPR) == 0) sc.M[j] = m;
-      }
-      named_bar(1 + gi, kGroupThreads);
-
-      // phase B: buffer term per row (four independent partial sums), S_0 q per row
-      const float abar = sc.abar;
-      for (int r = gtid; r < d; r += kGroupThreads) {
-        float acc0 = sc.wt[h] * sc.M[h] * load1(vin + r), acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-        int j = 0;
-        for (; j + 4 <= h; j += 4) {
-          acc0 = fmaf(sc.wt[j] * sc.M[j], load1(vring + static_cast<size_t>(sc.slot[j]) * d + r), acc0);
-          acc1 = fmaf(sc.wt[j + 1] * sc.M[j + 1], load1(vring + static_cast<size_t>(sc.slot[j + 1]) * d + r), acc1);
-          acc2 = fmaf(sc.wt[j + 2] * sc.M[j + 2], load1(vring + static_cast<size_t>(sc.slot[j + 2]) * d + r), acc2);
-          acc3 = fmaf(sc.wt[j + 3] * sc.M[j + 3], load1(vring + static_cast<size_t>(sc.slot[j + 3]) * d + r), acc3);
-        }
-        for (; j < h; ++j) acc0 = fmaf(sc.wt[j] * sc.M[j], load1(vring + static_cast<size_t>(sc.slot[j]) * d + r), acc0);
-        sc.buf[r] = (acc0 + acc1) + (acc2 + acc3);
-      }
-      for (int base = 0; base < d; base += 8 * RPP) {
-        float x[8];
+      // rows in batches of RB per lane group: RB independent shared-memory
+      // loads in flight, then one multi-value reduction (RB - 1 + log2(LPR/RB)
+      // shuffles), which keeps this latency-bound phase short
+      constexpr int RB = LPR >= 16 ? 16 : 8;
+      for (int base = 0; base < d; base += RB * RPP) {
+        float x[RB];
 #pragma unroll
-        for (int pp = 0; pp < 8; ++pp) {
+        for (int pp = 0; pp < RB; ++pp) {
           const int r = base + wg * RPW + lane / LPR + pp * RPP;
           x[pp] = (r < d) ? dot4(*reinterpret_cast<const float4 *>(s0 + static_cast<size_t>(r) * N + col), q4) : 0.f;
         }
-        if constexpr (8 <= LPR) {
-          group_sum_multi<LPR, 8>(x, lane);
-          constexpr int SPAN = LPR / 8;
+        if constexpr (RB <= LPR) {
+          group_sum_multi<LPR, RB>(x, lane);
+          constexpr int SPAN = LPR / RB;
           const int pp = (lane % LPR) / SPAN;
           const int r = base + wg * RPW + lane / LPR + pp * RPP;
           if ((lane % SPAN) == 0 && r < d) sc.dot[r] = x[0];
         } else {
 #pragma unroll
-          for (int pp = 0; pp < 8; ++pp) {
+          for (int pp = 0; pp < RB; ++pp) {
             const float t = group_sum<LPR>(x[pp]);
             const int r = base + wg * RPW + lane / LPR + pp * RPP;
             if ((lane % LPR) == 0 && r < d) sc.dot[r] = t;
           }
         }
       }
+      if (!fold) {
+        __syncwarp();  // this warp's rows of S_0 are read
+        if (lane == 0) mbar_arrive(empty + stage);
+        released = true;
+      }
+      // the next item's small data goes out now, into the other buffer
+      if (it + kGroups < n_items) {
+        prefetch_item<N, TI>(a, geo, meta[it + kGroups], it0 + it + kGroups, pb_next, gtid);
+        cp_async_commit();
+      }
+      if constexpr (LPR == 32) {
+        // four entries per warp per pass, reduced together
+        for (int jb = wg; jb < p; jb += 4 * kGroupWarps) {
+          float x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = jb + u * kGroupWarps;
+            x[u] = 0.f;
+            if (j < p) x[u] = dot4(load4((j < h ? kring + static_cast<size_t>(wrap(st + j, L)) * N : kin) + col), q4);
+          }
+          group_sum_multi<32, 4>(x, lane);
+          const int j = jb + (lane >> 3) * kGroupWarps;
+          if ((lane & 7) == 0 && j < p) sc.M[j] = x[0];
+        }
+      } else {
+        for (int jb = wg * RPW; jb < p; jb += RPP) {
+          const int j = jb + lane / LPR;
+          float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j < p) kv = load4((j < h ? kring + static_cast<size_t>(wrap(st + j, L)) * N : kin) + col);
+          const float mm = group_sum<LPR>(dot4(kv, q4));
+          if (j < p && (lane % LPR) == 0) sc.M[j] = mm;
+        }
+      }
+      if (wg == 0) {
+        const int slot = wrap(st + lane, L);
+        const float dtj = (lane < h) ? dtring[slot] : (lane == h ? m.dt : 0.f);
+        float tot;
+        const float ex = excl_suffix_sum(m.A * dtj, lane, tot);
+        sc.wt[lane] = (lane < p) ? dtj * expf(ex) : 0.f;
+        sc.slot[lane] = slot;
+        if (lane == 0) sc.abar = expf(tot);
+      }
       named_bar(1 + gi, kGroupThreads);
+      if (gtid < p) sc.M[gtid] *= sc.wt[gtid];  // c_j = w_j (k_j^T q), read after the next barrier
 
-      // phase C: y, the appended ring entry
+      // phase 2: y = abar (S_0 q) + sum_j c_j v_j; the appended entry
+      named_bar(1 + gi, kGroupThreads);
+      const float abar = sc.abar;
       const size_t bh = static_cast<size_t>(b) * H + i;
       const int slot = wrap(st + h, L);
       TO *y = static_cast<TO *>(a.y) + bh * d;
       TI *rv_out = static_cast<TI *>(a.ring_v) + (bh * L + slot) * d;
-      for (int r = gtid; r < d; r += kGroupThreads) {
-        store1(y + r, fmaf(abar, sc.dot[r], sc.buf[r]));
-        rv_out[r] = vin[r];
+      // two adjacent lanes per row, each summing every other entry
+      for (int rb = 0; rb < d; rb += kGroupThreads / 2) {
+        const int r = rb + (gtid >> 1), par = gtid & 1;
+        float acc0 = 0.f, acc1 = 0.f;
+        if (r < d) {
+          if (par == 0) acc0 = sc.M[h] * load1(vin + r);
+          int j = par;
+          for (; j + 2 < h; j += 4) {
+            acc0 = fmaf(sc.M[j], load1(vring + static_cast<size_t>(sc.slot[j]) * d + r), acc0);
+            acc1 = fmaf(sc.M[j + 2], load1(vring + static_cast<size_t>(sc.slot[j + 2]) * d + r), acc1);
+          }
+          for (; j < h; j += 2) acc0 = fmaf(sc.M[j], load1(vring + static_cast<size_t>(sc.slot[j]) * d + r), acc0);
+        }
+        float acc = acc0 + acc1;
+        acc += __shfl_xor_sync(kFull, acc, 1);
+        if (r < d && par == 0) {
+          store1(y + r, fmaf(abar, sc.dot[r], acc));
+          rv_out[r] = vin[r];
+        }
       }
-      if (gtid == 0) a.ring_dt[bh * L + slot] = hdr.dt_in;
+      if (gtid == 0) a.ring_dt[bh * L + slot] = m.dt;
       if (i % HpG == 0) {
         TI *rk_out = static_cast<TI *>(a.ring_k) + ((static_cast<size_t>(b) * a.G + g) * L + slot) * N;
         for (int c = gtid; c < N; c += kGroupThreads) rk_out[c] = kin[c];
       }
       if constexpr (kTc) {
-        if (p == L) {
+        if (fold) {
           // The buffer is full after this append: fold all L entries into S_0
           // with this step's weights on the tensor core (see fold_tc).
           fold_tc<N, TI>(a, geo, fu, sc, gi, gtid, warp, lane, s0, kring, vring, kin, vin, st, h, abar,
                          a.S + bh * d * N);
         }
-      } else if (kFuse && p == L) {
+      } else if (fold) {
         // The buffer is full after this append: fold all L entries into S_0
         // with this step's weights, S_0 <- abar S_0 + sum_j s_j v_j k_j^T,
-        // reading S_0 and the entries from the stage in shared memory.
+        // reading S_0 and the entries from shared memory.
         float *S0g = a.S + bh * d * N;
         constexpr int CG = N / 4;                  // column groups of 4
         constexpr int RSTEP = kGroupThreads / CG;  // rows covered per pass
@@ -492,10 +559,20 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
           }
         }
       }
+      // phase 2 reads sc.* and the group buffer; the next item overwrites
+      // them only after its own vote barrier, which every thread reaches
+      // after finishing this item
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty + stage);
+    else if (it + kGroups < n_items) {
+      prefetch_item<N, TI>(a, geo, meta[it + kGroups], it0 + it + kGroups, pb_next, gtid);
+      cp_async_commit();
+    }
+    if (!released) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + stage);
+    }
   }
+  cp_async_wait_all();  // no copy of this thread outlives the kernel
   if (kTc) {
     // every consumer warp is done with TMEM before warp 1 releases it
     tc05::fence_before_sync();
@@ -516,21 +593,22 @@ cudaError_t launch_pipe_n(const M2Launch &a, cudaStream_t stream, bool *launched
   const uint32_t es = sizeof(TI);
   auto al = [](uint32_t x) { return (x + 127u) & ~127u; };
   PipeGeom geo;
-  uint32_t off = al(static_cast<uint32_t>(a.d) * N * 4u);
+  geo.stage_bytes = al(static_cast<uint32_t>(a.d) * N * 4u);
+  // one group buffer: v ring, k ring, Delta ring, v, k, q (16-byte aligned pieces)
+  auto a16 = [](uint32_t x) { return (x + 15u) & ~15u; };
+  uint32_t off = 0;
   geo.off_vring = off;
-  off = al(off + static_cast<uint32_t>(a.L) * a.d * es);
+  off = a16(off + static_cast<uint32_t>(a.L) * a.d * es);
   geo.off_kring = off;
-  off = al(off + static_cast<uint32_t>(a.L) * N * es);
+  off = a16(off + static_cast<uint32_t>(a.L) * N * es);
   geo.off_dtring = off;
-  off = al(off + static_cast<uint32_t>(a.L) * 4u);
+  off = a16(off + static_cast<uint32_t>(a.L) * 4u);
   geo.off_vin = off;
-  off = al(off + static_cast<uint32_t>(a.d) * es);
+  off = a16(off + static_cast<uint32_t>(a.d) * es);
   geo.off_kin = off;
-  off = al(off + N * es);
+  off = a16(off + N * es);
   geo.off_qin = off;
-  off = al(off + N * es);
-  geo.off_hdr = off;
-  geo.stage_bytes = al(off + sizeof(StageHdr));
+  geo.pbuf_bytes = al(off + N * es);
   constexpr bool tc = kFuse && N == 128 && sizeof(TI) == 2;
   const bool use_tc = tc && a.d % 32 == 0 && a.d <= 256 && a.L <= kMaxL;
   geo.ke = a.L <= 16 ? 16u : 32u;
@@ -538,24 +616,26 @@ cudaError_t launch_pipe_n(const M2Launch &a, cudaStream_t stream, bool *launched
   while (geo.ncols < static_cast<uint32_t>(a.d)) geo.ncols <<= 1;
   const uint32_t fold_bytes =
       use_tc ? al(sizeof(FoldUnit)) + 128u * geo.ke * 2u + 3u * static_cast<uint32_t>(a.d) * geo.ke * 2u : 0u;
-  const uint32_t fixed =
-      2u * kMaxStages * 8u + 16u + kGroups * sizeof(GroupScratch) + kItemMax * sizeof(ItemMeta) + fold_bytes + 128u;
+  const uint32_t bars = al(2u * kMaxStages * 8u + 16u + kGroups * sizeof(GroupScratch));
+  const uint32_t pbufs = 2u * kGroups * geo.pbuf_bytes;
+  const uint32_t metas = al(kItemMax * sizeof(ItemMeta));
+  const uint32_t fixed = bars + pbufs + metas + fold_bytes;
+  if (static_cast<uint32_t>(optin) <= fixed) return cudaSuccess;
   const int stages = static_cast<int>((static_cast<uint32_t>(optin) - fixed) / geo.stage_bytes);
   if (stages < kGroups) return cudaSuccess;  // not launched: the caller uses the per-head kernel
   geo.stages = stages < kMaxStages ? stages : kMaxStages;
-  {
-    const uint32_t head = static_cast<uint32_t>(geo.stages) * geo.stage_bytes + 2u * kMaxStages * 8u + 16u +
-                          kGroups * sizeof(GroupScratch) + kItemMax * sizeof(ItemMeta);
-    geo.off_fold = al(head);
-    geo.off_opA = geo.off_fold + al(sizeof(FoldUnit));
-    geo.off_opB = geo.off_opA + 128u * geo.ke * 2u;
-  }
+  const uint32_t head = static_cast<uint32_t>(geo.stages) * geo.stage_bytes;
+  geo.off_pbufs = head + bars;
+  geo.off_meta = geo.off_pbufs + pbufs;
+  geo.off_fold = geo.off_meta + metas;
+  geo.off_opA = geo.off_fold + al(sizeof(FoldUnit));
+  geo.off_opB = geo.off_opA + 128u * geo.ke * 2u;
   const int total = a.B * a.H;
   int grid = total < sms ? total : sms;
   geo.items_per_cta = (total + grid - 1) / grid;
   if (geo.items_per_cta > kItemMax) geo.items_per_cta = kItemMax;
   grid = (total + geo.items_per_cta - 1) / geo.items_per_cta;
-  const size_t smem = static_cast<size_t>(geo.stages) * geo.stage_bytes + fixed;
+  const size_t smem = static_cast<size_t>(head) + fixed;
   auto kern = use_tc ? m2_decode_pipe_kernel<N, kFuse, tc, TI, TO> : m2_decode_pipe_kernel<N, kFuse, false, TI, TO>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
       cudaSuccess)
@@ -592,7 +672,9 @@ cudaError_t launch_pipe_f(const M2Launch &a, cudaStream_t stream, bool *launched
 bool m2_decode_pipe_eligible(const M2Launch &a) {
   const int es = a.in_dtype == RSSM_BF16 ? 2 : 4;
   auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  return a.L % 4 == 0 && (a.d * es) % 16 == 0 && a.d <= kMaxRows && a.d * a.n * 4 <= 96 * 1024 && a16(a.S) &&
+  // one 16-byte chunk per thread covers the Delta ring and this step's v, k, q
+  const bool small_fits = a.L / 4 + a.d * es / 16 + 2 * a.n * es / 16 <= kGroupThreads;
+  return a.L % 4 == 0 && (a.d * es) % 16 == 0 && a.d <= kMaxRows && a.d * a.n * 4 <= 96 * 1024 && small_fits && a16(a.S) &&
          a16(a.ring_v) && a16(a.ring_k) && a16(a.ring_dt) && a16(a.v) && a16(a.k) && a16(a.q);
 }
 

@@ -17,7 +17,13 @@ struct M2Launch {
   const void *v, *k, *q;
   const float *dt, *A;
   void *y;
+  float *work;  // decode workspace (two-launch decode) or null
 };
+
+// Floats per (sequence, head) record of the two-launch decode workspace:
+// abar, info, two spare words, the L decay weights, the d-row buffer term,
+// rounded up to 16 bytes.
+__host__ __device__ constexpr int work_stride_floats(int d, int L) { return (4 + L + d + 3) & ~3; }
 
 enum class M2Kind { Baseline, Decode, DecodeFused, Verify, SnapshotVerify };
 
@@ -27,6 +33,13 @@ cudaError_t launch_m2(M2Kind kind, const M2Launch &a, cudaStream_t stream);
 // every bulk copy is 16-byte sized and aligned; `launched` reports whether the
 // kernel ran (false: the caller falls back to the per-head kernel).
 bool m2_decode_pipe_eligible(const M2Launch &a);
+// Two launches through the caller's workspace (decode_split.cu): a precompute
+// kernel per (sequence, group), then a kernel streaming S_0 per (sequence, head).
+bool m2_decode_split_eligible(const M2Launch &a);
+cudaError_t launch_m2_decode_split(const M2Launch &a, bool fuse_flush, cudaStream_t stream);
+// One CTA per (sequence, head) with every load issued up front (decode_flat.cu).
+bool m2_decode_flat_eligible(const M2Launch &a);
+cudaError_t launch_m2_decode_flat(const M2Launch &a, bool fuse_flush, cudaStream_t stream);
 // fuse_flush: a sequence whose buffer fills is folded into S_0 in the same
 // launch (count and flag end at 0) instead of being flagged for replay_flush.
 cudaError_t launch_m2_decode_pipe(const M2Launch &a, bool fuse_flush, cudaStream_t stream, bool *launched);

@@ -384,6 +384,10 @@ cudaError_t launch_m2_t(M2Kind kind, const M2Launch &a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_m2(M2Kind kind, const M2Launch &a, cudaStream_t stream) {
+  if ((kind == M2Kind::Decode || kind == M2Kind::DecodeFused) && m2_decode_split_eligible(a))
+    return launch_m2_decode_split(a, kind == M2Kind::DecodeFused, stream);
+  if ((kind == M2Kind::Decode || kind == M2Kind::DecodeFused) && m2_decode_flat_eligible(a))
+    return launch_m2_decode_flat(a, kind == M2Kind::DecodeFused, stream);
   if ((kind == M2Kind::Decode || kind == M2Kind::DecodeFused) && m2_decode_pipe_eligible(a)) {
     bool launched = false;
     const cudaError_t e = launch_m2_decode_pipe(a, kind == M2Kind::DecodeFused, stream, &launched);

@@ -33,7 +33,7 @@ class M2Dims(ctypes.Structure):
 
 class M2Replay(ctypes.Structure):
     _fields_ = [(f, ctypes.c_void_p) for f in
-                ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err")]
+                ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err", "work")]
 
 
 class GdnDims(ctypes.Structure):
@@ -51,6 +51,7 @@ EXPORTS = (
     "replay_spec_commit", "ssm_spec_verify_baseline", "ssm_spec_commit_baseline",
     "gdn_state_update_baseline", "gdn_replay_decode", "gdn_replay_flush", "gdn_replay_verify",
     "gdn_spec_verify_baseline", "rssm_version", "rssm_status_string", "rssm_last_cuda_error",
+    "replay_decode_workspace_bytes",
 )
 
 
@@ -85,6 +86,8 @@ def _load() -> ctypes.CDLL:
     lib.rssm_status_string.argtypes = [ctypes.c_int32]
     lib.rssm_last_cuda_error.restype = ctypes.c_char_p
     lib.rssm_last_cuda_error.argtypes = []
+    lib.replay_decode_workspace_bytes.restype = ctypes.c_int64
+    lib.replay_decode_workspace_bytes.argtypes = [ctypes.POINTER(M2Dims)]
     return lib
 
 
@@ -147,13 +150,24 @@ class Mamba2State:
     flag: torch.Tensor  # [B] i32
     sync: torch.Tensor  # [B] i32, zero
     err: torch.Tensor  # [1] i32
+    work: torch.Tensor | None = None  # decode workspace (f32, decode_workspace_bytes) or None
 
     @classmethod
-    def empty(cls, B, H, G, d, n, L, dtype=torch.bfloat16, device="cuda"):
+    def empty(cls, B, H, G, d, n, L, dtype=torch.bfloat16, device="cuda", workspace=True):
         z = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt, device=device)  # noqa: E731
-        return cls(z(B, H, d, n), z(B, H, L, d, dt=dtype), z(B, G, L, n, dt=dtype), z(B, H, L),
-                   z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32),
-                   z(1, dt=torch.int32))
+        st = cls(z(B, H, d, n), z(B, H, L, d, dt=dtype), z(B, G, L, n, dt=dtype), z(B, H, L),
+                 z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32),
+                 z(1, dt=torch.int32))
+        if workspace:
+            st.add_workspace()
+        return st
+
+    def add_workspace(self):
+        """Attach a decode workspace, which lets the decode step run as a
+        precompute launch plus a launch that streams S_0."""
+        nbytes = decode_workspace_bytes(self.dims())
+        self.work = torch.empty(nbytes // 4, dtype=torch.float32, device=self.S0.device)
+        return self
 
     @property
     def shape(self):
@@ -169,8 +183,12 @@ class Mamba2State:
         _f32(self.ring_dt, "ring_dt")
         for name in ("start", "count", "flag", "sync", "err"):
             _i32(getattr(self, name), name)
+        if self.work is not None:
+            _f32(self.work, "work")
+            if self.work.numel() * 4 < decode_workspace_bytes(self.dims()):
+                raise ValueError("work is smaller than decode_workspace_bytes()")
         return M2Replay(*(_ptr(getattr(self, f)) for f in
-                          ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err")))
+                          ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err", "work")))
 
 
 @dataclasses.dataclass
@@ -215,6 +233,14 @@ class GdnState:
 # ---------------------------------------------------------------------------
 # Mamba-2 calls
 # ---------------------------------------------------------------------------
+
+
+def decode_workspace_bytes(dims: M2Dims) -> int:
+    """Bytes of the optional Mamba-2 decode workspace for these dims."""
+    n = int(LIB.replay_decode_workspace_bytes(ctypes.byref(dims)))
+    if n <= 0:
+        raise ReplaySSMError("replay_decode_workspace_bytes: invalid dims")
+    return n
 
 
 def _out(y, shape, dtype, device):

@@ -44,17 +44,23 @@ def assert_close(gpu, ref, rtol=RTOL_F32, atol=ATOL_F32, what=""):
                              f"gpu={g[tuple(idx)]!r} ref={r[tuple(idx)]!r}; max scaled err {diag:.3e}")
 
 
-def m2_state(init: wl.Mamba2Init):
+def m2_state(init: wl.Mamba2Init, workspace: bool = True):
+    """Device state from a seeded init; workspace=True attaches the decode
+    workspace (two-launch decode), False leaves it out (single-launch decode)."""
     from ssm_decode_hybrid_gb300 import replayssm as rs
 
     s = init.shape
     t = TORCH_DT[s.in_dtype]
     B = s.B
-    return rs.Mamba2State(
+    st = rs.Mamba2State(
         S0=dev(init.S0), ring_v=dev(init.ring_v, t), ring_k=dev(init.ring_k, t), ring_dt=dev(init.ring_dt),
         start=dev(init.start, torch.int32), count=dev(init.count, torch.int32),
         flag=torch.zeros(B, dtype=torch.int32, device="cuda"), sync=torch.zeros(B, dtype=torch.int32, device="cuda"),
         err=torch.zeros(1, dtype=torch.int32, device="cuda"))
+    if workspace:
+        st.add_workspace()
+        st.work.fill_(float("nan"))  # scratch: nothing may depend on its prior contents
+    return st
 
 
 def m2_step_dev(step: wl.Mamba2Step, in_dtype: str):

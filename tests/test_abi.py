@@ -74,6 +74,9 @@ def test_host_validation_rejects_bad_arguments():
     assert L.replay_decode_step(ctypes.byref(dims()), None, *args) == -1
     bad = R.M2Replay(mis, *([fake] * 8))  # misaligned S0
     assert L.replay_decode_step(ctypes.byref(dims()), ctypes.byref(bad), *args) == -1
+    badwork = R.M2Replay(*([fake] * 9), mis)  # misaligned decode workspace
+    assert L.replay_decode_step(ctypes.byref(dims()), ctypes.byref(badwork), *args) == -1
+    assert L.replay_decode_step_fused(ctypes.byref(dims()), ctypes.byref(badwork), *args) == -1
     nosync = R.M2Replay(*([fake] * 7), None, fake)
     assert L.replay_decode_step(ctypes.byref(dims()), ctypes.byref(nosync), *args) == -1
     assert L.replay_flush(ctypes.byref(dims()), ctypes.byref(nosync), fake, None) == -1
@@ -97,3 +100,18 @@ def test_host_validation_rejects_bad_arguments():
     assert L.gdn_replay_decode(ctypes.byref(bad_g), ctypes.byref(grep), *gargs) == -2
     assert L.gdn_replay_verify(ctypes.byref(gd), ctypes.byref(grep), 17, *gargs) == -1
     assert L.gdn_replay_flush(ctypes.byref(gd), None, None) == -1
+
+
+def test_decode_workspace_size_query():
+    """Host-only size query: B * H records of 4 + L + d floats rounded up to 16 bytes."""
+    _lib_path()
+    from ssm_decode_hybrid_gb300 import replayssm as R
+
+    def nbytes(B, H, G, d, n, L):
+        return R.LIB.replay_decode_workspace_bytes(ctypes.byref(R.M2Dims(B, H, G, d, n, L, R.BF16, R.F32)))
+
+    assert nbytes(256, 32, 8, 64, 128, 16) == 256 * 32 * 84 * 4
+    assert nbytes(3, 4, 2, 20, 32, 3) == 3 * 4 * 28 * 4
+    assert nbytes(1, 1, 1, 4, 16, 1) == 12 * 4
+    assert nbytes(2, 3, 2, 64, 128, 16) == 0  # H % G != 0
+    assert R.LIB.replay_decode_workspace_bytes(None) == 0

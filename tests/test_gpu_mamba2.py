@@ -31,11 +31,11 @@ def check_pointers(state, orc, idx, what):
     np.testing.assert_array_equal(host(state.flag)[idx], orc.flag, err_msg=f"{what}: flag")
 
 
-def run_decode(shape, seed, steps, sample=None, y_dtype=torch.float32, check_every=1):
+def run_decode(shape, seed, steps, sample=None, y_dtype=torch.float32, check_every=1, workspace=True):
     R = rs()
     init = wl.mamba2_init(shape, seed)
     idx = np.arange(shape.B) if sample is None else np.asarray(sample)
-    state = m2_state(init)
+    state = m2_state(init, workspace)
     orc = oracle_replay(init, idx)
     A = dev(init.A)
     rtol, atol = tol_for(y_dtype)
@@ -74,9 +74,13 @@ SHAPES = [
 ]
 
 
+WORKSPACE = [pytest.param(True, id="two-launch"), pytest.param(False, id="one-launch")]
+
+
+@pytest.mark.parametrize("workspace", WORKSPACE)
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"B{s.B}H{s.H}G{s.G}d{s.d}n{s.n}L{s.L}{s.in_dtype}")
-def test_decode_parity(shape):
-    run_decode(shape, seed=123, steps=2 * shape.L + 3)
+def test_decode_parity(shape, workspace):
+    run_decode(shape, seed=123, steps=2 * shape.L + 3, workspace=workspace)
 
 
 FUSED_SHAPES = [
@@ -87,13 +91,14 @@ FUSED_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("workspace", WORKSPACE)
 @pytest.mark.parametrize("shape", FUSED_SHAPES, ids=lambda s: f"B{s.B}H{s.H}d{s.d}n{s.n}L{s.L}{s.in_dtype}")
-def test_decode_fused_parity(shape):
+def test_decode_fused_parity(shape, workspace):
     """replay_decode_step_fused == decode step followed by the flush."""
     R = rs()
     seed = 321
     init = wl.mamba2_init(shape, seed)
-    state = m2_state(init)
+    state = m2_state(init, workspace)
     orc = oracle_replay(init, np.arange(shape.B))
     A = dev(init.A)
     for t in range(2 * shape.L + 3):
@@ -305,10 +310,11 @@ def test_checkpoint_resume_bit_identical():
     ys = []
     for t, inp in enumerate(steps):
         if t == 5:
-            snap = {f: getattr(state, f).cpu().clone() for f in state.__dataclass_fields__}
+            # the workspace is scratch: not part of the checkpoint
+            snap = {f: getattr(state, f).cpu().clone() for f in state.__dataclass_fields__ if f != "work"}
         ys.append(R.replay_decode_step(state, *inp, A).clone())
         R.replay_flush(state, A)
-    restored = R.Mamba2State(**{f: v.cuda() for f, v in snap.items()})
+    restored = R.Mamba2State(**{f: v.cuda() for f, v in snap.items()}).add_workspace()
     for t, inp in enumerate(steps[5:], start=5):
         y = R.replay_decode_step(restored, *inp, A)
         R.replay_flush(restored, A)
