@@ -34,6 +34,12 @@ __device__ __forceinline__ float load1(const bf16 *p) {
   return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(p)) << 16);
 }
 
+__device__ __forceinline__ float2 load2(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+__device__ __forceinline__ float2 load2(const bf16 *p) {
+  const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
 __device__ __forceinline__ void store1(float *p, float v) { *p = v; }
 __device__ __forceinline__ void store1(bf16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
@@ -231,5 +237,19 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+}  // namespace rssm
+
+namespace rssm {
+
+// Programmatic dependent launch (sm_90+).  A grid launched with the
+// programmatic stream-serialization attribute may start once every block of
+// the preceding grid has called pdl_launch_dependents (or exited);
+// pdl_wait blocks until that preceding grid has completed and its memory
+// writes are visible.  Without the attribute pdl_wait returns at once.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 }  // namespace rssm

@@ -8,14 +8,18 @@
 // staging buffer.  "Algorithm: Mamba-2 standard decode": output-only decode,
 // and "if the buffer is full, flush".
 //
-// Precompute (grid B x G, one warp per head of the group) works on data that
-// sits in L2 (the ring entries, this step's inputs): it reads the pointers,
-// computes k_j^T q for the group, per head the decay weights w_j and abar
-// and the buffer term buf[r] = sum_j w_j (k_j^T q) v_j[r], appends this step's
-// entry to the ring, advances the pointers, and leaves per head in the
-// caller's workspace: abar, (h, start, flags), w_1..w_L, buf[0..d).
+// Precompute (grid B x G, one warp per head of the group) brings in the
+// group's ring entries and this step's inputs with bulk copies, reads the
+// pointers, computes k_j^T q for the group, per head the decay weights w_j and
+// abar and the buffer term buf[r] = sum_j w_j (k_j^T q) v_j[r], appends this
+// step's entry to the ring, and leaves per head in the caller's workspace:
+// abar, (h, start, flags), w_1..w_L, buf[0..d).  It does not move the
+// pointers: the streaming kernel's block of head 0 does, once every
+// precompute block has read them, so no arrival counter is needed.
 //
-// Stream (grid B x H, 256 threads) is then as lean as the baseline kernel:
+// Stream (grid B x H, 256 threads, launched as a programmatic dependent of the
+// precompute so that its S_0 loads overlap the precompute's tail) is then as
+// lean as the baseline kernel:
 // each thread loads its eight 16-byte slices of the head's S_0 block, forms
 // S_0 q with shuffle reductions and writes y = abar (S_0 q) + buf.  Its CTAs
 // live little longer than their loads, so the S_0 stream runs near the HBM
@@ -36,133 +40,167 @@ __device__ __forceinline__ int wrapL(int s, int L) { return s >= L ? s - L : s; 
 // ---------------------------------------------------------------------------
 // precompute: one CTA per (sequence, group), one warp per head of the group
 // ---------------------------------------------------------------------------
+// Shared memory, each part 16-byte aligned and filled by one bulk copy:
+//   [L][N] group k ring | [N] k | [N] q | [HpG][L][d] v rings | [HpG][d] v |
+//   [HpG][L] Delta rings | [HpG][kMaxL] per-slot coefficients
+struct PrepSmem {
+  uint32_t k_ring, k_in, q_in, v_ring, v_in, dt_ring, coef, total, copied;
+  __host__ __device__ PrepSmem(int L, int N, int d, int HpG, int es) {
+    k_ring = 0;
+    k_in = k_ring + L * N * es;
+    q_in = k_in + N * es;
+    v_ring = q_in + N * es;
+    v_in = v_ring + HpG * L * d * es;
+    dt_ring = v_in + HpG * d * es;
+    coef = dt_ring + HpG * L * 4;
+    copied = coef;
+    total = coef + HpG * kMaxL * 4;
+  }
+};
+
 template <int N, bool kFuse, typename TI>
 __global__ void __launch_bounds__(1024) m2_prep_kernel(M2Launch a, int stride) {
   constexpr int LPR = N / 4;
   constexpr int es = sizeof(TI);
-  extern __shared__ __align__(16) unsigned char psm[];
+  extern __shared__ __align__(128) unsigned char psm[];
+  __shared__ __align__(8) uint64_t bar;
   __shared__ float s_M[kMaxL];
   __shared__ int s_ptr[2];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int nthreads = blockDim.x;
   const int HpG = a.H / a.G;
   const int b = blockIdx.x / a.G, g = blockIdx.x - b * a.G;
   const int i = g * HpG + w;  // this warp's head
   const int d = a.d, L = a.L;
   const size_t bg = static_cast<size_t>(b) * a.G + g;
-  const size_t bh = static_cast<size_t>(b) * a.H + i;
-  const int vc = d * es / 16, kc = N * es / 16;
-
-  // shared: [L][N] group k ring | k | q | per head: [L][d] v ring, v, [L] Delta ring, [32] weights
-  unsigned char *sk = psm;
-  unsigned char *skin = sk + static_cast<size_t>(L) * N * es;
-  unsigned char *sqin = skin + static_cast<size_t>(N) * es;
-  unsigned char *shead = sqin + static_cast<size_t>(N) * es;
-  const size_t head_bytes = static_cast<size_t>(L) * d * es + static_cast<size_t>(d) * es + L * 4 + kMaxL * 4;
-  unsigned char *sv = shead + w * head_bytes;
-  unsigned char *svin = sv + static_cast<size_t>(L) * d * es;
-  float *sdt = reinterpret_cast<float *>(svin + static_cast<size_t>(d) * es);
-  float *swt = sdt + L;
+  const size_t h0 = static_cast<size_t>(b) * a.H + g * HpG;  // first head of the group
+  const size_t bh = h0 + w;
+  const PrepSmem lay(L, N, d, HpG, es);
 
   if (tid == 0) {
-    s_ptr[0] = a.count[b];
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, lay.copied);
+    const unsigned char *ck = static_cast<const unsigned char *>(a.ring_k);
+    const unsigned char *cv = static_cast<const unsigned char *>(a.ring_v);
+    bulk_g2s(psm + lay.k_ring, ck + bg * L * N * es, lay.k_in - lay.k_ring, &bar);
+    bulk_g2s(psm + lay.k_in, static_cast<const unsigned char *>(a.k) + bg * N * es, N * es, &bar);
+    bulk_g2s(psm + lay.q_in, static_cast<const unsigned char *>(a.q) + bg * N * es, N * es, &bar);
+    bulk_g2s(psm + lay.v_ring, cv + h0 * L * d * es, lay.v_in - lay.v_ring, &bar);
+    bulk_g2s(psm + lay.v_in, static_cast<const unsigned char *>(a.v) + h0 * d * es, lay.dt_ring - lay.v_in, &bar);
+    bulk_g2s(psm + lay.dt_ring, a.ring_dt + h0 * L, lay.coef - lay.dt_ring, &bar);
+    s_ptr[0] = a.count[b];  // after the copies are issued: the two latencies overlap
     s_ptr[1] = a.start[b];
   }
-  // all ring slots and this step's inputs, 16 bytes per copy
-  {
-    const unsigned char *gk = static_cast<const unsigned char *>(a.ring_k) + bg * L * N * es;
-    const int ng = L * kc + 2 * kc;
-    for (int idx = tid; idx < ng; idx += nthreads) {
-      if (idx < L * kc)
-        cp_async16(sk + idx * 16, gk + idx * 16);
-      else if (idx < L * kc + kc)
-        cp_async16(skin + (idx - L * kc) * 16, static_cast<const unsigned char *>(a.k) + bg * N * es + (idx - L * kc) * 16);
-      else
-        cp_async16(sqin + (idx - L * kc - kc) * 16,
-                   static_cast<const unsigned char *>(a.q) + bg * N * es + (idx - L * kc - kc) * 16);
-    }
-    const unsigned char *gv = static_cast<const unsigned char *>(a.ring_v) + bh * L * d * es;
-    const int nh = L * vc + vc + L / 4;
-    for (int idx = lane; idx < nh; idx += 32) {
-      if (idx < L * vc)
-        cp_async16(sv + idx * 16, gv + idx * 16);
-      else if (idx < L * vc + vc)
-        cp_async16(svin + (idx - L * vc) * 16, static_cast<const unsigned char *>(a.v) + bh * d * es + (idx - L * vc) * 16);
-      else
-        cp_async16(reinterpret_cast<unsigned char *>(sdt) + (idx - L * vc - vc) * 16,
-                   reinterpret_cast<const unsigned char *>(a.ring_dt + bh * L) + (idx - L * vc - vc) * 16);
-    }
-    cp_async_commit();
-  }
+  // the streaming kernel may start its S_0 loads now; it waits for this grid
+  // before it reads the workspace
+  pdl_launch_dependents();
   const float dt_in = a.dt[bh];
   const float Ai = a.A[i];
-  cp_async_wait_all();
-  __syncthreads();
+  __syncthreads();  // barrier initialised, pointers read
+  const bool arrived = mbar_wait(&bar, 0);
+  if (__syncthreads_or(!arrived)) {
+    if (tid == 0) {
+      set_err(a.err, RSSM_EBIT_TIMEOUT);
+      mbar_wait(&bar, 0);  // bounded: the copies must land before shared memory is released
+    }
+    return;
+  }
 
   const int h = s_ptr[0], st = s_ptr[1];
   float *wk = a.work + bh * stride;
-  const bool valid = h >= 0 && h < L && st >= 0 && st < L;
-  if (!valid) {
+  if (h < 0 || h >= L || st < 0 || st >= L) {
     if (lane == 0) reinterpret_cast<int *>(wk)[1] = 0;
     if (tid == 0) set_err(a.err, RSSM_EBIT_COUNT_RANGE);
     return;
   }
   const int p = h + 1;
-  if (tid == 0 && last_arrival(a.sync, b, a.G)) {
-    a.count[b] = (kFuse && p == L) ? 0 : p;  // fused: a filled buffer is folded by this step
-    a.flag[b] = (!kFuse && p == L) ? 1 : 0;
-  }
-  const TI *kring = reinterpret_cast<const TI *>(sk);
-  const TI *kin = reinterpret_cast<const TI *>(skin);
-  const TI *qin = reinterpret_cast<const TI *>(sqin);
-  const TI *vring = reinterpret_cast<const TI *>(sv);
-  const TI *vin = reinterpret_cast<const TI *>(svin);
+  // start/count/flag are rewritten by the streaming kernel, after every block
+  // of this grid has read them
+  const TI *kring = reinterpret_cast<const TI *>(psm + lay.k_ring);
+  const TI *kin = reinterpret_cast<const TI *>(psm + lay.k_in);
+  const TI *qin = reinterpret_cast<const TI *>(psm + lay.q_in);
+  TI *vring = reinterpret_cast<TI *>(psm + lay.v_ring) + static_cast<size_t>(w) * L * d;
+  const TI *vin = reinterpret_cast<const TI *>(psm + lay.v_in) + static_cast<size_t>(w) * d;
+  const float *sdt = reinterpret_cast<const float *>(psm + lay.dt_ring) + w * L;
+  float *scoef = reinterpret_cast<float *>(psm + lay.coef) + w * kMaxL;
+  const int slot_new = wrapL(st + h, L);
 
-  // k_j^T q for the group: entries spread over the warps, one lane group per entry
+  // k_j^T q for the group, in window order: each lane group of LPR lanes
+  // forms V entries at a time and reduces them together
   {
+    constexpr int V = LPR >= 4 ? 4 : LPR;
+    constexpr int RPW = 32 / LPR;
     const int col = (lane % LPR) * 4;
     const float4 q4 = load4(qin + col);
-    constexpr int RPW = 32 / LPR;
-    const int nw = nthreads / 32;
-    for (int jb = w * RPW; jb < p; jb += nw * RPW) {
-      const int j = jb + lane / LPR;
-      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (j < p) kv = load4((j < h ? kring + static_cast<size_t>(wrapL(st + j, L)) * N : kin) + col);
-      const float m = group_sum<LPR>(dot4(kv, q4));
-      if (j < p && (lane % LPR) == 0) s_M[j] = m;
+    const int nw = blockDim.x / 32;
+    const int grp = lane / LPR;
+    for (int base = w * RPW * V; base < p; base += nw * RPW * V) {
+      float x[V];
+#pragma unroll
+      for (int m = 0; m < V; ++m) {
+        const int j = base + grp * V + m;
+        x[m] = 0.f;
+        if (j < p) x[m] = dot4(load4((j < h ? kring + static_cast<size_t>(wrapL(st + j, L)) * N : kin) + col), q4);
+      }
+      group_sum_multi<LPR, V>(x, lane);
+      const int j = base + grp * V + (lane % LPR) / (LPR / V);
+      if ((lane % (LPR / V)) == 0 && j < p) s_M[j] = x[0];
     }
   }
-  // decay weights of this warp's head: w_j = Delta_j exp(A sum_{j<m<p} Delta_m), abar = exp(A sum Delta)
-  float abar;
+  // decay weights of this warp's head, one entry per lane:
+  // w_j = Delta_j exp(A sum_{j<m<p} Delta_m), abar = exp(A sum_{m<p} Delta_m)
+  float abar, wj;
   {
-    const int slot = wrapL(st + lane, L);
-    const float dtj = (lane < h) ? sdt[slot] : (lane == h ? dt_in : 0.f);
+    const float dtj = (lane < h) ? sdt[wrapL(st + lane, L)] : (lane == h ? dt_in : 0.f);
     float tot;
     const float ex = excl_suffix_sum(Ai * dtj, lane, tot);
-    swt[lane] = (lane < p) ? dtj * expf(ex) : 0.f;
+    wj = (lane < p) ? dtj * expf(ex) : 0.f;
     abar = expf(tot);
   }
-  __syncthreads();
-
-  // buffer term of this head; the workspace record
-  for (int r = lane; r < d; r += 32) {
-    float acc = s_M[h] * swt[h] * load1(vin + r);
-    for (int j = 0; j < h; ++j) acc = fmaf(s_M[j] * swt[j], load1(vring + static_cast<size_t>(wrapL(st + j, L)) * d + r), acc);
-    wk[4 + L + r] = acc;
-  }
-  if (lane < L) wk[4 + lane] = swt[lane];
+  // this step's v joins its head's ring copy, so that the window is slots
+  // st .. st+h (mod L) of one array
+  for (int c = lane; c < d * es / 4; c += 32)
+    reinterpret_cast<uint32_t *>(vring + static_cast<size_t>(slot_new) * d)[c] =
+        reinterpret_cast<const uint32_t *>(vin)[c];
+  __syncthreads();  // s_M complete
+  if (lane < p) scoef[wrapL(st + lane, L)] = s_M[lane] * wj;
+  if (lane < L) wk[4 + lane] = wj;
   if (lane == 0) {
     wk[0] = abar;
     reinterpret_cast<int *>(wk)[1] = h | (st << 8) | kInfoValid | ((kFuse && p == L) ? kInfoFold : 0);
   }
+  __syncwarp();
+
+  // buffer term buf[r] = sum over the window's slots of coef(slot) v_slot[r], two rows per lane
+  const int seg1 = min(st + p, L), seg2 = st + p - L;
+  for (int r = 2 * lane; r < d; r += 64) {
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int sl = st; sl < seg1; ++sl) {
+      const float c = scoef[sl];
+      const float2 v2 = load2(vring + static_cast<size_t>(sl) * d + r);
+      acc.x = fmaf(c, v2.x, acc.x);
+      acc.y = fmaf(c, v2.y, acc.y);
+    }
+#pragma unroll 4
+    for (int sl = 0; sl < seg2; ++sl) {
+      const float c = scoef[sl];
+      const float2 v2 = load2(vring + static_cast<size_t>(sl) * d + r);
+      acc.x = fmaf(c, v2.x, acc.x);
+      acc.y = fmaf(c, v2.y, acc.y);
+    }
+    *reinterpret_cast<float2 *>(wk + 4 + L + r) = acc;
+  }
+
   // append this step's entry at slot (start + h) mod L
-  const int slot_new = wrapL(st + h, L);
-  TI *rv_out = static_cast<TI *>(a.ring_v) + (bh * L + slot_new) * d;
-  for (int r = lane; r < d; r += 32) rv_out[r] = vin[r];
-  if (lane == 0) a.ring_dt[bh * L + slot_new] = dt_in;
-  if (w == 0) {
-    TI *rk_out = static_cast<TI *>(a.ring_k) + (bg * L + slot_new) * N;
-    for (int c = lane; c < N; c += 32) rk_out[c] = kin[c];
+  {
+    uint32_t *rv_out = reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_v) + (bh * L + slot_new) * d);
+    for (int c = lane; c < d * es / 4; c += 32) rv_out[c] = reinterpret_cast<const uint32_t *>(vin)[c];
+    if (lane == 0) a.ring_dt[bh * L + slot_new] = dt_in;
+    if (w == 0) {
+      uint32_t *rk_out = reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_k) + (bg * L + slot_new) * N);
+      for (int c = lane; c < N * es / 4; c += 32) rk_out[c] = reinterpret_cast<const uint32_t *>(kin)[c];
+    }
   }
 }
 
@@ -194,9 +232,16 @@ __global__ void __launch_bounds__(kThreads, 4) m2_stream_kernel(M2Launch a, int 
   const int g = i / (a.H / a.G);
   const size_t bg = static_cast<size_t>(b) * a.G + g;
   const float4 q4 = load4(static_cast<const TI *>(a.q) + bg * N + col);
+  pdl_wait();  // the precompute grid has finished: workspace, ring and pointers are final
   const int info = reinterpret_cast<const int *>(wk)[1];
   const float abar = wk[0];
   if (!(info & kInfoValid)) return;
+  if (i == 0 && tid == 0) {
+    // every precompute block has read this sequence's pointers: advance them
+    const int p = (info & 0xff) + 1;
+    a.count[b] = (kFuse && p == L) ? 0 : p;  // fused: a filled buffer is folded below
+    a.flag[b] = (!kFuse && p == L) ? 1 : 0;
+  }
 
   float x[kSPass];
 #pragma unroll
@@ -271,8 +316,7 @@ cudaError_t launch_split_n(const M2Launch &a, cudaStream_t stream) {
   constexpr int es = sizeof(TI);
   const int HpG = a.H / a.G;
   const int stride = work_stride_floats(a.d, a.L);
-  const size_t head_bytes = static_cast<size_t>(a.L) * a.d * es + static_cast<size_t>(a.d) * es + a.L * 4 + kMaxL * 4;
-  const size_t psm = static_cast<size_t>(a.L) * N * es + 2u * N * es + HpG * head_bytes;
+  const size_t psm = PrepSmem(a.L, N, a.d, HpG, es).total;
   auto prep = m2_prep_kernel<N, kFuse, TI>;
   cudaError_t e;
   if (psm > 48 * 1024 &&
@@ -287,8 +331,18 @@ cudaError_t launch_split_n(const M2Launch &a, cudaStream_t stream) {
       (e = cudaFuncSetAttribute(strm, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm))) !=
           cudaSuccess)
     return e;
-  strm<<<static_cast<unsigned>(a.B) * a.H, kThreads, ssm, stream>>>(a, stride);
-  return cudaGetLastError();
+  // programmatic dependent launch: the S_0 stream overlaps the precompute's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.H);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = ssm;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, strm, a, stride);
 }
 
 template <bool kFuse, typename TI, typename TO>
@@ -317,8 +371,8 @@ bool m2_decode_split_eligible(const M2Launch &a) {
   const int rpp = kWarps * (128 / a.n);
   const int HpG = a.H / a.G;
   auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  const size_t psm = static_cast<size_t>(a.L) * a.n * es + 2u * a.n * es +
-                     static_cast<size_t>(HpG) * (static_cast<size_t>(a.L + 1) * a.d * es + a.L * 4 + kMaxL * 4);
+  if (HpG > 32) return false;
+  const size_t psm = PrepSmem(a.L, a.n, a.d, HpG, es).total;
   return a.work != nullptr && a16(a.work) && HpG <= 32 && psm <= 160 * 1024 && a.L % 4 == 0 && a.L <= 255 &&
          (a.d * es) % 16 == 0 &&
          a.d <= kSPass * rpp && a16(a.S) && a16(a.ring_v) && a16(a.ring_k) && a16(a.ring_dt) && a16(a.v) &&
