@@ -180,6 +180,21 @@ RSSM_API rssm_status replay_decode_step_fused(const rssm_m2_dims *dims, const rs
                                               const void *k, const void *q, const float *dt, const float *A,
                                               void *y, rssm_stream_t stream);
 
+/* replay_decode_step_fused with a workspace owned by the library, so that
+ * the call allocates nothing and needs no caller buffer beyond the state.
+ * The pages have no counterpart: this is an interface variant of
+ * replay_decode_step_fused, with the same outputs and state updates.
+ * st->work is ignored; the two-launch kernels use a file-scope device array
+ * of 8 MiB (2,097,152 floats) inside the library, whose address is looked up
+ * once per device.  Requires B * H * 4 * ceil((d + L + 4) / 4) <= 2,097,152
+ * (RSSM_ERR_UNSUPPORTED otherwise).  All calls on one device share that
+ * array, so they must be ordered (one stream, or synchronised streams).
+ * Arguments as replay_decode_step.                                            */
+RSSM_API rssm_status replay_decode_step_fused_noalloc(const rssm_m2_dims *dims, const rssm_m2_replay *st,
+                                                      const void *v, const void *k, const void *q,
+                                                      const float *dt, const float *A, void *y,
+                                                      rssm_stream_t stream);
+
 /* Speculative verify of T drafts ("Algorithm -- speculative decoding"): with
  * h = count[b] (requires h + T <= L, else RSSM_EBIT_WINDOW and the sequence is
  * skipped), write the T drafts tentatively at slots (start + h + s - 1) mod L

@@ -3,6 +3,7 @@
 // synchronises.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "kernels.cuh"
 
@@ -441,3 +442,75 @@ rssm_status gdn_spec_verify_baseline(const rssm_gdn_dims *dims, int32_t T, float
 }
 
 }  // extern "C"
+
+// ---------------- fused decode step with a library-owned workspace ----------
+
+namespace {
+
+// Workspace of replay_decode_step_fused_noalloc: module data, so the call
+// needs no allocation by anyone.  Every call on a device uses the same array.
+constexpr size_t kStaticWorkFloats = size_t(1) << 21;  // 8 MiB
+__device__ __align__(256) float g_static_work[kStaticWorkFloats];
+
+constexpr int kMaxCachedDevices = 64;
+std::mutex g_static_work_mu;
+float *g_static_work_ptr[kMaxCachedDevices] = {};
+
+// Device address of g_static_work on the current device, looked up once per device.
+cudaError_t static_work_ptr(float **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxCachedDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_work_mu);
+  if (g_static_work_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_work);
+    if (e != cudaSuccess) return e;
+    g_static_work_ptr[dev] = static_cast<float *>(p);
+  }
+  *out = g_static_work_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" rssm_status replay_decode_step_fused_noalloc(const rssm_m2_dims *dims, const rssm_m2_replay *s,
+                                                        const void *v, const void *k, const void *q,
+                                                        const float *dt, const float *A, void *y,
+                                                        rssm_stream_t stream) {
+  rssm_status st = check_m2_dims(dims);
+  if (st) return st;
+  const rssm_m2_dims &d = *dims;
+  if (!m2_replay_ok(d, s, true) || !ok_elem(v, d.in_dtype) || !ok16(k) || !ok16(q) || !ok4(dt) || !ok4(A) ||
+      !ok_elem(y, d.y_dtype))
+    return RSSM_ERR_INVALID_ARG;
+  if (static_cast<size_t>(d.B) * d.H * work_stride_floats(d.d, d.L) > kStaticWorkFloats) return RSSM_ERR_UNSUPPORTED;
+  float *work = nullptr;
+  cudaError_t e = static_work_ptr(&work);
+  if (e != cudaSuccess) return cuda_status(e);
+  M2Launch a = m2_launch(d);
+  a.S = s->S0;
+  a.ring_v = s->ring_v;
+  a.ring_k = s->ring_k;
+  a.ring_dt = s->ring_dt;
+  a.start = s->start;
+  a.count = s->count;
+  a.flag = s->flag;
+  a.sync = s->sync;
+  a.err = s->err;
+  a.v = v;
+  a.k = k;
+  a.q = q;
+  a.dt = dt;
+  a.A = A;
+  a.y = y;
+  a.work = work;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  e = launch_m2(M2Kind::DecodeFused, a, cs);
+  if (e != cudaErrorNotSupported) return cuda_status(e);
+  // shapes outside the fused kernels: the decode step, then the flush
+  e = launch_m2(M2Kind::Decode, a, cs);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_flush(m2_flush_launch(d, s, A), cs));
+}

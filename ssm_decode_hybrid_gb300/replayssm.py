@@ -51,7 +51,7 @@ EXPORTS = (
     "replay_spec_commit", "ssm_spec_verify_baseline", "ssm_spec_commit_baseline",
     "gdn_state_update_baseline", "gdn_replay_decode", "gdn_replay_flush", "gdn_replay_verify",
     "gdn_spec_verify_baseline", "rssm_version", "rssm_status_string", "rssm_last_cuda_error",
-    "replay_decode_workspace_bytes",
+    "replay_decode_workspace_bytes", "replay_decode_step_fused_noalloc",
 )
 
 
@@ -65,6 +65,7 @@ def _load() -> ctypes.CDLL:
         "ssm_state_update_baseline": [ctypes.POINTER(M2Dims), P, P, P, P, P, P, P, P],
         "replay_decode_step": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), P, P, P, P, P, P, P],
         "replay_decode_step_fused": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), P, P, P, P, P, P, P],
+        "replay_decode_step_fused_noalloc": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), P, P, P, P, P, P, P],
         "replay_flush": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), P, P],
         "replay_spec_verify": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), I, P, P, P, P, P, P, P],
         "replay_spec_commit": [I, I, I, P, P, P, P],
@@ -279,6 +280,19 @@ def replay_decode_step_fused(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype
     st = state.struct()
     _check(LIB.replay_decode_step_fused(ctypes.byref(dims), ctypes.byref(st), _ptr(v), _ptr(k), _ptr(q), _ptr(dt),
                                         _ptr(A), _ptr(y), _stream()), "replay_decode_step_fused")
+    return y
+
+
+def replay_decode_step_fused_noalloc(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+    """replay_decode_step_fused with the library's own workspace (state.work is
+    not used); allocates nothing when y is given."""
+    B, H, G, d, n, L = state.shape
+    y = _out(y, (B, H, d), y_dtype, state.S0.device)
+    dims = state.dims(y.dtype)
+    st = state.struct()
+    _check(LIB.replay_decode_step_fused_noalloc(ctypes.byref(dims), ctypes.byref(st), _ptr(v), _ptr(k), _ptr(q),
+                                                _ptr(dt), _ptr(A), _ptr(y), _stream()),
+           "replay_decode_step_fused_noalloc")
     return y
 
 
