@@ -500,6 +500,414 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# measurement suite (--suite): the other workloads, one JSON line each
+# ---------------------------------------------------------------------------
+
+
+def m2_verify_bytes(s: wl.Mamba2Shape, h: int, T: int) -> int:
+    """One verify round of one sequence with h committed entries: S_0, the h
+    entries, T drafts' v/k/q/dt, the T tentative entries written, T outputs."""
+    e = 2 if s.in_dtype == wl.BF16 else 4
+    inputs = s.H * s.d * e + 2 * s.G * s.n * e + s.H * 4
+    return 4 * s.H * s.d * s.n + h * m2_entry_bytes(s) + T * (inputs + m2_entry_bytes(s) + 4 * s.H * s.d)
+
+
+def m2_snapshot_verify_bytes(s: wl.Mamba2Shape, T: int) -> int:
+    """Snapshot baseline round: read one state slot, write T slots, T drafts' inputs and outputs."""
+    e = 2 if s.in_dtype == wl.BF16 else 4
+    inputs = s.H * s.d * e + 2 * s.G * s.n * e + s.H * 4
+    return (T + 1) * 4 * s.H * s.d * s.n + T * (inputs + 4 * s.H * s.d)
+
+
+def gdn_entry_bytes(s: wl.GdnShape) -> int:
+    eu = 4 if s.u_dtype == wl.F32 else 2
+    ek = 2 if s.in_dtype == wl.BF16 else 4
+    return s.Hv * s.dv * eu + s.Hk * s.dk * ek + s.Hv * 4
+
+
+def gdn_input_bytes(s: wl.GdnShape) -> int:
+    e = 2 if s.in_dtype == wl.BF16 else 4
+    return 2 * s.Hk * s.dk * e + s.Hv * s.dv * e + 2 * s.Hv * 4
+
+
+def gdn_decode_bytes(s: wl.GdnShape, h: int) -> int:
+    return 4 * s.Hv * s.dv * s.dk + h * gdn_entry_bytes(s) + gdn_input_bytes(s) + gdn_entry_bytes(s) + 4 * s.Hv * s.dv
+
+
+def gdn_flush_bytes(s: wl.GdnShape, c: int) -> int:
+    return 8 * s.Hv * s.dv * s.dk + c * gdn_entry_bytes(s)
+
+
+def gdn_baseline_bytes(s: wl.GdnShape) -> int:
+    return 8 * s.Hv * s.dv * s.dk + gdn_input_bytes(s) + 4 * s.Hv * s.dv
+
+
+def gdn_verify_bytes(s: wl.GdnShape, h: int, T: int) -> int:
+    return 4 * s.Hv * s.dv * s.dk + h * gdn_entry_bytes(s) + T * (gdn_input_bytes(s) + gdn_entry_bytes(s) +
+                                                                   4 * s.Hv * s.dv)
+
+
+def gdn_snapshot_verify_bytes(s: wl.GdnShape, T: int) -> int:
+    return (T + 1) * 4 * s.Hv * s.dv * s.dk + T * (gdn_input_bytes(s) + 4 * s.Hv * s.dv)
+
+
+def _time_graph(fn, K: int, W: int, reps: int = 8) -> float:
+    """Milliseconds per call of fn(i), with K calls (i = 0..K-1) captured in one
+    CUDA graph and the graph replayed `reps` times after W warm-up replays."""
+    import torch
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn(0)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(K):
+                fn(i)
+    torch.cuda.synchronize()
+    for _ in range(W):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) / (reps * K)
+
+
+def _time_loop(fn, K: int, W: int) -> float:
+    """Milliseconds per call of fn(i) over K calls after W warm-up calls (CUDA events)."""
+    import torch
+
+    for i in range(W):
+        fn(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        fn(W + i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / K
+
+
+def _dev(x, dt=None):
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    return (t.to(dt) if dt is not None else t).cuda()
+
+
+def suite_layers(R, peak):
+    """Layer-stack sweep: 23 independent Nemotron-H Mamba-2 layers per step,
+    batch B and ring capacity L swept; fused decode step per layer.  The
+    23-layer step is captured in a CUDA graph (as a serving loop would), so
+    small batches measure the GPU rather than host launch overhead; byte
+    accounting follows each sequence's fill level through the replays."""
+    import torch
+
+    LAYERS, out = 23, []
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    for bi, B in enumerate((1, 8, 64, 256, 512)):
+        base_ms = None
+        for li, L in enumerate((4, 8, 16, 32)):
+            shape = wl.Mamba2Shape(B=B, H=32, G=8, d=64, n=128, L=L, in_dtype=wl.BF16)
+            seed = wl.SEED_SWEEP + 100 * (bi * 4 + li)
+            layers, counts0 = [], []
+            for layer in range(LAYERS):
+                t = wl.mamba2_state_tensors_device(shape, seed + layer, "cuda")
+                z = lambda n: torch.zeros(n, dtype=torch.int32, device="cuda")  # noqa: E731
+                st = R.Mamba2State(t["S0"], t["ring_v"], t["ring_k"], t["ring_dt"], t["start"], t["count"], z(B),
+                                   z(B), z(1)).add_workspace()
+                layers.append((st, t["A"]))
+                counts0.append(t["count"].cpu().numpy())
+            g = torch.Generator(device="cuda")
+            g.manual_seed(seed + 999)
+            pool = [(torch.randn(B, 32, 64, generator=g, device="cuda").to(torch.bfloat16),
+                     torch.randn(B, 8, 128, generator=g, device="cuda").to(torch.bfloat16),
+                     torch.randn(B, 8, 128, generator=g, device="cuda").to(torch.bfloat16),
+                     torch.nn.functional.softplus(torch.randn(B, 32, generator=g, device="cuda")))
+                    for _ in range(4)]
+            y = torch.empty(B, 32, 64, device="cuda")
+
+            def step(i):
+                for st, A in layers:
+                    R.replay_decode_step_fused(st, *pool[i % 4], A, y=y)
+
+            K, W, reps = 16, 3, 8
+            ms = _time_graph(step, K, W, reps)
+            per_h = np.array([m2_decode_bytes(shape, h) for h in range(L)], dtype=np.int64)
+            nbytes = 0
+            for c0 in counts0:  # capture ran one eager step first, then W + reps replays of K steps
+                tr = fill_trace(c0, L, 1 + K * (W + reps))[1 + K * W:]
+                nbytes += int(per_h[tr].sum()) + int((tr + 1 == L).sum()) * m2_fused_flush_extra_bytes(shape)
+            nbytes = nbytes / reps
+            # the same step without a workspace: one launch per layer
+            works = [st.work for st, _ in layers]
+            for st, _ in layers:
+                st.work = None
+            one_ms = _time_graph(step, K, W, reps)
+            for (st, _), wkt in zip(layers, works):
+                st.work = wkt
+            err = max(int(st.err.item()) for st, _ in layers)
+            if base_ms is None:  # the baseline does not depend on L
+                Ss = [st.S0.clone() for st, _ in layers]
+
+                def bstep(i):
+                    for S, (_, A) in zip(Ss, layers):
+                        R.ssm_state_update_baseline(S, *pool[i % 4], A, y=y)
+
+                base_ms = _time_graph(bstep, K, W, reps)
+                del Ss
+            gbs = nbytes / K / (ms * 1e-3) / 1e9
+            out.append({"suite": "layers", "workload": f"{LAYERS} Mamba-2 layers (H=32, G=8, d=64, n=128), B={B}, L={L}",
+                        "B": B, "L": L, "layers": LAYERS, "steps": K * reps, "timing": "CUDA graph of 16 steps",
+                        "ms_per_step": ms,
+                        "tokens_per_s": B / (ms * 1e-3), "gbs": gbs, "frac_of_peak": gbs / peak,
+                        "one_launch_ms_per_step": one_ms,
+                        "baseline_ms_per_step": base_ms, "replay_over_baseline": base_ms / ms,
+                        "state_bytes": LAYERS * B * 32 * 64 * 128 * 4,
+                        "state_fits_l2": LAYERS * B * 32 * 64 * 128 * 4 <= l2, "device_error_word": err})
+            print(json.dumps(out[-1]), flush=True)
+            del layers, pool
+            torch.cuda.empty_cache()
+    return out
+
+
+def _spec_pool(shape, seed, T, n):
+    steps = [wl.mamba2_step(shape, seed, r, T=T) for r in range(n)]
+    inp = [(_dev(s.v, _bf16()), _dev(s.k, _bf16()), _dev(s.q, _bf16()), _dev(s.dt)) for s in steps]
+    acc = [_dev(wl.accepted_counts(shape.B, T, seed, r), _i32()) for r in range(n)]
+    return inp, acc
+
+
+def _bf16():
+    import torch
+
+    return torch.bfloat16
+
+
+def _i32():
+    import torch
+
+    return torch.int32
+
+
+def _m2_state(R, init):
+    import torch
+
+    B = init.shape.B
+    z = lambda n: torch.zeros(n, dtype=torch.int32, device="cuda")  # noqa: E731
+    return R.Mamba2State(_dev(init.S0), _dev(init.ring_v, _bf16()), _dev(init.ring_k, _bf16()), _dev(init.ring_dt),
+                         _dev(init.start, _i32()), _dev(init.count, _i32()), z(B), z(B), z(1))
+
+
+def suite_spec(R, peak):
+    """Speculative verify rounds, B=512, T=4, L=16, accepted ~ U{0..4}: replay
+    (verify + device commit + flush of early-flagged sequences) vs the
+    snapshot baseline (T+1 state slots)."""
+    import torch
+
+    shape, T, seed, P = wl.SPEC_MAMBA2, 4, wl.SEED_SPEC, 8
+    init = wl.mamba2_init(shape, seed, fill_max=shape.L - T)
+    inp, acc = _spec_pool(shape, seed, T, P)
+    A = _dev(init.A)
+    y = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
+    W, K = 4, 256
+
+    def make_round(st):
+        def rnd(i):
+            R.replay_spec_verify(st, *inp[i % P], A, y=y)
+            R.replay_spec_commit(acc[i % P], st.count, T, shape.L, st.err)
+            R.replay_flush(st, A)
+        return rnd
+
+    # the committed-count trace of these rounds, recorded on an untimed copy
+    st = _m2_state(R, init)
+    h_tr, fl_tr, acc_tr = [], [], []
+    for i in range(W + K):
+        h_tr.append(st.count.cpu().numpy().astype(np.int64))
+        R.replay_spec_verify(st, *inp[i % P], A, y=y)
+        fl_tr.append(st.flag.cpu().numpy() != 0)
+        R.replay_spec_commit(acc[i % P], st.count, T, shape.L, st.err)
+        acc_tr.append(acc[i % P].cpu().numpy().astype(np.int64))
+        R.replay_flush(st, A)
+    del st
+    st = _m2_state(R, init)
+    ms = _time_loop(make_round(st), K, W)
+    err = int(st.err.item())
+    nbytes = 0
+    for i in range(W, W + K):
+        h = h_tr[i]
+        nbytes += sum(m2_verify_bytes(shape, int(x), T) for x in h)
+        c = (h + acc_tr[i])[fl_tr[i]]
+        nbytes += sum(m2_flush_bytes(shape, int(x)) for x in c)
+    mean_acc = float(np.mean(acc_tr[W:]))
+    del st
+    torch.cuda.empty_cache()
+    slots = torch.zeros(shape.B, T + 1, shape.H, shape.d, shape.n, device="cuda")
+    slots[:, 0] = _dev(init.S0)
+    cur = torch.zeros(shape.B, dtype=torch.int32, device="cuda")
+    berr = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def brnd(i):
+        R.ssm_spec_verify_baseline(slots, cur, *inp[i % P], A, y=y, err=berr)
+        R.ssm_spec_commit_baseline(acc[i % P], cur, T, berr)
+
+    bms = _time_loop(brnd, K, W)
+    bbytes = m2_snapshot_verify_bytes(shape, T) * shape.B
+    gbs = nbytes / K / (ms * 1e-3) / 1e9
+    line = {"suite": "spec", "workload": "Mamba-2 layer B=512, T=4, L=16, accepted ~ U{0..4}",
+            "rounds": K, "ms_per_round": ms, "rounds_per_s": 1e3 / ms,
+            "accepted_tokens_per_s": shape.B * mean_acc / (ms * 1e-3), "gbs": gbs, "frac_of_peak": gbs / peak,
+            "calls_per_round": "replay_spec_verify + replay_spec_commit + replay_flush",
+            "baseline_ms_per_round": bms, "baseline_gbs": bbytes / (bms * 1e-3) / 1e9,
+            "replay_over_baseline": bms / ms, "device_error_word": err | int(berr.item())}
+    print(json.dumps(line), flush=True)
+    del slots
+    torch.cuda.empty_cache()
+    return [line]
+
+
+def _gdn_state(R, init):
+    import torch
+
+    B = init.shape.B
+    ut = torch.float32 if init.shape.u_dtype == wl.F32 else torch.bfloat16
+    z = lambda n: torch.zeros(n, dtype=torch.int32, device="cuda")  # noqa: E731
+    return R.GdnState(_dev(init.S0), _dev(init.ring_u, ut), _dev(init.ring_k, _bf16()), _dev(init.ring_g),
+                      _dev(init.start, _i32()), _dev(init.count, _i32()), z(B), z(B), z(1)).add_workspace(4)
+
+
+def _gdn_inp(st):
+    return (_dev(st.q, _bf16()), _dev(st.k, _bf16()), _dev(st.v, _bf16()), _dev(st.beta), _dev(st.g))
+
+
+def suite_gdn(R, peak):
+    """GDN layer (B=256, Hv=32, Hk=16, d_k=d_v=128, L=16): decode steps
+    (decode + flush) vs the baseline state update, and T=4 verify rounds vs
+    the snapshot baseline."""
+    import torch
+
+    shape, seed, P = wl.GDN_LAYER, wl.SEED_GDN, 8
+    out = []
+    init = wl.gdn_init(shape, seed)
+    pool = [_gdn_inp(wl.gdn_step(shape, seed, t)) for t in range(P)]
+    y = torch.empty(shape.B, shape.Hv, shape.dv, device="cuda")
+    st = _gdn_state(R, init)
+    W, K = 4, 512
+
+    def step(i):
+        R.gdn_replay_decode_fused(st, *pool[i % P], y=y)
+
+    ms = _time_loop(step, K, W)
+    err = int(st.err.item())
+    per_h = np.array([gdn_decode_bytes(shape, h) for h in range(shape.L)], dtype=np.int64)
+    tr = fill_trace(init.count, shape.L, W + K)[W:]
+    # a fused fold adds only the S_0 write: S_0 and the entries were read for the output
+    nbytes = int(per_h[tr].sum()) + int((tr + 1 == shape.L).sum()) * 4 * shape.Hv * shape.dv * shape.dk
+    del st
+    st = _gdn_state(R, init)
+
+    def ustep(i):
+        R.gdn_replay_decode(st, *pool[i % P], y=y)
+        R.gdn_replay_flush(st)
+
+    ums = _time_loop(ustep, K, W)
+    err |= int(st.err.item())
+    del st
+    S = _dev(init.S0)
+
+    def bstep(i):
+        R.gdn_state_update_baseline(S, *pool[i % P], y=y)
+
+    bms = _time_loop(bstep, K, W)
+    del S
+    gbs = nbytes / K / (ms * 1e-3) / 1e9
+    out.append({"suite": "gdn_decode", "workload": "GDN layer B=256, Hv=32, Hk=16, d_k=d_v=128, L=16, u f32",
+                "steps": K, "ms_per_step": ms, "tokens_per_s": shape.B / (ms * 1e-3), "gbs": gbs,
+                "frac_of_peak": gbs / peak, "calls_per_step": "gdn_replay_decode_fused (workspace)",
+                "unfused_ms_per_step": ums, "unfused_calls": "gdn_replay_decode + gdn_replay_flush",
+                "baseline_ms_per_step": bms,
+                "baseline_gbs": gdn_baseline_bytes(shape) * shape.B / (bms * 1e-3) / 1e9,
+                "replay_over_baseline": bms / ms, "device_error_word": err})
+    print(json.dumps(out[-1]), flush=True)
+
+    T, Kv = 4, 256
+    init = wl.gdn_init(shape, seed + 50, fill_max=shape.L - T)
+    vpool = [_gdn_inp(wl.gdn_step(shape, seed + 50, r, T=T)) for r in range(P)]
+    acc = [_dev(wl.accepted_counts(shape.B, T, seed + 50, r), _i32()) for r in range(P)]
+    yv = torch.empty(shape.B, T, shape.Hv, shape.dv, device="cuda")
+    st = _gdn_state(R, init)
+    h_tr, fl_tr, acc_tr = [], [], []
+    for i in range(W + Kv):
+        h_tr.append(st.count.cpu().numpy().astype(np.int64))
+        R.gdn_replay_verify(st, *vpool[i % P], y=yv)
+        fl_tr.append(st.flag.cpu().numpy() != 0)
+        R.replay_spec_commit(acc[i % P], st.count, T, shape.L, st.err)
+        acc_tr.append(acc[i % P].cpu().numpy().astype(np.int64))
+        R.gdn_replay_flush(st)
+    del st
+    st = _gdn_state(R, init)
+
+    def rnd(i):
+        R.gdn_replay_verify(st, *vpool[i % P], y=yv)
+        R.replay_spec_commit(acc[i % P], st.count, T, shape.L, st.err)
+        R.gdn_replay_flush(st)
+
+    vms = _time_loop(rnd, Kv, W)
+    err = int(st.err.item())
+    nbytes = 0
+    for i in range(W, W + Kv):
+        nbytes += sum(gdn_verify_bytes(shape, int(x), T) for x in h_tr[i])
+        nbytes += sum(gdn_flush_bytes(shape, int(x)) for x in (h_tr[i] + acc_tr[i])[fl_tr[i]])
+    del st
+    torch.cuda.empty_cache()
+    slots = torch.zeros(shape.B, T + 1, shape.Hv, shape.dv, shape.dk, device="cuda")
+    slots[:, 0] = _dev(init.S0)
+    cur = torch.zeros(shape.B, dtype=torch.int32, device="cuda")
+    berr = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def brnd(i):
+        R.gdn_spec_verify_baseline(slots, cur, *vpool[i % P], y=yv, err=berr)
+        R.ssm_spec_commit_baseline(acc[i % P], cur, T, berr)
+
+    bvms = _time_loop(brnd, Kv, W)
+    gbs = nbytes / Kv / (vms * 1e-3) / 1e9
+    out.append({"suite": "gdn_verify", "workload": "GDN layer B=256, T=4, L=16, accepted ~ U{0..4}",
+                "rounds": Kv, "ms_per_round": vms, "rounds_per_s": 1e3 / vms,
+                "accepted_tokens_per_s": shape.B * float(np.mean(acc_tr[W:])) / (vms * 1e-3),
+                "gbs": gbs, "frac_of_peak": gbs / peak,
+                "calls_per_round": "gdn_replay_verify + replay_spec_commit + gdn_replay_flush",
+                "decode_step_ms": ms, "verify_over_decode": vms / ms,
+                "baseline_ms_per_round": bvms,
+                "baseline_gbs": gdn_snapshot_verify_bytes(shape, T) * shape.B / (bvms * 1e-3) / 1e9,
+                "replay_over_baseline": bvms / vms, "device_error_word": err | int(berr.item())})
+    print(json.dumps(out[-1]), flush=True)
+    del slots
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_suite(args):
+    import torch
+
+    torch.cuda.set_device(0)
+    from ssm_decode_hybrid_gb300 import replayssm as R
+
+    peak, _ = measured_peaks()
+    names = args.suite.split(",")
+    for name in names:
+        {"layers": suite_layers, "spec": suite_spec, "gdn": suite_gdn}[name](R, peak)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -509,10 +917,15 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", default=None,
+                    help="instead of the headline line, print one JSON line per measurement of the other "
+                         "workloads: comma-separated subset of layers,spec,gdn")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.suite:
+        run_suite(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

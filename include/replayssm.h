@@ -100,8 +100,10 @@ typedef struct {
   float *ring_dt;
   int32_t *start, *count, *flag, *sync;
   int32_t *err; /* one int32 */
-  float *work;  /* optional decode workspace of replay_decode_workspace_bytes()
-                   bytes, 16-byte aligned, or NULL (see replay_decode_step) */
+  float *work;        /* optional workspace, 16-byte aligned, or NULL (see
+                         replay_decode_step) */
+  int64_t work_bytes; /* its size; a call uses it only if it holds at least
+                         replay_decode_workspace_bytes() */
 } rssm_m2_replay;
 
 typedef struct {
@@ -118,6 +120,10 @@ typedef struct {
   float *ring_g;
   int32_t *start, *count, *flag, *sync;
   int32_t *err;
+  float *work;        /* optional workspace, 16-byte aligned, or NULL (see
+                         gdn_replay_decode) */
+  int64_t work_bytes; /* its size; a call with T drafts (T = 1: decode) uses it
+                         only if it holds gdn_replay_workspace_bytes(dims, T) */
 } rssm_gdn_replay;
 
 /* ------------------------------------------------------------------------ */
@@ -244,10 +250,31 @@ RSSM_API rssm_status gdn_state_update_baseline(const rssm_gdn_dims *dims, float 
  * h = count[b], S_h = (prod alpha_j) S_0 + sum_j (prod_{i>j} alpha_i) u_j k_j^T
  * (never materialised: S_h k and S_h q are formed from S_0 k, S_0 q and the
  * buffer), u = beta (v - alpha S_h k), y = alpha S_h q + u (k . q); append
- * (u, k, g); count <- h+1; flag <- (count == L).                             */
+ * (u, k, g); count <- h+1; flag <- (count == L).
+ * With a large enough st->work (bf16 inputs, d_k 64 or 128, L a multiple of
+ * 4) the step runs as a precompute launch per (sequence, key head) and a
+ * launch streaming S_0 per (sequence, value head, row block) ("Kernel design
+ * details"); otherwise as one launch per (sequence, value head).  The
+ * workspace carries nothing from one call to the next.                       */
 RSSM_API rssm_status gdn_replay_decode(const rssm_gdn_dims *dims, const rssm_gdn_replay *st, const void *q,
                               const void *k, const void *v, const float *beta, const float *g, void *y,
                               rssm_stream_t stream);
+
+/* GDN decode step with the flush fused in: the same outputs as
+ * gdn_replay_decode followed by gdn_replay_flush.  A sequence whose buffer
+ * fills with this token has all L entries (this token's u included) folded
+ * into S_0 by the same launches; it ends with count = 0, flag = 0.  Falls
+ * back to the two calls when the workspace path does not apply.
+ * Arguments as gdn_replay_decode.                                             */
+RSSM_API rssm_status gdn_replay_decode_fused(const rssm_gdn_dims *dims, const rssm_gdn_replay *st, const void *q,
+                                             const void *k, const void *v, const float *beta, const float *g,
+                                             void *y, rssm_stream_t stream);
+
+/* Bytes of the optional GDN workspace (rssm_gdn_replay.work) for calls with
+ * up to T drafts (T = 1 for decode): B * Hv * 4 * ceil((180 + 2 P dv) / 4)
+ * with P = 1 for T = 1, 4 for T <= 4, 8 for T <= 8.  0 for invalid
+ * arguments.  Host only.                                                      */
+RSSM_API int64_t gdn_replay_workspace_bytes(const rssm_gdn_dims *dims, int32_t T);
 
 /* GDN flush: S_0 <- (prod alpha_j) S_0 + sum_j (prod_{i>j} alpha_i) u_j k_j^T
  * over the committed entries of flagged sequences; pointer reset as the Mamba-2
@@ -280,7 +307,7 @@ RSSM_API rssm_status gdn_spec_verify_baseline(const rssm_gdn_dims *dims, int32_t
 /* Utilities                                                                  */
 /* ------------------------------------------------------------------------ */
 
-/* Library version, e.g. 100 for 0.1.0.  Host-only; never fails. */
+/* Library version, e.g. 200 for 0.2.0.  Host-only; never fails. */
 RSSM_API int32_t rssm_version(void);
 
 /* Static description of a status code.  Host-only; never fails. */

@@ -89,7 +89,7 @@ bool m2_replay_ok(const rssm_m2_dims &d, const rssm_m2_replay *s, bool need_sync
 bool gdn_replay_ok(const rssm_gdn_dims &d, const rssm_gdn_replay *s, bool need_sync) {
   return s != nullptr && ok16(s->S0) && ok_elem(s->ring_u, d.u_dtype) && ok16(s->ring_k) && ok4(s->ring_g) &&
          ok4(s->start) && ok4(s->count) && ok4(s->flag) && (!need_sync || ok4(s->sync)) &&
-         (s->err == nullptr || aligned(s->err, 4));
+         (s->err == nullptr || aligned(s->err, 4)) && (s->work == nullptr || aligned(s->work, 16));
 }
 
 int device_sm_count() {
@@ -103,7 +103,7 @@ int device_sm_count() {
 
 extern "C" {
 
-int32_t rssm_version(void) { return 100; }
+int32_t rssm_version(void) { return 200; }
 
 const char *rssm_status_string(rssm_status s) {
   switch (s) {
@@ -168,6 +168,7 @@ rssm_status replay_decode_step(const rssm_m2_dims *dims, const rssm_m2_replay *s
   a.A = A;
   a.y = y;
   a.work = s->work;
+  a.work_bytes = s->work_bytes;
   return cuda_status(launch_m2(M2Kind::Decode, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -199,6 +200,7 @@ rssm_status replay_decode_step_fused(const rssm_m2_dims *dims, const rssm_m2_rep
   a.A = A;
   a.y = y;
   a.work = s->work;
+  a.work_bytes = s->work_bytes;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_m2(M2Kind::DecodeFused, a, cs);
   if (e != cudaErrorNotSupported) return cuda_status(e);
@@ -343,8 +345,12 @@ static GdnLaunch gdn_replay_launch(const rssm_gdn_dims &d, const rssm_gdn_replay
   a.flag = s->flag;
   a.sync = s->sync;
   a.err = s->err;
+  a.work = s->work;
+  a.work_bytes = s->work_bytes;
   return a;
 }
+
+static FlushLaunch gdn_flush_launch(const rssm_gdn_dims &d, const rssm_gdn_replay *s);
 
 rssm_status gdn_replay_decode(const rssm_gdn_dims *dims, const rssm_gdn_replay *s, const void *q, const void *k,
                               const void *v, const float *beta, const float *g, void *y, rssm_stream_t stream) {
@@ -364,11 +370,36 @@ rssm_status gdn_replay_decode(const rssm_gdn_dims *dims, const rssm_gdn_replay *
   return cuda_status(launch_gdn(GdnKind::Decode, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-rssm_status gdn_replay_flush(const rssm_gdn_dims *dims, const rssm_gdn_replay *s, rssm_stream_t stream) {
+rssm_status gdn_replay_decode_fused(const rssm_gdn_dims *dims, const rssm_gdn_replay *s, const void *q,
+                                   const void *k, const void *v, const float *beta, const float *g, void *y,
+                                   rssm_stream_t stream) {
   rssm_status st = check_gdn_dims(dims);
   if (st) return st;
   const rssm_gdn_dims &d = *dims;
-  if (!gdn_replay_ok(d, s, true)) return RSSM_ERR_INVALID_ARG;
+  if (!gdn_replay_ok(d, s, true) || !ok16(q) || !ok16(k) || !ok_elem(v, d.in_dtype) || !ok4(beta) || !ok4(g) ||
+      !ok_elem(y, d.y_dtype))
+    return RSSM_ERR_INVALID_ARG;
+  GdnLaunch a = gdn_replay_launch(d, s);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.beta = beta;
+  a.g = g;
+  a.y = y;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (gdn_split_eligible(GdnKind::DecodeFused, a)) return cuda_status(launch_gdn_split(GdnKind::DecodeFused, a, cs));
+  // outside the two-launch kernels: the decode step, then the flush
+  cudaError_t e = launch_gdn(GdnKind::Decode, a, cs);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_flush(gdn_flush_launch(d, s), cs));
+}
+
+int64_t gdn_replay_workspace_bytes(const rssm_gdn_dims *dims, int32_t T) {
+  if (check_gdn_dims(dims) != RSSM_OK || T < 1 || T > kMaxT) return 0;
+  return static_cast<int64_t>(dims->B) * dims->Hv * gdn_work_stride_floats(dims->dv, gdn_window_width(T)) * 4;
+}
+
+static FlushLaunch gdn_flush_launch(const rssm_gdn_dims &d, const rssm_gdn_replay *s) {
   FlushLaunch a;
   std::memset(&a, 0, sizeof(a));
   a.B = d.B;
@@ -391,7 +422,15 @@ rssm_status gdn_replay_flush(const rssm_gdn_dims *dims, const rssm_gdn_replay *s
   a.sync = s->sync;
   a.err = s->err;
   a.num_sms = device_sm_count();
-  return cuda_status(launch_flush(a, reinterpret_cast<cudaStream_t>(stream)));
+  return a;
+}
+
+rssm_status gdn_replay_flush(const rssm_gdn_dims *dims, const rssm_gdn_replay *s, rssm_stream_t stream) {
+  rssm_status st = check_gdn_dims(dims);
+  if (st) return st;
+  const rssm_gdn_dims &d = *dims;
+  if (!gdn_replay_ok(d, s, true)) return RSSM_ERR_INVALID_ARG;
+  return cuda_status(launch_flush(gdn_flush_launch(d, s), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 rssm_status gdn_replay_verify(const rssm_gdn_dims *dims, const rssm_gdn_replay *s, int32_t T, const void *q,
@@ -506,6 +545,7 @@ extern "C" rssm_status replay_decode_step_fused_noalloc(const rssm_m2_dims *dims
   a.A = A;
   a.y = y;
   a.work = work;
+  a.work_bytes = static_cast<int64_t>(kStaticWorkFloats * sizeof(float));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   e = launch_m2(M2Kind::DecodeFused, a, cs);
   if (e != cudaErrorNotSupported) return cuda_status(e);

@@ -373,7 +373,8 @@ bool m2_decode_split_eligible(const M2Launch &a) {
   auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   if (HpG > 32) return false;
   const size_t psm = PrepSmem(a.L, a.n, a.d, HpG, es).total;
-  return a.work != nullptr && a16(a.work) && HpG <= 32 && psm <= 160 * 1024 && a.L % 4 == 0 && a.L <= 255 &&
+  const int64_t need = static_cast<int64_t>(a.B) * a.H * work_stride_floats(a.d, a.L) * 4;
+  return a.work != nullptr && a.work_bytes >= need && a16(a.work) && HpG <= 32 && psm <= 160 * 1024 && a.L % 4 == 0 && a.L <= 255 &&
          (a.d * es) % 16 == 0 &&
          a.d <= kSPass * rpp && a16(a.S) && a16(a.ring_v) && a16(a.ring_k) && a16(a.ring_dt) && a16(a.v) &&
          a16(a.k) && a16(a.q);

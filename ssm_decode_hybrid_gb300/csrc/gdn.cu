@@ -402,6 +402,8 @@ cudaError_t launch_gdn_n(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) 
     case GdnKind::SnapshotVerify:
       gdn_snapshot_verify_kernel<N, TI, TO><<<grid, kThreads, 0, stream>>>(a);
       break;
+    case GdnKind::DecodeFused:
+      return cudaErrorNotSupported;
   }
   return cudaGetLastError();
 }
@@ -426,6 +428,9 @@ cudaError_t launch_gdn_u(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) 
 }  // namespace
 
 cudaError_t launch_gdn(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) {
+  if ((kind == GdnKind::Decode || kind == GdnKind::Verify) && gdn_split_eligible(kind, a))
+    return launch_gdn_split(kind, a, stream);
+  if (kind == GdnKind::DecodeFused) return cudaErrorNotSupported;  // caller: decode, then flush
   if (a.in_dtype == RSSM_F32 && a.y_dtype == RSSM_F32) return launch_gdn_u<float, float>(kind, a, stream);
   if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_F32) return launch_gdn_u<bf16, float>(kind, a, stream);
   if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_BF16) return launch_gdn_u<bf16, bf16>(kind, a, stream);

@@ -1,9 +1,25 @@
 // Launch descriptors and launcher declarations of libreplayssm (internal).
 #pragma once
 
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 
 namespace rssm {
+
+// Number of SMs of the current device, looked up once per device.
+inline int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 
 // Everything a Mamba-2 kernel launch needs, already validated on the host.
 struct M2Launch {
@@ -17,7 +33,8 @@ struct M2Launch {
   const void *v, *k, *q;
   const float *dt, *A;
   void *y;
-  float *work;  // decode workspace (two-launch decode) or null
+  float *work;         // workspace of the two-launch decode, or null
+  int64_t work_bytes;  // its size
 };
 
 // Floats per (sequence, head) record of the two-launch decode workspace:
@@ -60,9 +77,27 @@ struct GdnLaunch {
   const void *q, *k, *v;
   const float *beta, *g;
   void *y;
+  float *work;         // workspace of the two-launch decode / verify, or null
+  int64_t work_bytes;  // its size
 };
 
-enum class GdnKind { Baseline, Decode, Verify, SnapshotVerify };
+enum class GdnKind { Baseline, Decode, DecodeFused, Verify, SnapshotVerify };
+
+// Window width P of the GDN two-launch kernels for a call with T drafts
+// (T = 1 also covers decode), and the floats of one (sequence, value head)
+// workspace record: a 180-float header of per-head scalars, then the 2P
+// buffer-term vectors of dv rows.
+__host__ __device__ constexpr int gdn_window_width(int T) { return T <= 1 ? 1 : (T <= 4 ? 4 : 8); }
+constexpr int kGdnWorkHeader = 180;
+__host__ __device__ constexpr int gdn_work_stride_floats(int dv, int P) {
+  return (kGdnWorkHeader + 2 * P * dv + 3) & ~3;
+}
+
+// Two launches through the caller's workspace (gdn_split.cu): a precompute
+// kernel per (sequence, key head), then a kernel streaming S_0 per (sequence,
+// value head, row block).  kind: Decode, DecodeFused or Verify.
+bool gdn_split_eligible(GdnKind kind, const GdnLaunch &a);
+cudaError_t launch_gdn_split(GdnKind kind, const GdnLaunch &a, cudaStream_t stream);
 
 cudaError_t launch_gdn(GdnKind kind, const GdnLaunch &a, cudaStream_t stream);
 

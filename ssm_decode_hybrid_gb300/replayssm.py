@@ -33,7 +33,8 @@ class M2Dims(ctypes.Structure):
 
 class M2Replay(ctypes.Structure):
     _fields_ = [(f, ctypes.c_void_p) for f in
-                ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err", "work")]
+                ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err", "work")] + \
+               [("work_bytes", ctypes.c_int64)]
 
 
 class GdnDims(ctypes.Structure):
@@ -42,7 +43,8 @@ class GdnDims(ctypes.Structure):
 
 class GdnReplay(ctypes.Structure):
     _fields_ = [(f, ctypes.c_void_p) for f in
-                ("S0", "ring_u", "ring_k", "ring_g", "start", "count", "flag", "sync", "err")]
+                ("S0", "ring_u", "ring_k", "ring_g", "start", "count", "flag", "sync", "err", "work")] + \
+               [("work_bytes", ctypes.c_int64)]
 
 
 EXPORTS = (
@@ -52,6 +54,7 @@ EXPORTS = (
     "gdn_state_update_baseline", "gdn_replay_decode", "gdn_replay_flush", "gdn_replay_verify",
     "gdn_spec_verify_baseline", "rssm_version", "rssm_status_string", "rssm_last_cuda_error",
     "replay_decode_workspace_bytes", "replay_decode_step_fused_noalloc",
+    "gdn_replay_decode_fused", "gdn_replay_workspace_bytes",
 )
 
 
@@ -73,6 +76,7 @@ def _load() -> ctypes.CDLL:
         "ssm_spec_commit_baseline": [I, I, P, P, P, P],
         "gdn_state_update_baseline": [ctypes.POINTER(GdnDims), P, P, P, P, P, P, P, P],
         "gdn_replay_decode": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), P, P, P, P, P, P, P],
+        "gdn_replay_decode_fused": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), P, P, P, P, P, P, P],
         "gdn_replay_flush": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), P],
         "gdn_replay_verify": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), I, P, P, P, P, P, P, P],
         "gdn_spec_verify_baseline": [ctypes.POINTER(GdnDims), I, P, P, P, P, P, P, P, P, P, P],
@@ -89,6 +93,8 @@ def _load() -> ctypes.CDLL:
     lib.rssm_last_cuda_error.argtypes = []
     lib.replay_decode_workspace_bytes.restype = ctypes.c_int64
     lib.replay_decode_workspace_bytes.argtypes = [ctypes.POINTER(M2Dims)]
+    lib.gdn_replay_workspace_bytes.restype = ctypes.c_int64
+    lib.gdn_replay_workspace_bytes.argtypes = [ctypes.POINTER(GdnDims), ctypes.c_int32]
     return lib
 
 
@@ -188,8 +194,9 @@ class Mamba2State:
             _f32(self.work, "work")
             if self.work.numel() * 4 < decode_workspace_bytes(self.dims()):
                 raise ValueError("work is smaller than decode_workspace_bytes()")
-        return M2Replay(*(_ptr(getattr(self, f)) for f in
-                          ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err", "work")))
+        ptrs = [_ptr(getattr(self, f)) for f in
+                ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err", "work")]
+        return M2Replay(*ptrs, 0 if self.work is None else self.work.numel() * 4)
 
 
 @dataclasses.dataclass
@@ -205,13 +212,26 @@ class GdnState:
     flag: torch.Tensor
     sync: torch.Tensor
     err: torch.Tensor
+    work: torch.Tensor | None = None  # workspace (f32, gdn_workspace_bytes) or None
 
     @classmethod
-    def empty(cls, B, Hv, Hk, dk, dv, L, dtype=torch.bfloat16, u_dtype=torch.float32, device="cuda"):
+    def empty(cls, B, Hv, Hk, dk, dv, L, dtype=torch.bfloat16, u_dtype=torch.float32, device="cuda",
+              workspace_T=4):
         z = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt, device=device)  # noqa: E731
-        return cls(z(B, Hv, dv, dk), z(B, Hv, L, dv, dt=u_dtype), z(B, Hk, L, dk, dt=dtype), z(B, Hv, L),
-                   z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32),
-                   z(1, dt=torch.int32))
+        st = cls(z(B, Hv, dv, dk), z(B, Hv, L, dv, dt=u_dtype), z(B, Hk, L, dk, dt=dtype), z(B, Hv, L),
+                 z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32), z(B, dt=torch.int32),
+                 z(1, dt=torch.int32))
+        if workspace_T:
+            st.add_workspace(workspace_T)
+        return st
+
+    def add_workspace(self, max_T: int = 4):
+        """Attach a workspace for decode steps and verify rounds of up to max_T
+        drafts, which lets them run as a precompute launch plus a launch that
+        streams S_0."""
+        nbytes = gdn_workspace_bytes(self.dims(), max_T)
+        self.work = torch.empty(nbytes // 4, dtype=torch.float32, device=self.S0.device)
+        return self
 
     @property
     def shape(self):
@@ -227,13 +247,24 @@ class GdnState:
         _f32(self.ring_g, "ring_g")
         for name in ("start", "count", "flag", "sync", "err"):
             _i32(getattr(self, name), name)
-        return GdnReplay(*(_ptr(getattr(self, f)) for f in
-                           ("S0", "ring_u", "ring_k", "ring_g", "start", "count", "flag", "sync", "err")))
+        if self.work is not None:
+            _f32(self.work, "work")
+        ptrs = [_ptr(getattr(self, f)) for f in
+                ("S0", "ring_u", "ring_k", "ring_g", "start", "count", "flag", "sync", "err", "work")]
+        return GdnReplay(*ptrs, 0 if self.work is None else self.work.numel() * 4)
 
 
 # ---------------------------------------------------------------------------
 # Mamba-2 calls
 # ---------------------------------------------------------------------------
+
+
+def gdn_workspace_bytes(dims: GdnDims, max_T: int = 1) -> int:
+    """Bytes of the optional GDN workspace for calls with up to max_T drafts."""
+    n = int(LIB.gdn_replay_workspace_bytes(ctypes.byref(dims), int(max_T)))
+    if n <= 0:
+        raise ReplaySSMError("gdn_replay_workspace_bytes: invalid arguments")
+    return n
 
 
 def decode_workspace_bytes(dims: M2Dims) -> int:
@@ -362,6 +393,17 @@ def gdn_replay_decode(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.f
     st = state.struct()
     _check(LIB.gdn_replay_decode(ctypes.byref(dims), ctypes.byref(st), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
                                  _ptr(y), _stream()), "gdn_replay_decode")
+    return y
+
+
+def gdn_replay_decode_fused(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+    """GDN decode step with the full-buffer flush in the same launches."""
+    B, Hv, Hk, dk, dv, L = state.shape
+    y = _out(y, (B, Hv, dv), y_dtype, state.S0.device)
+    dims = state.dims(y.dtype)
+    st = state.struct()
+    _check(LIB.gdn_replay_decode_fused(ctypes.byref(dims), ctypes.byref(st), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                       _ptr(g), _ptr(y), _stream()), "gdn_replay_decode_fused")
     return y
 
 

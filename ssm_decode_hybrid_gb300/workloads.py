@@ -215,3 +215,35 @@ SEED_NEMOTRON = 1001
 SEED_SWEEP = 1002
 SEED_SPEC = 1003
 SEED_GDN = 1004
+
+
+# ---------------------------------------------------------------------------
+# device-side generators for timing-only workloads (no oracle comparison)
+# ---------------------------------------------------------------------------
+
+
+def mamba2_state_tensors_device(shape: Mamba2Shape, seed: int, device, fill_max: int | None = None):
+    """S_0, ring buffer and pointers of one Mamba-2 layer drawn directly on the
+    device with a seeded torch generator, from the same distributions as
+    mamba2_init (for sizes where host generation would dominate).  Returns a
+    dict of tensors keyed like Mamba2Init's fields."""
+    import torch
+
+    s = shape
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if s.in_dtype == BF16 else torch.float32
+    fm = s.L - 1 if fill_max is None else fill_max
+
+    def normal(*size):
+        return torch.randn(*size, generator=g, device=device, dtype=torch.float32)
+
+    return {
+        "S0": 0.1 * normal(s.B, s.H, s.d, s.n),
+        "A": -torch.exp(torch.rand(s.H, generator=g, device=device)),
+        "ring_v": normal(s.B, s.H, s.L, s.d).to(dt),
+        "ring_k": normal(s.B, s.G, s.L, s.n).to(dt),
+        "ring_dt": torch.nn.functional.softplus(normal(s.B, s.H, s.L)),
+        "start": torch.randint(0, s.L, (s.B,), generator=g, device=device, dtype=torch.int32),
+        "count": torch.randint(0, fm + 1, (s.B,), generator=g, device=device, dtype=torch.int32),
+    }

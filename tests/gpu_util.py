@@ -68,16 +68,22 @@ def m2_step_dev(step: wl.Mamba2Step, in_dtype: str):
     return dev(step.v, t), dev(step.k, t), dev(step.q, t), dev(step.dt)
 
 
-def gdn_state(init: wl.GdnInit):
+def gdn_state(init: wl.GdnInit, workspace_T: int = 8):
+    """Device state from a seeded init; workspace_T > 0 attaches a workspace for
+    calls of up to that many drafts (two-launch kernels), 0 leaves it out."""
     from ssm_decode_hybrid_gb300 import replayssm as rs
 
     s = init.shape
     B = s.B
-    return rs.GdnState(
+    st = rs.GdnState(
         S0=dev(init.S0), ring_u=dev(init.ring_u, TORCH_DT[s.u_dtype]), ring_k=dev(init.ring_k, TORCH_DT[s.in_dtype]),
         ring_g=dev(init.ring_g), start=dev(init.start, torch.int32), count=dev(init.count, torch.int32),
         flag=torch.zeros(B, dtype=torch.int32, device="cuda"), sync=torch.zeros(B, dtype=torch.int32, device="cuda"),
         err=torch.zeros(1, dtype=torch.int32, device="cuda"))
+    if workspace_T:
+        st.add_workspace(workspace_T)
+        st.work.fill_(float("nan"))  # scratch: nothing may depend on its prior contents
+    return st
 
 
 def gdn_step_dev(step: wl.GdnStep, in_dtype: str):

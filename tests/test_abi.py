@@ -42,7 +42,7 @@ def test_binding_covers_exports():
     from ssm_decode_hybrid_gb300 import replayssm as R
 
     assert set(declared_symbols()) == set(R.EXPORTS)
-    assert R.version() == 100
+    assert R.version() == 200
     assert R.LIB.rssm_status_string(-1) == b"invalid argument"
     assert R.LIB.rssm_status_string(-2) == b"unsupported shape or dtype"
 

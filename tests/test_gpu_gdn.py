@@ -31,23 +31,27 @@ def check_pointers(state, orc, idx, what):
     np.testing.assert_array_equal(host(state.flag)[idx], orc.flag, err_msg=f"{what}: flag")
 
 
-def run_decode(shape, seed, steps, sample=None, y_dtype=torch.float32):
+def run_decode(shape, seed, steps, sample=None, y_dtype=torch.float32, workspace_T=8, fused=False):
     R = rs()
     init = wl.gdn_init(shape, seed)
     idx = np.arange(shape.B) if sample is None else np.asarray(sample)
-    state = gdn_state(init)
+    state = gdn_state(init, workspace_T)
     orc = oracle_replay(init, idx)
     rtol, atol = tol_for(y_dtype)
     if shape.u_dtype == wl.BF16:
         rtol, atol = max(rtol, 1e-2), max(atol, 1e-3)
     for t in range(steps):
         st = wl.gdn_step(shape, seed, t)
-        y = R.gdn_replay_decode(state, *gdn_step_dev(st, shape.in_dtype), y_dtype=y_dtype)
-        flags = host(state.flag)
-        R.gdn_replay_flush(state)
+        if fused:
+            y = R.gdn_replay_decode_fused(state, *gdn_step_dev(st, shape.in_dtype), y_dtype=y_dtype)
+        else:
+            y = R.gdn_replay_decode(state, *gdn_step_dev(st, shape.in_dtype), y_dtype=y_dtype)
+            flags = host(state.flag)
+            R.gdn_replay_flush(state)
         y_ref = orc.decode_step(take(st.q, idx), take(st.k, idx), take(st.v, idx), take(st.beta, idx),
                                 take(st.g, idx))
-        np.testing.assert_array_equal(flags[idx], orc.flag, err_msg=f"step {t}: flag")
+        if not fused:
+            np.testing.assert_array_equal(flags[idx], orc.flag, err_msg=f"step {t}: flag")
         orc.flush()
         assert_close(y[idx], y_ref, rtol, atol, what=f"step {t}: y")
         check_pointers(state, orc, idx, f"step {t}")
@@ -67,10 +71,28 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("shape", SHAPES,
-                         ids=lambda s: f"B{s.B}Hv{s.Hv}Hk{s.Hk}dk{s.dk}dv{s.dv}L{s.L}{s.in_dtype}u{s.u_dtype}")
-def test_decode_parity(shape):
-    run_decode(shape, 200, steps=2 * shape.L + 3)
+WORKSPACE = [pytest.param(8, id="two-launch"), pytest.param(0, id="one-launch")]
+SHAPE_ID = lambda s: f"B{s.B}Hv{s.Hv}Hk{s.Hk}dk{s.dk}dv{s.dv}L{s.L}{s.in_dtype}u{s.u_dtype}"  # noqa: E731
+
+
+@pytest.mark.parametrize("workspace_T", WORKSPACE)
+@pytest.mark.parametrize("shape", SHAPES, ids=SHAPE_ID)
+def test_decode_parity(shape, workspace_T):
+    run_decode(shape, 200, steps=2 * shape.L + 3, workspace_T=workspace_T)
+
+
+FUSED_SHAPES = [
+    wl.GdnShape(B=4, Hv=8, Hk=4, dk=128, dv=128, L=16, in_dtype=wl.BF16),  # the GDN layer, small batch
+    wl.GdnShape(B=3, Hv=6, Hk=3, dk=64, dv=72, L=8, in_dtype=wl.BF16),  # two row blocks, ragged second
+    wl.GdnShape(B=3, Hv=2, Hk=2, dk=128, dv=64, L=4, in_dtype=wl.BF16, u_dtype=wl.BF16),  # bf16 u
+    wl.GdnShape(B=2, Hv=4, Hk=2, dk=32, dv=20, L=5, in_dtype=wl.BF16),  # outside the two-launch kernels
+]
+
+
+@pytest.mark.parametrize("shape", FUSED_SHAPES, ids=SHAPE_ID)
+def test_decode_fused_parity(shape):
+    """gdn_replay_decode_fused == decode step followed by the flush."""
+    run_decode(shape, 203, steps=2 * shape.L + 3, fused=True)
 
 
 def test_decode_bf16_u_and_bf16_y():
@@ -102,37 +124,49 @@ def test_baseline_parity():
     assert_close(S, S_ref, what="baseline state")
 
 
-def run_verify(shape, T, rounds, seed, sample=None):
+def run_verify(shape, T, rounds, seed, sample=None, workspace_T=8):
     R = rs()
     init = wl.gdn_init(shape, seed, fill_max=shape.L - T)
     idx = np.arange(shape.B) if sample is None else np.asarray(sample)
-    state = gdn_state(init)
+    state = gdn_state(init, workspace_T)
     orc = oracle_replay(init, idx)
+    rtol, atol = (1e-2, 1e-3) if shape.u_dtype == wl.BF16 else (1e-3, 1e-4)
     for r in range(rounds):
         st = wl.gdn_step(shape, seed, r, T=T)
         acc = wl.accepted_counts(shape.B, T, seed, r)
         y = R.gdn_replay_verify(state, *gdn_step_dev(st, shape.in_dtype))
         Y_ref = orc.verify(take(st.q, idx), take(st.k, idx), take(st.v, idx), take(st.beta, idx), take(st.g, idx))
         np.testing.assert_array_equal(host(state.flag)[idx], orc.flag, err_msg=f"round {r}: flag")
-        assert_close(y[idx], Y_ref, what=f"round {r}: y")
+        assert_close(y[idx], Y_ref, rtol, atol, what=f"round {r}: y")
         R.replay_spec_commit(dev(acc, torch.int32), state.count, T, shape.L, state.err)
         orc.commit(take(acc, idx), T)
         R.gdn_replay_flush(state)
         orc.flush()
         check_pointers(state, orc, idx, f"round {r}")
-    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert_close(state.S0[idx], orc.S0, rtol, atol, what="final S0")
     assert int(host(state.err)[0]) == 0
 
 
+@pytest.mark.parametrize("workspace_T", WORKSPACE)
 @pytest.mark.parametrize("T", [1, 2, 4, 6, 8])
-def test_chunked_verify_parity(T):
+def test_chunked_verify_parity(T, workspace_T):
     shape = wl.GdnShape(B=8, Hv=8, Hk=4, dk=128, dv=128, L=16, in_dtype=wl.BF16)
-    run_verify(shape, T, rounds=10, seed=300 + T)
+    run_verify(shape, T, rounds=10, seed=300 + T, workspace_T=workspace_T)
+
+
+def test_chunked_verify_workspace_too_small_for_T():
+    """A workspace sized for 4 drafts: T = 4 uses it, T = 6 takes the one-launch path; both match."""
+    shape = wl.GdnShape(B=4, Hv=8, Hk=4, dk=64, dv=64, L=16, in_dtype=wl.BF16)
+    run_verify(shape, 4, rounds=6, seed=330, workspace_T=4)
+    run_verify(shape, 6, rounds=6, seed=331, workspace_T=4)
 
 
 def test_chunked_verify_small_shapes():
     run_verify(wl.GdnShape(B=4, Hv=4, Hk=2, dk=16, dv=16, L=6, in_dtype=wl.F32), 3, rounds=10, seed=310)
     run_verify(wl.GdnShape(B=4, Hv=6, Hk=3, dk=64, dv=36, L=9, in_dtype=wl.BF16), 4, rounds=10, seed=311)
+    run_verify(wl.GdnShape(B=3, Hv=6, Hk=3, dk=64, dv=72, L=8, in_dtype=wl.BF16), 3, rounds=8, seed=312)
+    run_verify(wl.GdnShape(B=3, Hv=4, Hk=2, dk=128, dv=64, L=12, in_dtype=wl.BF16, u_dtype=wl.BF16), 2, rounds=8,
+               seed=313)
 
 
 def test_chunked_verify_full_batch_sampled():
