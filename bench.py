@@ -718,6 +718,7 @@ def suite_spec(R, peak):
     shape, T, seed, P = wl.SPEC_MAMBA2, 4, wl.SEED_SPEC, 8
     init = wl.mamba2_init(shape, seed, fill_max=shape.L - T)
     inp, acc = _spec_pool(shape, seed, T, P)
+    mk = lambda: _m2_state(R, init).add_workspace(max_T=T)  # noqa: E731
     A = _dev(init.A)
     y = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
     W, K = 4, 256
@@ -730,7 +731,7 @@ def suite_spec(R, peak):
         return rnd
 
     # the committed-count trace of these rounds, recorded on an untimed copy
-    st = _m2_state(R, init)
+    st = mk()
     h_tr, fl_tr, acc_tr = [], [], []
     for i in range(W + K):
         h_tr.append(st.count.cpu().numpy().astype(np.int64))
@@ -740,7 +741,7 @@ def suite_spec(R, peak):
         acc_tr.append(acc[i % P].cpu().numpy().astype(np.int64))
         R.replay_flush(st, A)
     del st
-    st = _m2_state(R, init)
+    st = mk()
     ms = _time_loop(make_round(st), K, W)
     err = int(st.err.item())
     nbytes = 0

@@ -162,6 +162,11 @@ RSSM_API rssm_status replay_decode_step(const rssm_m2_dims *dims, const rssm_m2_
  * Host only; launches nothing.                                                */
 RSSM_API int64_t replay_decode_workspace_bytes(const rssm_m2_dims *dims);
 
+/* Bytes of the optional workspace for replay_spec_verify with up to T drafts:
+ * B * H * 4 * ceil((16 + P d) / 4) with P = 1 for T = 1, 4 for T <= 4, 8 for
+ * T <= 8.  0 for invalid arguments.  Host only.                               */
+RSSM_API int64_t replay_verify_workspace_bytes(const rssm_m2_dims *dims, int32_t T);
+
 /* Flush ("Algorithm -- Mamba-2 standard decode", flush): for every sequence
  * with flag[b] != 0 and c = count[b] committed entries,
  *   S_0 <- abar S_0 + sum_{j=1}^{c} s_j v_j k_j^T
@@ -207,6 +212,10 @@ RSSM_API rssm_status replay_decode_step_fused_noalloc(const rssm_m2_dims *dims, 
  * and, for s = 1..T with p_s = h + s,
  *   Y_s = abar_s (S_0 q_s) + sum_{j<=p_s} w_{j,s} (k_j^T q_s) v_j.
  * count is unchanged; flag <- (h + 2T > L) (early flush one window ahead).
+ * With st->work holding replay_verify_workspace_bytes(dims, T) bytes (and L a
+ * multiple of 4) the round runs as a precompute launch per (sequence, group)
+ * and a launch streaming S_0 once per (sequence, head) for all T drafts;
+ * otherwise as one launch per (sequence, head).  Same results.
  *   v  in_dtype [B][T][H][d]   k, q in_dtype [B][T][G][n]   dt float [B][T][H]
  *   y  y_dtype [B][T][H][d]                                                   */
 RSSM_API rssm_status replay_spec_verify(const rssm_m2_dims *dims, const rssm_m2_replay *st, int32_t T,

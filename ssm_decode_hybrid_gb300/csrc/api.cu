@@ -124,6 +124,11 @@ int64_t replay_decode_workspace_bytes(const rssm_m2_dims *dims) {
   return static_cast<int64_t>(dims->B) * dims->H * work_stride_floats(dims->d, dims->L) * 4;
 }
 
+int64_t replay_verify_workspace_bytes(const rssm_m2_dims *dims, int32_t T) {
+  if (check_m2_dims(dims) != RSSM_OK || T < 1 || T > kMaxT) return 0;
+  return static_cast<int64_t>(dims->B) * dims->H * m2_verify_stride_floats(dims->d, gdn_window_width(T)) * 4;
+}
+
 rssm_status ssm_state_update_baseline(const rssm_m2_dims *dims, float *S, const void *v, const void *k,
                                       const void *q, const float *dt, const float *A, void *y,
                                       rssm_stream_t stream) {
@@ -272,6 +277,8 @@ rssm_status replay_spec_verify(const rssm_m2_dims *dims, const rssm_m2_replay *s
   a.dt = dt;
   a.A = A;
   a.y = y;
+  a.work = s->work;
+  a.work_bytes = s->work_bytes;
   return cuda_status(launch_m2(M2Kind::Verify, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -364,7 +364,309 @@ cudaError_t launch_split_f(const M2Launch &a, cudaStream_t stream) {
   return launch_split_t<kFuse, float, bf16>(a, stream);
 }
 
+// ---------------------------------------------------------------------------
+// speculative verify of T drafts ("Algorithm -- speculative decoding"):
+//   Y_s = abar_s (S_0 q_s) + sum_{j <= p_s} w_{j,s} (k_j^T q_s) v_j,  p_s = h + s,
+// with the drafts' (v, k, Delta) written tentatively after the committed window.
+// The precompute kernel (per sequence and group) forms abar_s and the buffer
+// vectors buf_s[r] = sum_j w_{j,s} (k_j^T q_s) v_j[r] for every draft s; the
+// streaming kernel (per sequence and head) reads S_0 once for all T queries.
+// Workspace record per (sequence, head): abar_s [kMaxT], info, pad, then
+// buf [P][d] (P = 1, 4 or 8 >= T).
+// ---------------------------------------------------------------------------
+constexpr int kVwInfo = kMaxT;
+constexpr int kVwBuf = kM2VerifyHeader;
+
+struct VPrepSmem {
+  uint32_t k_ring, v_ring, dt_ring, k_in, q_in, v_in, dots, coef, total;
+  __host__ __device__ VPrepSmem(int L, int N, int d, int HpG, int P, int es) {
+    k_ring = 0;
+    v_ring = k_ring + L * N * es;
+    dt_ring = v_ring + HpG * L * d * es;
+    k_in = dt_ring + HpG * L * 4;
+    q_in = k_in + P * N * es;
+    v_in = q_in + P * N * es;            // [P][HpG][d]
+    dots = v_in + P * HpG * d * es;      // float [P][kMaxL]: k_e . q_s over the committed and draft keys
+    coef = dots + P * kMaxL * 4;         // float [HpG][P][kMaxL]
+    total = coef + HpG * P * kMaxL * 4;
+  }
+};
+
+template <int N, int NT, typename TI>
+__global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) {
+  constexpr int LPR = N / 4;
+  constexpr int es = sizeof(TI);
+  extern __shared__ __align__(128) unsigned char psm[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_ptr[2];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int HpG = a.H / a.G;
+  const int b = blockIdx.x / a.G, g = blockIdx.x - b * a.G;
+  const int i = g * HpG + w;
+  const int d = a.d, L = a.L, T = a.T;
+  const size_t bg = static_cast<size_t>(b) * a.G + g;
+  const size_t h0 = static_cast<size_t>(b) * a.H + g * HpG;
+  const size_t bh = h0 + w;
+  const VPrepSmem lay(L, N, d, HpG, NT, es);
+
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    // the Delta rings and the drafts' k, q, v first; then, once the pointers
+    // are in, the committed slots of the k and v rings (at their own slot
+    // positions in shared memory)
+    mbar_expect_tx(&bar, (lay.k_in - lay.dt_ring) + static_cast<uint32_t>(T) * (2 * N + HpG * d) * es);
+    bulk_g2s(psm + lay.dt_ring, a.ring_dt + h0 * L, lay.k_in - lay.dt_ring, &bar);
+    for (int m = 0; m < T; ++m) {
+      const size_t kq = ((static_cast<size_t>(b) * T + m) * a.G + g) * N * es;
+      bulk_g2s(psm + lay.k_in + m * N * es, static_cast<const unsigned char *>(a.k) + kq, N * es, &bar);
+      bulk_g2s(psm + lay.q_in + m * N * es, static_cast<const unsigned char *>(a.q) + kq, N * es, &bar);
+      const size_t vo = ((static_cast<size_t>(b) * T + m) * a.H + g * HpG) * d * es;
+      bulk_g2s(psm + lay.v_in + m * HpG * d * es, static_cast<const unsigned char *>(a.v) + vo, HpG * d * es, &bar);
+    }
+    const int hc = a.count[b], sc = a.start[b];
+    s_ptr[0] = hc;
+    s_ptr[1] = sc;
+    if (hc >= 1 && hc <= L && sc >= 0 && sc < L) {
+      const int n1 = min(hc, L - sc), n2 = hc - n1;
+      mbar_expect_tx(&bar, static_cast<uint32_t>(hc) * (N * es + HpG * d * es));
+      const unsigned char *gk = static_cast<const unsigned char *>(a.ring_k) + bg * L * N * es;
+      bulk_g2s(psm + lay.k_ring + sc * N * es, gk + static_cast<size_t>(sc) * N * es, n1 * N * es, &bar);
+      if (n2 > 0) bulk_g2s(psm + lay.k_ring, gk, n2 * N * es, &bar);
+      for (int hw = 0; hw < HpG; ++hw) {
+        const unsigned char *gv = static_cast<const unsigned char *>(a.ring_v) + (h0 + hw) * L * d * es;
+        unsigned char *sv = psm + lay.v_ring + static_cast<size_t>(hw) * L * d * es;
+        bulk_g2s(sv + static_cast<size_t>(sc) * d * es, gv + static_cast<size_t>(sc) * d * es, n1 * d * es, &bar);
+        if (n2 > 0) bulk_g2s(sv, gv, n2 * d * es, &bar);
+      }
+    }
+    mbar_arrive(&bar);
+  }
+  pdl_launch_dependents();
+  const float Ai = a.A[i];
+  const float dt_draft = (lane < T) ? a.dt[(static_cast<size_t>(b) * T + lane) * a.H + i] : 0.f;
+  __syncthreads();  // barrier initialised, pointers read
+  bool arrived = true;
+  if (w == 0) arrived = mbar_wait(&bar, 0);
+  if (__syncthreads_or(!arrived)) {
+    if (tid == 0) {
+      set_err(a.err, RSSM_EBIT_TIMEOUT);
+      mbar_wait(&bar, 0);  // bounded: the copies must land before shared memory is released
+    }
+    return;
+  }
+  const int h = s_ptr[0], st = s_ptr[1];
+  float *wk = a.work + bh * stride;
+  if (h < 0 || st < 0 || st >= L || h + T > L) {
+    if (lane == 0) reinterpret_cast<int *>(wk)[kVwInfo] = 0;
+    if (tid == 0) set_err(a.err, RSSM_EBIT_WINDOW);
+    return;
+  }
+  const int ne = h + T;  // committed entries, then the drafts
+  const TI *kring = reinterpret_cast<const TI *>(psm + lay.k_ring);
+  const TI *kin = reinterpret_cast<const TI *>(psm + lay.k_in);
+  const TI *qin = reinterpret_cast<const TI *>(psm + lay.q_in);
+  const TI *vring = reinterpret_cast<const TI *>(psm + lay.v_ring) + static_cast<size_t>(w) * L * d;
+  const TI *vin = reinterpret_cast<const TI *>(psm + lay.v_in);
+  const float *sdt = reinterpret_cast<const float *>(psm + lay.dt_ring) + w * L;
+  float *sM = reinterpret_cast<float *>(psm + lay.dots);
+  float *scoef = reinterpret_cast<float *>(psm + lay.coef) + w * NT * kMaxL;
+
+  // k_e . q_s for every entry e and draft s: pairs spread over the lane groups
+  {
+    constexpr int V = LPR >= 4 ? 4 : LPR;
+    constexpr int RPW = 32 / LPR;
+    const int col = (lane % LPR) * 4;
+    const int nw = blockDim.x / 32, grp = lane / LPR;
+    const int npair = ne * T;
+    for (int base = w * RPW * V; base < npair; base += nw * RPW * V) {
+      float x[V];
+#pragma unroll
+      for (int m = 0; m < V; ++m) {
+        const int pi = base + grp * V + m;
+        x[m] = 0.f;
+        if (pi < npair) {
+          const int e = pi / T, sq = pi - e * T;
+          const TI *key = e < h ? kring + static_cast<size_t>(wrapL(st + e, L)) * N : kin + (e - h) * N;
+          x[m] = dot4(load4(key + col), load4(qin + sq * N + col));
+        }
+      }
+      group_sum_multi<LPR, V>(x, lane);
+      const int pi = base + grp * V + (lane % LPR) / (LPR / V);
+      if ((lane % (LPR / V)) == 0 && pi < npair) {
+        const int e = pi / T, sq = pi - e * T;
+        sM[sq * kMaxL + e] = x[0];
+      }
+    }
+  }
+  // decay of this head for each draft s: w_{e,s} = Delta_e exp(A sum_{e<m<p_s} Delta_m)
+  const float dd = __shfl_sync(kFull, dt_draft, (lane - h) & 31);
+  const float dte = (lane < h) ? sdt[wrapL(st + lane, L)] : (lane < ne ? dd : 0.f);
+  __syncthreads();  // sM complete
+  for (int sq = 0; sq < T; ++sq) {
+    const int p = h + sq + 1;
+    float tot;
+    const float ex = excl_suffix_sum((lane < p) ? Ai * dte : 0.f, lane, tot);
+    scoef[sq * kMaxL + lane] = (lane < p) ? dte * expf(ex) * sM[sq * kMaxL + lane] : 0.f;
+    if (lane == 0) wk[sq] = expf(tot);
+  }
+  if (lane == 0) reinterpret_cast<int *>(wk)[kVwInfo] = h | (st << 8) | kInfoValid;
+  __syncwarp();
+
+  // buffer vectors of this head, two rows per lane
+  for (int r = 2 * lane; r < d; r += 64) {
+    float2 acc[NT];
+#pragma unroll
+    for (int sq = 0; sq < NT; ++sq) acc[sq] = make_float2(0.f, 0.f);
+    for (int e = 0; e < ne; ++e) {
+      const float2 v2 = load2((e < h ? vring + static_cast<size_t>(wrapL(st + e, L)) * d
+                                     : vin + static_cast<size_t>((e - h) * HpG + w) * d) + r);
+#pragma unroll
+      for (int sq = 0; sq < NT; ++sq) {
+        const float c = scoef[sq * kMaxL + e];
+        acc[sq].x = fmaf(c, v2.x, acc[sq].x);
+        acc[sq].y = fmaf(c, v2.y, acc[sq].y);
+      }
+    }
+#pragma unroll
+    for (int sq = 0; sq < NT; ++sq)
+      if (sq < T) *reinterpret_cast<float2 *>(wk + kVwBuf + sq * d + r) = acc[sq];
+  }
+
+  // the drafts' entries, tentatively, at slots (start + h + m) mod L
+  for (int m = 0; m < T; ++m) {
+    const int sl = (st + h + m) % L;
+    uint32_t *rv = reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_v) + (bh * L + sl) * d);
+    const uint32_t *sv = reinterpret_cast<const uint32_t *>(vin + static_cast<size_t>(m * HpG + w) * d);
+    for (int c = lane; c < d * es / 4; c += 32) rv[c] = sv[c];
+    const float dtm = __shfl_sync(kFull, dt_draft, m);
+    if (lane == 0) a.ring_dt[bh * L + sl] = dtm;
+    if (w == 0) {
+      uint32_t *rk = reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_k) + (bg * L + sl) * N);
+      const uint32_t *sk = reinterpret_cast<const uint32_t *>(kin + m * N);
+      for (int c = lane; c < N * es / 4; c += 32) rk[c] = sk[c];
+    }
+  }
+}
+
+template <int N, int NT, typename TI, typename TO>
+__global__ void __launch_bounds__(kThreads, NT == 8 ? 2 : 4) m2_vstream_kernel(M2Launch a, int stride) {
+  constexpr int LPR = N / 4, RPW = 32 / LPR, RPP = kWarps * RPW;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x / a.H, i = blockIdx.x - b * a.H;
+  const int d = a.d, L = a.L, T = a.T;
+  const size_t bh = static_cast<size_t>(b) * a.H + i;
+  const int col = (lane % LPR) * 4;
+  const int row0 = warp * RPW + lane / LPR;
+  const float *wk = a.work + bh * stride;
+
+  const float *S0 = a.S + bh * d * N;
+  float4 s[kSPass];
+#pragma unroll
+  for (int p = 0; p < kSPass; ++p) {
+    const int r = row0 + p * RPP;
+    s[p] = (r < d) ? ldg_stream4(S0 + static_cast<size_t>(r) * N + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int g = i / (a.H / a.G);
+  float4 xv[NT];
+#pragma unroll
+  for (int sq = 0; sq < NT; ++sq)
+    xv[sq] = (sq < T) ? load4(static_cast<const TI *>(a.q) + ((static_cast<size_t>(b) * T + sq) * a.G + g) * N + col)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  pdl_wait();  // the precompute grid has finished
+  const int info = reinterpret_cast<const int *>(wk)[kVwInfo];
+  if (!(info & kInfoValid)) return;
+  if (i == 0 && tid == 0) a.flag[b] = ((info & 0xff) + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
+
+  // S_0 q_s, PB passes x NT drafts reduced together; the reducing lane writes y
+  static_assert(NT <= LPR, "drafts per lane group");
+  constexpr int PB = (kSPass * NT <= LPR) ? kSPass : LPR / NT;
+  TO *y = static_cast<TO *>(a.y);
+#pragma unroll
+  for (int p0 = 0; p0 < kSPass; p0 += PB) {
+    float x[PB * NT];
+#pragma unroll
+    for (int pp = 0; pp < PB; ++pp)
+#pragma unroll
+      for (int sq = 0; sq < NT; ++sq) x[pp * NT + sq] = dot4(s[p0 + pp], xv[sq]);
+    group_sum_multi<LPR, PB * NT>(x, lane);
+    constexpr int SPAN = LPR / (PB * NT);
+    const int idx = (lane % LPR) / SPAN;
+    const int pp = idx / NT, sq = idx - pp * NT;
+    const int r = row0 + (p0 + pp) * RPP;
+    if ((lane % SPAN) == 0 && r < d && sq < T)
+      store1(y + ((static_cast<size_t>(b) * T + sq) * a.H + i) * d + r, fmaf(wk[sq], x[0], wk[kVwBuf + sq * d + r]));
+  }
+}
+
+template <int N, int NT, typename TI, typename TO>
+cudaError_t launch_vsplit(const M2Launch &a, cudaStream_t stream) {
+  constexpr int es = sizeof(TI);
+  const int HpG = a.H / a.G;
+  const int stride = m2_verify_stride_floats(a.d, NT);
+  const size_t psm = VPrepSmem(a.L, N, a.d, HpG, NT, es).total;
+  auto prep = m2_vprep_kernel<N, NT, TI>;
+  cudaError_t e;
+  if (psm > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psm))) !=
+          cudaSuccess)
+    return e;
+  prep<<<static_cast<unsigned>(a.B) * a.G, 32 * HpG, psm, stream>>>(a, stride);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.H);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, m2_vstream_kernel<N, NT, TI, TO>, a, stride);
+}
+
+template <int N, typename TI, typename TO>
+cudaError_t launch_vsplit_t(const M2Launch &a, cudaStream_t stream) {
+  switch (gdn_window_width(a.T)) {
+    case 1: return launch_vsplit<N, 1, TI, TO>(a, stream);
+    case 4: return launch_vsplit<N, 4, TI, TO>(a, stream);
+    default: return launch_vsplit<N, 8, TI, TO>(a, stream);
+  }
+}
+
+template <typename TI, typename TO>
+cudaError_t launch_vsplit_n(const M2Launch &a, cudaStream_t stream) {
+  switch (a.n) {
+    case 32: return launch_vsplit_t<32, TI, TO>(a, stream);
+    case 64: return launch_vsplit_t<64, TI, TO>(a, stream);
+    case 128: return launch_vsplit_t<128, TI, TO>(a, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
+
+bool m2_verify_split_eligible(const M2Launch &a) {
+  if (a.T < 1 || a.T > kMaxT || (a.n != 32 && a.n != 64 && a.n != 128)) return false;
+  const int es = a.in_dtype == RSSM_BF16 ? 2 : 4;
+  const int rpp = kWarps * (128 / a.n);
+  const int HpG = a.H / a.G;
+  const int P = gdn_window_width(a.T);
+  auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (HpG > 32 || P > a.n / 4) return false;
+  const int64_t need = static_cast<int64_t>(a.B) * a.H * m2_verify_stride_floats(a.d, P) * 4;
+  return a.work != nullptr && a.work_bytes >= need && a16(a.work) && a.L % 4 == 0 && (a.d * es) % 16 == 0 &&
+         a.d % 2 == 0 && a.d <= kSPass * rpp && VPrepSmem(a.L, a.n, a.d, HpG, P, es).total <= 160u * 1024u &&
+         a16(a.S) && a16(a.ring_v) && a16(a.ring_k) && a16(a.ring_dt) && a16(a.v) && a16(a.k) && a16(a.q);
+}
+
+cudaError_t launch_m2_verify_split(const M2Launch &a, cudaStream_t stream) {
+  if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_F32) return launch_vsplit_n<bf16, float>(a, stream);
+  if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_BF16) return launch_vsplit_n<bf16, bf16>(a, stream);
+  if (a.in_dtype == RSSM_F32 && a.y_dtype == RSSM_F32) return launch_vsplit_n<float, float>(a, stream);
+  return launch_vsplit_n<float, bf16>(a, stream);
+}
 
 bool m2_decode_split_eligible(const M2Launch &a) {
   const int es = a.in_dtype == RSSM_BF16 ? 2 : 4;

@@ -54,6 +54,14 @@ bool m2_decode_pipe_eligible(const M2Launch &a);
 // kernel per (sequence, group), then a kernel streaming S_0 per (sequence, head).
 bool m2_decode_split_eligible(const M2Launch &a);
 cudaError_t launch_m2_decode_split(const M2Launch &a, bool fuse_flush, cudaStream_t stream);
+// Speculative verify through the caller's workspace (decode_split.cu): a
+// precompute kernel per (sequence, group), then a kernel streaming S_0 per
+// (sequence, head) for all T drafts.  Record per (sequence, head): a 16-float
+// header (abar_s, info), then P buffer vectors of d rows, P = 1, 4 or 8 >= T.
+constexpr int kM2VerifyHeader = 16;
+__host__ __device__ constexpr int m2_verify_stride_floats(int d, int P) { return (kM2VerifyHeader + P * d + 3) & ~3; }
+bool m2_verify_split_eligible(const M2Launch &a);
+cudaError_t launch_m2_verify_split(const M2Launch &a, cudaStream_t stream);
 // One CTA per (sequence, head) with every load issued up front (decode_flat.cu).
 bool m2_decode_flat_eligible(const M2Launch &a);
 cudaError_t launch_m2_decode_flat(const M2Launch &a, bool fuse_flush, cudaStream_t stream);

@@ -54,7 +54,7 @@ EXPORTS = (
     "gdn_state_update_baseline", "gdn_replay_decode", "gdn_replay_flush", "gdn_replay_verify",
     "gdn_spec_verify_baseline", "rssm_version", "rssm_status_string", "rssm_last_cuda_error",
     "replay_decode_workspace_bytes", "replay_decode_step_fused_noalloc",
-    "gdn_replay_decode_fused", "gdn_replay_workspace_bytes",
+    "gdn_replay_decode_fused", "gdn_replay_workspace_bytes", "replay_verify_workspace_bytes",
 )
 
 
@@ -93,6 +93,8 @@ def _load() -> ctypes.CDLL:
     lib.rssm_last_cuda_error.argtypes = []
     lib.replay_decode_workspace_bytes.restype = ctypes.c_int64
     lib.replay_decode_workspace_bytes.argtypes = [ctypes.POINTER(M2Dims)]
+    lib.replay_verify_workspace_bytes.restype = ctypes.c_int64
+    lib.replay_verify_workspace_bytes.argtypes = [ctypes.POINTER(M2Dims), ctypes.c_int32]
     lib.gdn_replay_workspace_bytes.restype = ctypes.c_int64
     lib.gdn_replay_workspace_bytes.argtypes = [ctypes.POINTER(GdnDims), ctypes.c_int32]
     return lib
@@ -169,10 +171,13 @@ class Mamba2State:
             st.add_workspace()
         return st
 
-    def add_workspace(self):
-        """Attach a decode workspace, which lets the decode step run as a
-        precompute launch plus a launch that streams S_0."""
+    def add_workspace(self, max_T: int = 0):
+        """Attach a workspace, which lets the decode step (and verify rounds of
+        up to max_T drafts) run as a precompute launch plus a launch that
+        streams S_0."""
         nbytes = decode_workspace_bytes(self.dims())
+        if max_T:
+            nbytes = max(nbytes, verify_workspace_bytes(self.dims(), max_T))
         self.work = torch.empty(nbytes // 4, dtype=torch.float32, device=self.S0.device)
         return self
 
@@ -192,8 +197,6 @@ class Mamba2State:
             _i32(getattr(self, name), name)
         if self.work is not None:
             _f32(self.work, "work")
-            if self.work.numel() * 4 < decode_workspace_bytes(self.dims()):
-                raise ValueError("work is smaller than decode_workspace_bytes()")
         ptrs = [_ptr(getattr(self, f)) for f in
                 ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag", "sync", "err", "work")]
         return M2Replay(*ptrs, 0 if self.work is None else self.work.numel() * 4)
@@ -264,6 +267,14 @@ def gdn_workspace_bytes(dims: GdnDims, max_T: int = 1) -> int:
     n = int(LIB.gdn_replay_workspace_bytes(ctypes.byref(dims), int(max_T)))
     if n <= 0:
         raise ReplaySSMError("gdn_replay_workspace_bytes: invalid arguments")
+    return n
+
+
+def verify_workspace_bytes(dims: M2Dims, max_T: int) -> int:
+    """Bytes of the optional Mamba-2 workspace for verify rounds of up to max_T drafts."""
+    n = int(LIB.replay_verify_workspace_bytes(ctypes.byref(dims), int(max_T)))
+    if n <= 0:
+        raise ReplaySSMError("replay_verify_workspace_bytes: invalid arguments")
     return n
 
 

@@ -58,7 +58,7 @@ def m2_state(init: wl.Mamba2Init, workspace: bool = True):
         flag=torch.zeros(B, dtype=torch.int32, device="cuda"), sync=torch.zeros(B, dtype=torch.int32, device="cuda"),
         err=torch.zeros(1, dtype=torch.int32, device="cuda"))
     if workspace:
-        st.add_workspace()
+        st.add_workspace(max_T=8)
         st.work.fill_(float("nan"))  # scratch: nothing may depend on its prior contents
     return st
 

@@ -201,11 +201,11 @@ def test_flush_anywhere_gpu():
         assert_close(y2, host(y1), what=f"step {t}")
 
 
-def run_spec(shape, T, rounds, seed, sample=None):
+def run_spec(shape, T, rounds, seed, sample=None, workspace=True):
     R = rs()
     init = wl.mamba2_init(shape, seed, fill_max=shape.L - T)
     idx = np.arange(shape.B) if sample is None else np.asarray(sample)
-    state = m2_state(init)
+    state = m2_state(init, workspace)
     orc = oracle_replay(init, idx)
     A = dev(init.A)
     for r in range(rounds):
@@ -224,15 +224,19 @@ def run_spec(shape, T, rounds, seed, sample=None):
     assert int(host(state.err)[0]) == 0
 
 
+@pytest.mark.parametrize("workspace", WORKSPACE)
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8])
-def test_spec_verify_parity(T):
+def test_spec_verify_parity(T, workspace):
     shape = wl.Mamba2Shape(B=12, H=8, G=2, d=64, n=128, L=16, in_dtype=wl.BF16)
-    run_spec(shape, T, rounds=12, seed=40 + T)
+    run_spec(shape, T, rounds=12, seed=40 + T, workspace=workspace)
 
 
 def test_spec_verify_small_shapes():
     run_spec(wl.Mamba2Shape(B=5, H=4, G=1, d=16, n=16, L=6, in_dtype=wl.F32), 3, rounds=10, seed=3)
     run_spec(wl.Mamba2Shape(B=5, H=6, G=3, d=36, n=32, L=9, in_dtype=wl.BF16), 4, rounds=10, seed=4)
+    # two-launch verify: fp32 inputs with n = 32, ragged heads, bf16 with n = 64 and a 12-slot ring
+    run_spec(wl.Mamba2Shape(B=4, H=6, G=3, d=20, n=32, L=8, in_dtype=wl.F32), 3, rounds=10, seed=5)
+    run_spec(wl.Mamba2Shape(B=4, H=8, G=2, d=48, n=64, L=12, in_dtype=wl.BF16), 6, rounds=10, seed=6)
 
 
 def test_spec_full_batch_sampled():
