@@ -231,12 +231,15 @@ __global__ void __launch_bounds__(kTcThreads) flush_tc_kernel(FlushLaunch a, int
         if (tid == 0) set_err(a.err, RSSM_EBIT_COUNT_RANGE);
         continue;
       }
-      if (tid == 0 && last_arrival(a.sync, b, H)) {
-        a.start[b] = (st + c) % L;
-        a.count[b] = 0;
-      }
       const size_t bh = static_cast<size_t>(b) * H + i;
       const size_t bg = static_cast<size_t>(b) * a.G + i / HpG;
+      // this thread's state column for the first kPre rows, loaded now so that
+      // the loads overlap the operand staging and the MMA
+      constexpr int kPre = 64;
+      float *S0 = a.S0 + bh * d * N;
+      float spre[kPre];
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) spre[u] = (u < d) ? __ldcs(S0 + static_cast<size_t>(u) * N + tid) : 0.f;
       if (warp == 0) {
         float ld = 0.f;
         if (lane < c) ld = a.ring_ld[bh * L + (st + lane) % L];
@@ -294,15 +297,29 @@ __global__ void __launch_bounds__(kTcThreads) flush_tc_kernel(FlushLaunch a, int
       phase ^= 1u;
       tc05::fence_after_sync();
       // epilogue: this thread owns state column tid (TMEM lane tid)
-      float *S0 = a.S0 + bh * d * N;
       const float abar = s_abar;
-      for (int r0 = 0; r0 < d; r0 += 32) {
+#pragma unroll
+      for (int r0 = 0; r0 < kPre; r0 += 32) {
+        if (r0 < d) {
+          float dv[32];
+          tc05::ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(r0), dv);
+#pragma unroll
+          for (int u = 0; u < 32; ++u)
+            __stcs(S0 + static_cast<size_t>(r0 + u) * N + tid, fmaf(abar, spre[r0 + u], dv[u]));
+        }
+      }
+      for (int r0 = kPre; r0 < d; r0 += 32) {
         float dv[32], sv[32];
         tc05::ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(r0), dv);
 #pragma unroll
         for (int u = 0; u < 32; ++u) sv[u] = __ldcs(S0 + static_cast<size_t>(r0 + u) * N + tid);
 #pragma unroll
         for (int u = 0; u < 32; ++u) __stcs(S0 + static_cast<size_t>(r0 + u) * N + tid, fmaf(abar, sv[u], dv[u]));
+      }
+      // the pointers of b are reset once every item of b has read them
+      if (tid == 0 && last_arrival(a.sync, b, H)) {
+        a.start[b] = (st + c) % L;
+        a.count[b] = 0;
       }
       tc05::fence_before_sync();
       __syncthreads();  // TMEM and the operand buffers are reused by the next item
