@@ -605,7 +605,7 @@ def _dev(x, dt=None):
     return (t.to(dt) if dt is not None else t).cuda()
 
 
-def suite_layers(R, peak):
+def suite_layers(R, peak, steps=None):
     """Layer-stack sweep: 23 independent Nemotron-H Mamba-2 layers per step,
     batch B and ring capacity L swept; fused decode step per layer.  The
     23-layer step is captured in a CUDA graph (as a serving loop would), so
@@ -709,7 +709,7 @@ def _m2_state(R, init):
                          _dev(init.start, _i32()), _dev(init.count, _i32()), z(B), z(B), z(1))
 
 
-def suite_spec(R, peak):
+def suite_spec(R, peak, steps=None):
     """Speculative verify rounds, B=512, T=4, L=16, accepted ~ U{0..4}: replay
     (verify + device commit + flush of early-flagged sequences) vs the
     snapshot baseline (T+1 state slots)."""
@@ -721,7 +721,7 @@ def suite_spec(R, peak):
     mk = lambda: _m2_state(R, init).add_workspace(max_T=T)  # noqa: E731
     A = _dev(init.A)
     y = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
-    W, K = 4, 256
+    W, K = 4, steps or 256
 
     def make_round(st):
         def rnd(i):
@@ -791,7 +791,7 @@ def _gdn_inp(st):
     return (_dev(st.q, _bf16()), _dev(st.k, _bf16()), _dev(st.v, _bf16()), _dev(st.beta), _dev(st.g))
 
 
-def suite_gdn(R, peak):
+def suite_gdn(R, peak, steps=None):
     """GDN layer (B=256, Hv=32, Hk=16, d_k=d_v=128, L=16): decode steps
     (decode + flush) vs the baseline state update, and T=4 verify rounds vs
     the snapshot baseline."""
@@ -803,7 +803,7 @@ def suite_gdn(R, peak):
     pool = [_gdn_inp(wl.gdn_step(shape, seed, t)) for t in range(P)]
     y = torch.empty(shape.B, shape.Hv, shape.dv, device="cuda")
     st = _gdn_state(R, init)
-    W, K = 4, 512
+    W, K = 4, steps or 512
 
     def step(i):
         R.gdn_replay_decode_fused(st, *pool[i % P], y=y)
@@ -841,7 +841,7 @@ def suite_gdn(R, peak):
                 "replay_over_baseline": bms / ms, "device_error_word": err})
     print(json.dumps(out[-1]), flush=True)
 
-    T, Kv = 4, 256
+    T, Kv = 4, steps or 256
     init = wl.gdn_init(shape, seed + 50, fill_max=shape.L - T)
     vpool = [_gdn_inp(wl.gdn_step(shape, seed + 50, r, T=T)) for r in range(P)]
     acc = [_dev(wl.accepted_counts(shape.B, T, seed + 50, r), _i32()) for r in range(P)]
@@ -906,7 +906,7 @@ def run_suite(args):
     peak, _ = measured_peaks()
     names = args.suite.split(",")
     for name in names:
-        {"layers": suite_layers, "spec": suite_spec, "gdn": suite_gdn}[name](R, peak)
+        {"layers": suite_layers, "spec": suite_spec, "gdn": suite_gdn}[name](R, peak, args.suite_steps)
 
 
 def main():
@@ -921,6 +921,9 @@ def main():
     ap.add_argument("--suite", default=None,
                     help="instead of the headline line, print one JSON line per measurement of the other "
                          "workloads: comma-separated subset of layers,spec,gdn")
+    ap.add_argument("--suite-steps", type=int, default=None,
+                    help="timed steps (rounds) per suite measurement instead of each suite's own count "
+                         "(short runs for profiling; the layer sweep keeps its graph of 16 steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

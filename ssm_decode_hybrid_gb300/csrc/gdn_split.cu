@@ -296,8 +296,10 @@ struct GStreamSmem {
   static constexpr size_t sx = tile + size_t(HALF) * N;             // [2NT][kSxStride] S_0 x_v
   static constexpr size_t su = sx + size_t(2 * NT) * kSxStride;     // [CHUNK] this step's u (fold)
   static constexpr size_t hdr = su + CHUNK;                         // [kGwBuf] workspace header
-  static constexpr size_t fold = hdr + kGwBuf;                      // [L][CHUNK] wu, [L][N] keys
-  static size_t bytes(bool fused, int L) { return 4 * (fold + (fused ? size_t(L) * (CHUNK + N) : 0)); }
+  static constexpr size_t fold = hdr + kGwBuf;                      // [L][CHUNK] u (TU), [L][N] keys (TI)
+  static size_t bytes(bool fused, int L, int eu, int es) {
+    return 4 * fold + (fused ? size_t(L) * (size_t(CHUNK) * eu + size_t(N) * es) : 0);
+  }
   static_assert((sx * 4) % 16 == 0 && (hdr * 4) % 16 == 0 && (fold * 4) % 16 == 0, "16-byte aligned parts");
 };
 
@@ -462,49 +464,79 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 8 ? 1 : 2)) gdn
   if constexpr (kDecode && kFuse) {
     if (info & kInfoFold) {
       // every slot holds an entry: the L - 1 committed ones and this step's.
-      // Stage wu[j][r] = W_j u_j[r] and the keys in fp32, window order j.
+      // The block's rows of the u ring and the group's keys are staged raw, in
+      // window order j, with copies issued together; this step's u (slot j = h)
+      // is taken from su.  The register half of S_0 is read again with all of
+      // its loads in flight at once (its registers were released).
+      constexpr int es = sizeof(TI), eu = sizeof(TU);
       const int rows = rows1 + rows2;
-      float *wu = ssm + SM::fold;                      // [L][CHUNK]
-      float *kf = wu + static_cast<size_t>(L) * CHUNK;  // [L][N]
-      __syncthreads();  // su complete
-      const TU *gu = static_cast<const TU *>(a.ring_u) + bh * L * dv + r_base;
-      for (int idx = tid; idx < L * CHUNK; idx += kThreads) {
-        const int j = idx / CHUNK, rl = idx - j * CHUNK;
-        const int sl = (st + j) % L;
-        float uv = 0.f;
-        if (rl < rows) uv = (j == h) ? su[rl] : load1(gu + static_cast<size_t>(sl) * dv + rl);
-        wu[idx] = shdr[kGwW + j] * uv;
+      unsigned char *ustage = reinterpret_cast<unsigned char *>(ssm + SM::fold);  // [L][CHUNK] TU
+      unsigned char *kstage = ustage + static_cast<size_t>(L) * CHUNK * eu;       // [L][N] TI
+      const unsigned char *gu =
+          reinterpret_cast<const unsigned char *>(static_cast<const TU *>(a.ring_u) + bh * L * dv + r_base);
+      const unsigned char *gk = reinterpret_cast<const unsigned char *>(static_cast<const TI *>(a.ring_k) + bk * L * N);
+      const int uc = rows * eu / 16, kc = N * es / 16;  // 16-byte chunks per slot
+      __syncthreads();  // su complete; every u of this step stored
+      for (int idx = tid; idx < L * (uc + kc); idx += kThreads) {
+        const int j = idx / (uc + kc), c = idx - j * (uc + kc);
+        const int sl = wrapL(st + j, L);
+        if (c < uc)
+          cp_async16(ustage + (static_cast<size_t>(j) * CHUNK * eu) + c * 16,
+                     gu + static_cast<size_t>(sl) * dv * eu + c * 16);
+        else
+          cp_async16(kstage + static_cast<size_t>(j) * N * es + (c - uc) * 16, gk + static_cast<size_t>(sl) * N * es + (c - uc) * 16);
       }
-      const TI *gk = static_cast<const TI *>(a.ring_k) + bk * L * N;
-      for (int idx = tid; idx < L * N / 4; idx += kThreads) {
-        const int j = idx / (N / 4), c4 = (idx - j * (N / 4)) * 4;
-        *reinterpret_cast<float4 *>(kf + j * N + c4) = load4(gk + static_cast<size_t>((st + j) % L) * N + c4);
-      }
-      __syncthreads();
+      cp_async_commit();
       const float af = shdr[kGwAbarFold];
+      float4 o[kPass];
+#pragma unroll
+      for (int p = 0; p < kPass; ++p) {
+        const int rl = row0 + p * RPP;
+        o[p] = (rl < rows1) ? ldg_stream4(S0 + static_cast<size_t>(rl) * N + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      const TU *us = reinterpret_cast<const TU *>(ustage);
+      const TI *ks = reinterpret_cast<const TI *>(kstage);
       float *S0w = a.S + (bh * dv + r_base) * N;
 #pragma unroll 1
-      for (int p = 0; p < 2 * kPass; ++p) {
-        // rows of the register half are read again (their registers were released)
-        const int rl = row0 + (p % kPass) * RPP + (p < kPass ? 0 : HALF);
-        const bool in_regs = p < kPass;
-        if (rl >= (in_regs ? rows1 : HALF + rows2)) continue;
-        float4 o = in_regs ? ldg_stream4(S0 + static_cast<size_t>(rl) * N + col)
-                           : *reinterpret_cast<const float4 *>(tile + (rl - HALF) * N + col);
-        o.x *= af;
-        o.y *= af;
-        o.z *= af;
-        o.w *= af;
-#pragma unroll 4
-        for (int j = 0; j < L; ++j) {
-          const float w = wu[j * CHUNK + rl];
-          const float4 kv = *reinterpret_cast<const float4 *>(kf + j * N + col);
-          o.x = fmaf(w, kv.x, o.x);
-          o.y = fmaf(w, kv.y, o.y);
-          o.z = fmaf(w, kv.z, o.z);
-          o.w = fmaf(w, kv.w, o.w);
+      for (int half = 0; half < 2; ++half) {
+        const int off = half * HALF;
+        const int lim = half ? rows2 : rows1;
+        if (half) {
+#pragma unroll
+          for (int p = 0; p < kPass; ++p) {
+            const int rl = row0 + p * RPP;
+            o[p] = (rl < rows2) ? *reinterpret_cast<const float4 *>(tile + rl * N + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
-        stg_stream4(S0w + static_cast<size_t>(rl) * N + col, o);
+#pragma unroll
+        for (int p = 0; p < kPass; ++p) {
+          o[p].x *= af;
+          o[p].y *= af;
+          o[p].z *= af;
+          o[p].w *= af;
+        }
+#pragma unroll 2
+        for (int j = 0; j < L; ++j) {
+          const float wj = shdr[kGwW + j];
+          const float4 kv = load4(ks + static_cast<size_t>(j) * N + col);
+#pragma unroll
+          for (int p = 0; p < kPass; ++p) {
+            const int rb2 = off + row0 + p * RPP;
+            const float uv = (j == h) ? su[rb2] : load1(us + static_cast<size_t>(j) * CHUNK + rb2);
+            const float w = wj * uv;
+            o[p].x = fmaf(w, kv.x, o[p].x);
+            o[p].y = fmaf(w, kv.y, o[p].y);
+            o[p].z = fmaf(w, kv.z, o[p].z);
+            o[p].w = fmaf(w, kv.w, o[p].w);
+          }
+        }
+#pragma unroll
+        for (int p = 0; p < kPass; ++p) {
+          const int rl = row0 + p * RPP;
+          if (rl < lim) stg_stream4(S0w + static_cast<size_t>(off + rl) * N + col, o[p]);
+        }
       }
     }
   }
@@ -527,7 +559,7 @@ cudaError_t launch_gs(const GdnLaunch &a, cudaStream_t stream) {
   prep<<<static_cast<unsigned>(a.B) * a.Hk, 32 * HpK, psm, stream>>>(a, stride);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int nrb = (a.dv + CHUNK - 1) / CHUNK;
-  const size_t ssm = GStreamSmem<N, NT>::bytes(kDecode && kFuse, a.L);
+  const size_t ssm = GStreamSmem<N, NT>::bytes(kDecode && kFuse, a.L, eu, es);
   auto strm = gdn_stream_kernel<N, NT, kDecode, kFuse, TI, TU, TO>;
   static std::atomic<size_t> configured{0};
   if (ssm > 48 * 1024 && ssm > configured.load()) {
