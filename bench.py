@@ -12,6 +12,7 @@ on the host cores instead (bounded sample of the same workload).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import multiprocessing as mp
@@ -897,6 +898,252 @@ def suite_gdn(R, peak, steps=None):
     return out
 
 
+def spec_trace(count0: np.ndarray, accs: list, T: int, L: int):
+    """Committed count h of every sequence at the start of each round of the
+    accepted-count sequence `accs`, and the number of entries the flush after
+    the round folds (-1 where it does not flush): verify flags h + 2T > L,
+    commit adds the accepted count, the flush resets flagged sequences."""
+    h = count0.astype(np.int64).copy()
+    hs, folds = [], []
+    for a in accs:
+        hs.append(h.copy())
+        flag = h + 2 * T > L
+        h = h + a.astype(np.int64)
+        folds.append(np.where(flag, h, -1))
+        h = np.where(flag, 0, h)
+    return hs, folds
+
+
+SWEEP_ROUNDS = 8  # rounds captured per CUDA graph (each with its own inputs and accepted counts)
+
+
+def suite_sweep(R, peak, steps=None):
+    """Speculative rounds against the window T = 1..6 (the shape of "Results --
+    speculative decoding", Fig. 9): each round is verify + device commit +
+    flush of the early-flagged sequences, captured in a CUDA graph with the
+    per-round accepted counts in device memory (the sampler is a stub: counts
+    drawn U{0..T} beforehand), so one graph covers every sequence's runtime
+    branch with no host synchronisation.  Against it, the snapshot baseline
+    round (T serial state updates into T + 1 slots, then the slot commit), and
+    both relative to the standard decode step of their own kind at the same
+    batch.  Mamba-2 layer at B = 512 and GDN layer at B = 256, L = 16."""
+    import torch
+
+    reps, W = (steps or 8), 2
+    K = SWEEP_ROUNDS
+    out = []
+    for model in ("mamba2", "gdn"):
+        if model == "mamba2":
+            shape = wl.SPEC_MAMBA2
+            t = wl.mamba2_state_tensors_device(shape, wl.SEED_SPEC + 7, "cuda")
+            z = lambda n: torch.zeros(n, dtype=torch.int32, device="cuda")  # noqa: E731
+            dst = R.Mamba2State(t["S0"].clone(), t["ring_v"].clone(), t["ring_k"].clone(), t["ring_dt"].clone(),
+                                t["start"].clone(), t["count"].clone(), z(shape.B), z(shape.B), z(1)).add_workspace()
+            A = t["A"]
+            dinp = [tuple(x[:, 0].contiguous() for x in wl.mamba2_round_device(shape, 50 + i, 1, "cuda"))
+                    for i in range(K)]
+            y1 = torch.empty(shape.B, shape.H, shape.d, device="cuda")
+            dec_ms = _time_graph(lambda i: R.replay_decode_step_fused(dst, *dinp[i % K], A, y=y1), K, W, reps)
+            Sb = t["S0"].clone()
+            base_dec_ms = _time_graph(lambda i: R.ssm_state_update_baseline(Sb, *dinp[i % K], A, y=y1), K, W, reps)
+            del dst, Sb
+        else:
+            shape = wl.GDN_LAYER
+            t = wl.gdn_state_tensors_device(shape, wl.SEED_GDN + 7, "cuda")
+            z = lambda n: torch.zeros(n, dtype=torch.int32, device="cuda")  # noqa: E731
+            dst = R.GdnState(t["S0"].clone(), t["ring_u"].clone(), t["ring_k"].clone(), t["ring_g"].clone(),
+                             t["start"].clone(), t["count"].clone(), z(shape.B), z(shape.B), z(1)).add_workspace(1)
+            dinp = [tuple(x[:, 0].contiguous() for x in wl.gdn_round_device(shape, 50 + i, 1, "cuda"))
+                    for i in range(K)]
+            y1 = torch.empty(shape.B, shape.Hv, shape.dv, device="cuda")
+            dec_ms = _time_graph(lambda i: R.gdn_replay_decode_fused(dst, *dinp[i % K], y=y1), K, W, reps)
+            Sb = t["S0"].clone()
+            base_dec_ms = _time_graph(lambda i: R.gdn_state_update_baseline(Sb, *dinp[i % K], y=y1), K, W, reps)
+            del dst, Sb
+        torch.cuda.empty_cache()
+        for T in range(1, 7):
+            fill = dict(fill_max=shape.L - T)
+            accs = [wl.accepted_counts_device(shape.B, T, 900 + 10 * T + i, "cuda") for i in range(K)]
+            if model == "mamba2":
+                t = wl.mamba2_state_tensors_device(shape, wl.SEED_SPEC + T, "cuda", **fill)
+                st = R.Mamba2State(t["S0"], t["ring_v"], t["ring_k"], t["ring_dt"], t["start"], t["count"],
+                                   z(shape.B), z(shape.B), z(1)).add_workspace(max_T=T)
+                inp = [wl.mamba2_round_device(shape, 100 * T + i, T, "cuda") for i in range(K)]
+                y = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
+
+                def rnd(i):
+                    R.replay_spec_verify(st, *inp[i % K], A, y=y)
+                    R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
+                    R.replay_flush(st, A)
+
+                vb = lambda h: m2_verify_bytes(shape, h, T)  # noqa: E731
+                fb = lambda c: m2_flush_bytes(shape, c)  # noqa: E731
+                snap_round_bytes = m2_snapshot_verify_bytes(shape, T) * shape.B
+                slot_shape = (shape.B, T + 1, shape.H, shape.d, shape.n)
+            else:
+                t = wl.gdn_state_tensors_device(shape, wl.SEED_GDN + T, "cuda", **fill)
+                st = R.GdnState(t["S0"], t["ring_u"], t["ring_k"], t["ring_g"], t["start"], t["count"],
+                                z(shape.B), z(shape.B), z(1)).add_workspace(T)
+                inp = [wl.gdn_round_device(shape, 100 * T + i, T, "cuda") for i in range(K)]
+                y = torch.empty(shape.B, T, shape.Hv, shape.dv, device="cuda")
+
+                def rnd(i):
+                    R.gdn_replay_verify(st, *inp[i % K], y=y)
+                    R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
+                    R.gdn_replay_flush(st)
+
+                vb = lambda h: gdn_verify_bytes(shape, h, T)  # noqa: E731
+                fb = lambda c: gdn_flush_bytes(shape, c)  # noqa: E731
+                snap_round_bytes = gdn_snapshot_verify_bytes(shape, T) * shape.B
+                slot_shape = (shape.B, T + 1, shape.Hv, shape.dv, shape.dk)
+            count0 = st.count.cpu().numpy()
+            acc_h = [a.cpu().numpy() for a in accs]
+            ms = _time_graph(rnd, K, W, reps)
+            err = int(st.err.item())
+            # rounds run: one eager, then W + reps replays of the K captured rounds; the last reps x K are timed
+            seq = [acc_h[0]] + [acc_h[i] for _ in range(W + reps) for i in range(K)]
+            hs, folds = spec_trace(count0, seq, T, shape.L)
+            per_h = {x: vb(x) for x in range(shape.L + 1)}
+            per_c = {x: fb(x) for x in range(shape.L + 1)}
+            nbytes = 0
+            for h, f in zip(hs[-reps * K:], folds[-reps * K:]):
+                nbytes += sum(per_h[int(x)] for x in h) + sum(per_c[int(x)] for x in f[f >= 0])
+            nbytes /= reps * K
+            mean_acc = float(np.mean([a.mean() for a in acc_h]))
+            del st
+            torch.cuda.empty_cache()
+            slots = torch.empty(*slot_shape, device="cuda")
+            slots[:, 0] = t["S0"]
+            del t
+            cur = torch.zeros(shape.B, dtype=torch.int32, device="cuda")
+            berr = torch.zeros(1, dtype=torch.int32, device="cuda")
+            if model == "mamba2":
+                def brnd(i):
+                    R.ssm_spec_verify_baseline(slots, cur, *inp[i % K], A, y=y, err=berr)
+                    R.ssm_spec_commit_baseline(accs[i % K], cur, T, berr)
+            else:
+                def brnd(i):
+                    R.gdn_spec_verify_baseline(slots, cur, *inp[i % K], y=y, err=berr)
+                    R.ssm_spec_commit_baseline(accs[i % K], cur, T, berr)
+            bms = _time_graph(brnd, K, W, reps)
+            err |= int(berr.item())
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            line = {"suite": "sweep", "model": model,
+                    "workload": (f"Mamba-2 layer B={shape.B}, H=32, G=8, d=64, n=128" if model == "mamba2" else
+                                 f"GDN layer B={shape.B}, Hv=32, Hk=16, d_k=d_v=128") + f", L=16, T={T}",
+                    "T": T, "rounds": reps * K, "timing": f"CUDA graph of {K} rounds (verify + commit + flush)",
+                    "ms_per_round": ms, "accepted_tokens_per_s": shape.B * mean_acc / (ms * 1e-3),
+                    "gbs": gbs, "frac_of_peak": gbs / peak,
+                    "decode_step_ms": dec_ms, "round_over_decode": ms / dec_ms,
+                    "baseline_ms_per_round": bms, "baseline_decode_step_ms": base_dec_ms,
+                    "baseline_round_over_decode": bms / base_dec_ms,
+                    "baseline_gbs": snap_round_bytes / (bms * 1e-3) / 1e9,
+                    "replay_over_baseline": bms / ms, "device_error_word": err}
+            out.append(line)
+            print(json.dumps(line), flush=True)
+            del slots, inp, y
+            torch.cuda.empty_cache()
+    return out
+
+
+CONCURRENCY_BUDGET = 8 * 2**30  # bytes of HBM per layer for decode state (a 23-layer stack in 184 GiB)
+
+
+def suite_concurrency(R, peak, steps=None):
+    """Maximum decode concurrency at a fixed HBM budget ("Results --
+    speculative decoding", Fig. 11).  The library's per-sequence accounting
+    (replay: checkpoint, ring, pointers, workspace share; snapshot baseline:
+    T + 1 states) gives the largest batch that fits CONCURRENCY_BUDGET per
+    layer for T = 0..6; then, at T = 4, one layer is allocated at each of the
+    two batches and runs speculative rounds (replay: verify + commit + flush;
+    baseline: snapshot verify + commit, CUDA graphs of 8 rounds), measuring
+    the accepted-token throughput each layout sustains within the budget."""
+    import torch
+
+    reps, W, K = (steps or 4), 2, SWEEP_ROUNDS
+    out = []
+    for model in ("mamba2", "gdn"):
+        base = wl.SPEC_MAMBA2 if model == "mamba2" else wl.GDN_LAYER
+        dims = (R.M2Dims(1, base.H, base.G, base.d, base.n, base.L, R.BF16, R.F32) if model == "mamba2" else
+                R.GdnDims(1, base.Hv, base.Hk, base.dk, base.dv, base.L, R.BF16, R.F32, R.F32))
+        rows = []
+        for T in range(0, 7):
+            rb, sb = R.seq_bytes(dims, T, R.SEQ_REPLAY), R.seq_bytes(dims, T, R.SEQ_SNAPSHOT)
+            rows.append({"T": T, "replay_bytes_per_seq": rb, "snapshot_bytes_per_seq": sb,
+                         "replay_max_batch": CONCURRENCY_BUDGET // rb, "snapshot_max_batch": CONCURRENCY_BUDGET // sb,
+                         "ratio": (CONCURRENCY_BUDGET // rb) / (CONCURRENCY_BUDGET // sb)})
+        T = 4
+        Br, Bs = rows[T]["replay_max_batch"], rows[T]["snapshot_max_batch"]
+        z = lambda n: torch.zeros(n, dtype=torch.int32, device="cuda")  # noqa: E731
+        tput = {}
+        for kind, Bk in (("replay", Br), ("snapshot", Bs)):
+            shape = dataclasses.replace(base, B=int(Bk))
+            accs = [wl.accepted_counts_device(shape.B, T, 700 + i, "cuda") for i in range(K)]
+            if model == "mamba2":
+                t = wl.mamba2_state_tensors_device(shape, 77, "cuda", fill_max=shape.L - T)
+                inp = [wl.mamba2_round_device(shape, 300 + i, T, "cuda") for i in range(K)]
+                y = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
+                A = t["A"]
+            else:
+                t = wl.gdn_state_tensors_device(shape, 77, "cuda", fill_max=shape.L - T)
+                inp = [wl.gdn_round_device(shape, 300 + i, T, "cuda") for i in range(K)]
+                y = torch.empty(shape.B, T, shape.Hv, shape.dv, device="cuda")
+            err = z(1)
+            if kind == "replay":
+                if model == "mamba2":
+                    st = R.Mamba2State(t["S0"], t["ring_v"], t["ring_k"], t["ring_dt"], t["start"], t["count"],
+                                       z(shape.B), z(shape.B), err).add_workspace(max_T=T)
+
+                    def rnd(i):
+                        R.replay_spec_verify(st, *inp[i % K], A, y=y)
+                        R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
+                        R.replay_flush(st, A)
+                else:
+                    st = R.GdnState(t["S0"], t["ring_u"], t["ring_k"], t["ring_g"], t["start"], t["count"],
+                                    z(shape.B), z(shape.B), err).add_workspace(T)
+
+                    def rnd(i):
+                        R.gdn_replay_verify(st, *inp[i % K], y=y)
+                        R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
+                        R.gdn_replay_flush(st)
+                held = sum(x.numel() * x.element_size() for x in
+                           (st.S0, st.ring_v if model == "mamba2" else st.ring_u, st.ring_k,
+                            st.ring_dt if model == "mamba2" else st.ring_g, st.start, st.count, st.flag, st.sync,
+                            st.work))
+            else:
+                S0 = t["S0"]
+                del t
+                slots = torch.empty(shape.B, T + 1, *S0.shape[1:], device="cuda")
+                slots[:, 0] = S0
+                del S0
+                cur = z(shape.B)
+                if model == "mamba2":
+                    def rnd(i):
+                        R.ssm_spec_verify_baseline(slots, cur, *inp[i % K], A, y=y, err=err)
+                        R.ssm_spec_commit_baseline(accs[i % K], cur, T, err)
+                else:
+                    def rnd(i):
+                        R.gdn_spec_verify_baseline(slots, cur, *inp[i % K], y=y, err=err)
+                        R.ssm_spec_commit_baseline(accs[i % K], cur, T, err)
+                held = slots.numel() * 4 + cur.numel() * 4
+            ms = _time_graph(rnd, K, W, reps)
+            mean_acc = float(np.mean([a.float().mean().item() for a in accs]))
+            tput[kind] = {"batch": int(Bk), "held_bytes": int(held), "ms_per_round": ms,
+                          "accepted_tokens_per_s": shape.B * mean_acc / (ms * 1e-3),
+                          "device_error_word": int(err.item())}
+            st = slots = t = inp = y = accs = None  # release this layout before allocating the next
+            torch.cuda.empty_cache()
+        line = {"suite": "concurrency", "model": model,
+                "workload": ("Mamba-2 layer H=32, G=8, d=64, n=128" if model == "mamba2" else
+                             "GDN layer Hv=32, Hk=16, d_k=d_v=128") + ", L=16",
+                "budget_bytes_per_layer": CONCURRENCY_BUDGET, "per_T": rows, "measured_T": T,
+                "at_max_batch": tput,
+                "throughput_ratio": tput["replay"]["accepted_tokens_per_s"] / tput["snapshot"]["accepted_tokens_per_s"]}
+        out.append(line)
+        print(json.dumps(line), flush=True)
+    return out
+
+
 def run_suite(args):
     import torch
 
@@ -906,7 +1153,8 @@ def run_suite(args):
     peak, _ = measured_peaks()
     names = args.suite.split(",")
     for name in names:
-        {"layers": suite_layers, "spec": suite_spec, "gdn": suite_gdn}[name](R, peak, args.suite_steps)
+        {"layers": suite_layers, "spec": suite_spec, "gdn": suite_gdn, "sweep": suite_sweep,
+         "concurrency": suite_concurrency}[name](R, peak, args.suite_steps)
 
 
 def main():
@@ -920,7 +1168,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", default=None,
                     help="instead of the headline line, print one JSON line per measurement of the other "
-                         "workloads: comma-separated subset of layers,spec,gdn")
+                         "workloads: comma-separated subset of layers,spec,gdn,sweep,concurrency")
     ap.add_argument("--suite-steps", type=int, default=None,
                     help="timed steps (rounds) per suite measurement instead of each suite's own count "
                          "(short runs for profiling; the layer sweep keeps its graph of 16 steps)")

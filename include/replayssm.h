@@ -87,6 +87,10 @@ typedef int32_t rssm_status;
 #define RSSM_EBIT_CUR 8         /* snapshot slot index outside [0, T]              */
 #define RSSM_EBIT_TIMEOUT 16    /* a bounded wait inside a pipelined kernel ran out */
 
+/* kinds of replay_seq_bytes / gdn_replay_seq_bytes */
+#define RSSM_SEQ_REPLAY 0   /* checkpoint S_0, ring buffer, pointers, workspace share */
+#define RSSM_SEQ_SNAPSHOT 1 /* the baseline: T + 1 full state slots and a slot index  */
+
 typedef struct {
   int32_t B, H, G, d, n, L;
   int32_t in_dtype; /* dtype of v, k, q and of ring_v, ring_k */
@@ -166,6 +170,22 @@ RSSM_API int64_t replay_decode_workspace_bytes(const rssm_m2_dims *dims);
  * B * H * 4 * ceil((16 + P d) / 4) with P = 1 for T = 1, 4 for T <= 4, 8 for
  * T <= 8.  0 for invalid arguments.  Host only.                               */
 RSSM_API int64_t replay_verify_workspace_bytes(const rssm_m2_dims *dims, int32_t T);
+
+/* Device bytes that one sequence holds per Mamba-2 layer, for the accounting
+ * of "Results -- speculative decoding" (maximum decode concurrency at a fixed
+ * HBM budget, Fig. 11): the budget divided by layers x this figure is the
+ * largest batch that fits.
+ *   kind RSSM_SEQ_REPLAY: S_0 (4 H d n), the v/k/Delta rings
+ *     (L (H d + G n) elements + 4 H L), the four int32 words start, count,
+ *     flag, sync, and this sequence's share of the workspace: the larger of
+ *     the decode and the verify workspace for window T >= 1, the decode
+ *     workspace for T = 0.
+ *   kind RSSM_SEQ_SNAPSHOT: the baseline, (T + 1) state slots of 4 H d n
+ *     bytes and the int32 slot index for T >= 1; one state for T = 0.
+ * Buffers shared by the whole batch (the error word) are not counted.
+ * 0 for invalid arguments (dims as replay_decode_step, 0 <= T <= 8, kind one
+ * of the two).  Host only; launches nothing.                                 */
+RSSM_API int64_t replay_seq_bytes(const rssm_m2_dims *dims, int32_t T, int32_t kind);
 
 /* Flush ("Algorithm -- Mamba-2 standard decode", flush): for every sequence
  * with flag[b] != 0 and c = count[b] committed entries,
@@ -284,6 +304,14 @@ RSSM_API rssm_status gdn_replay_decode_fused(const rssm_gdn_dims *dims, const rs
  * with P = 1 for T = 1, 4 for T <= 4, 8 for T <= 8.  0 for invalid
  * arguments.  Host only.                                                      */
 RSSM_API int64_t gdn_replay_workspace_bytes(const rssm_gdn_dims *dims, int32_t T);
+
+/* The same accounting for a GDN layer: RSSM_SEQ_REPLAY counts S_0
+ * (4 Hv dv dk), the u/k/g rings (L (Hv dv of u_dtype + Hk dk of in_dtype)
+ * + 4 Hv L), the four int32 pointer words and this sequence's share of
+ * gdn_replay_workspace_bytes for max(T, 1); RSSM_SEQ_SNAPSHOT counts T + 1
+ * state slots and the slot index (one state for T = 0).  0 for invalid
+ * arguments.  Host only.                                                     */
+RSSM_API int64_t gdn_replay_seq_bytes(const rssm_gdn_dims *dims, int32_t T, int32_t kind);
 
 /* GDN flush: S_0 <- (prod alpha_j) S_0 + sum_j (prod_{i>j} alpha_i) u_j k_j^T
  * over the committed entries of flagged sequences; pointer reset as the Mamba-2

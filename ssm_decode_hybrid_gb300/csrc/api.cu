@@ -2,6 +2,7 @@
 // one kernel launch on the caller's stream.  Nothing here allocates memory or
 // synchronises.
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -127,6 +128,34 @@ int64_t replay_decode_workspace_bytes(const rssm_m2_dims *dims) {
 int64_t replay_verify_workspace_bytes(const rssm_m2_dims *dims, int32_t T) {
   if (check_m2_dims(dims) != RSSM_OK || T < 1 || T > kMaxT) return 0;
   return static_cast<int64_t>(dims->B) * dims->H * m2_verify_stride_floats(dims->d, gdn_window_width(T)) * 4;
+}
+
+// Device bytes one sequence holds per layer, for the concurrency accounting of
+// "Results -- speculative decoding" (maximum concurrency at a fixed HBM budget).
+int64_t replay_seq_bytes(const rssm_m2_dims *dims, int32_t T, int32_t kind) {
+  if (check_m2_dims(dims) != RSSM_OK || T < 0 || T > kMaxT) return 0;
+  const rssm_m2_dims &d = *dims;
+  const int64_t es = d.in_dtype == RSSM_BF16 ? 2 : 4;
+  const int64_t state = 4ll * d.H * d.d * d.n;
+  if (kind == RSSM_SEQ_SNAPSHOT) return T == 0 ? state : (T + 1) * state + 4;
+  if (kind != RSSM_SEQ_REPLAY) return 0;
+  const int64_t ring = static_cast<int64_t>(d.L) * (d.H * d.d * es + d.G * d.n * es + 4ll * d.H);
+  int64_t stride = work_stride_floats(d.d, d.L);
+  if (T > 0) stride = std::max<int64_t>(stride, m2_verify_stride_floats(d.d, gdn_window_width(T)));
+  const int64_t work = 4ll * d.H * stride;
+  return state + ring + 4 * 4 + work;
+}
+
+int64_t gdn_replay_seq_bytes(const rssm_gdn_dims *dims, int32_t T, int32_t kind) {
+  if (check_gdn_dims(dims) != RSSM_OK || T < 0 || T > kMaxT) return 0;
+  const rssm_gdn_dims &d = *dims;
+  const int64_t es = d.in_dtype == RSSM_BF16 ? 2 : 4, eu = d.u_dtype == RSSM_BF16 ? 2 : 4;
+  const int64_t state = 4ll * d.Hv * d.dv * d.dk;
+  if (kind == RSSM_SEQ_SNAPSHOT) return T == 0 ? state : (T + 1) * state + 4;
+  if (kind != RSSM_SEQ_REPLAY) return 0;
+  const int64_t ring = static_cast<int64_t>(d.L) * (d.Hv * d.dv * eu + d.Hk * d.dk * es + 4ll * d.Hv);
+  const int64_t work = 4ll * d.Hv * gdn_work_stride_floats(d.dv, gdn_window_width(T < 1 ? 1 : T));
+  return state + ring + 4 * 4 + work;
 }
 
 rssm_status ssm_state_update_baseline(const rssm_m2_dims *dims, float *S, const void *v, const void *k,

@@ -19,6 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("REPLAYSSM_LIB") or os.path.join(_HERE, "libreplayssm.so")
 
 F32, BF16 = 0, 1
+SEQ_REPLAY, SEQ_SNAPSHOT = 0, 1
 EBIT_COUNT_RANGE, EBIT_WINDOW, EBIT_ACCEPTED, EBIT_CUR = 1, 2, 4, 8
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -55,6 +56,7 @@ EXPORTS = (
     "gdn_spec_verify_baseline", "rssm_version", "rssm_status_string", "rssm_last_cuda_error",
     "replay_decode_workspace_bytes", "replay_decode_step_fused_noalloc",
     "gdn_replay_decode_fused", "gdn_replay_workspace_bytes", "replay_verify_workspace_bytes",
+    "replay_seq_bytes", "gdn_replay_seq_bytes",
 )
 
 
@@ -97,6 +99,10 @@ def _load() -> ctypes.CDLL:
     lib.replay_verify_workspace_bytes.argtypes = [ctypes.POINTER(M2Dims), ctypes.c_int32]
     lib.gdn_replay_workspace_bytes.restype = ctypes.c_int64
     lib.gdn_replay_workspace_bytes.argtypes = [ctypes.POINTER(GdnDims), ctypes.c_int32]
+    lib.replay_seq_bytes.restype = ctypes.c_int64
+    lib.replay_seq_bytes.argtypes = [ctypes.POINTER(M2Dims), ctypes.c_int32, ctypes.c_int32]
+    lib.gdn_replay_seq_bytes.restype = ctypes.c_int64
+    lib.gdn_replay_seq_bytes.argtypes = [ctypes.POINTER(GdnDims), ctypes.c_int32, ctypes.c_int32]
     return lib
 
 
@@ -284,6 +290,22 @@ def decode_workspace_bytes(dims: M2Dims) -> int:
     if n <= 0:
         raise ReplaySSMError("replay_decode_workspace_bytes: invalid dims")
     return n
+
+
+def seq_bytes(dims, T: int, kind: int) -> int:
+    """Device bytes one sequence holds per layer (replay_seq_bytes or
+    gdn_replay_seq_bytes, chosen by the type of dims); kind SEQ_REPLAY or
+    SEQ_SNAPSHOT, T the speculative window (0: standard decode)."""
+    fn = LIB.gdn_replay_seq_bytes if isinstance(dims, GdnDims) else LIB.replay_seq_bytes
+    n = int(fn(ctypes.byref(dims), int(T), int(kind)))
+    if n <= 0:
+        raise ReplaySSMError("seq_bytes: invalid arguments")
+    return n
+
+
+def max_sequences(budget_bytes: int, dims, T: int, kind: int, layers: int = 1) -> int:
+    """Largest batch whose per-sequence state for `layers` layers fits in budget_bytes."""
+    return int(budget_bytes) // (int(layers) * seq_bytes(dims, T, kind))
 
 
 def _out(y, shape, dtype, device):

@@ -247,3 +247,76 @@ def mamba2_state_tensors_device(shape: Mamba2Shape, seed: int, device, fill_max:
         "start": torch.randint(0, s.L, (s.B,), generator=g, device=device, dtype=torch.int32),
         "count": torch.randint(0, fm + 1, (s.B,), generator=g, device=device, dtype=torch.int32),
     }
+
+
+def gdn_state_tensors_device(shape: GdnShape, seed: int, device, fill_max: int | None = None):
+    """S_0, ring buffer and pointers of one GDN layer drawn on the device, from
+    the same distributions as gdn_init.  Returns a dict keyed like GdnInit."""
+    import torch
+
+    s = shape
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if s.in_dtype == BF16 else torch.float32
+    ut = torch.bfloat16 if s.u_dtype == BF16 else torch.float32
+    fm = s.L - 1 if fill_max is None else fill_max
+
+    def normal(*size):
+        return torch.randn(*size, generator=g, device=device, dtype=torch.float32)
+
+    k = normal(s.B, s.Hk, s.L, s.dk)
+    return {
+        "S0": 0.1 * normal(s.B, s.Hv, s.dv, s.dk),
+        "ring_u": (0.5 * normal(s.B, s.Hv, s.L, s.dv)).to(ut),
+        "ring_k": (k / k.norm(dim=-1, keepdim=True)).to(dt),
+        "ring_g": -torch.nn.functional.softplus(normal(s.B, s.Hv, s.L)),
+        "start": torch.randint(0, s.L, (s.B,), generator=g, device=device, dtype=torch.int32),
+        "count": torch.randint(0, fm + 1, (s.B,), generator=g, device=device, dtype=torch.int32),
+    }
+
+
+def mamba2_round_device(shape: Mamba2Shape, seed: int, T: int, device):
+    """Inputs (v, k, q, dt) of one T-draft verify round drawn on the device,
+    distributed as mamba2_step's."""
+    import torch
+
+    s = shape
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if s.in_dtype == BF16 else torch.float32
+
+    def normal(*size):
+        return torch.randn(*size, generator=g, device=device, dtype=torch.float32)
+
+    return (normal(s.B, T, s.H, s.d).to(dt), normal(s.B, T, s.G, s.n).to(dt), normal(s.B, T, s.G, s.n).to(dt),
+            torch.nn.functional.softplus(normal(s.B, T, s.H)))
+
+
+def gdn_round_device(shape: GdnShape, seed: int, T: int, device):
+    """Inputs (q, k, v, beta, g) of one T-draft GDN verify round drawn on the
+    device, distributed as gdn_step's."""
+    import torch
+
+    s = shape
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    dt = torch.bfloat16 if s.in_dtype == BF16 else torch.float32
+
+    def normal(*size):
+        return torch.randn(*size, generator=gen, device=device, dtype=torch.float32)
+
+    def unit(x):
+        return x / x.norm(dim=-1, keepdim=True)
+
+    return (unit(normal(s.B, T, s.Hk, s.dk)).to(dt), unit(normal(s.B, T, s.Hk, s.dk)).to(dt),
+            normal(s.B, T, s.Hv, s.dv).to(dt), torch.sigmoid(normal(s.B, T, s.Hv)),
+            -torch.nn.functional.softplus(normal(s.B, T, s.Hv)))
+
+
+def accepted_counts_device(B: int, T: int, seed: int, device):
+    """Accepted draft counts U{0..T} for one round, drawn on the device."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randint(0, T + 1, (B,), generator=g, device=device, dtype=torch.int32)
