@@ -120,14 +120,23 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def source_digest() -> str:
+HEADLINE_SOURCES = ("decode_split.cu", "common.cuh", "kernels.cuh")  # the headline kernels and their headers
+# the capture the recorded DRAM traffic comes from (run after the same command without ncu exited 0)
+TRAFFIC_COMMAND = ("python bench.py --no-cpu-baseline --steps 64 --warmup 8 --e2e-steps 16 && "
+                   "ncu --set full --import-source no --clock-control none -k regex:\"m2_(prep|stream)_kernel\" -s 8 -c 2 "
+                   "-o prof python bench.py --no-cpu-baseline --steps 64 --warmup 8 --e2e-steps 16")
+
+
+def source_digest(names=None) -> str:
+    """Digest of the named sources under csrc/ (default: every .cu/.cuh file)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ssm_decode_hybrid_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    if names is None:
+        names = [n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh"))]
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -143,7 +152,7 @@ def recorded_traffic(*kernels: str):
         return None
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("source_digest") != source_digest():
+    if rec.get("source_digest") != source_digest(rec.get("sources")):
         return None
     total = 0.0
     for kernel in kernels:
@@ -1144,6 +1153,45 @@ def suite_concurrency(R, peak, steps=None):
     return out
 
 
+def record_traffic(report: str, command: str):
+    """Write profiles/ncu_traffic.json from an ncu report of the headline
+    command (read with `ncu -i`, no GPU needed): DRAM bytes and duration of
+    the first captured launch of each fused decode kernel, with the digest of
+    the sources that define them."""
+    import csv
+    import io
+
+    out = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], capture_output=True, text=True, check=True)
+    rows = list(csv.reader(io.StringIO(out.stdout)))
+    head, units = rows[0], rows[1]
+    col = {n: i for i, n in enumerate(head)}
+
+    def val(r, name):
+        v = float(r[col[name]].replace(",", ""))
+        u = units[col[name]]
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "nsecond": 1e-3, "usecond": 1, "msecond": 1e3}
+        return v * scale.get(u, 1)
+
+    kernels = {}
+    for r in rows[2:]:
+        name = r[col["Kernel Name"]]
+        for key, pat in (("m2_prep_kernel<fused>", "m2_prep_kernel<128, 1,"),
+                         ("m2_stream_kernel<fused>", "m2_stream_kernel<128, 1,")):
+            if pat in name and key not in kernels:
+                rd, wr = val(r, "dram__bytes_read.sum"), val(r, "dram__bytes_write.sum")
+                short = name[name.index(pat.split("<")[0]):].split("(")[0]
+                kernels[key] = {"kernel": short.replace("__nv_bfloat16", "bf16"),
+                                "dram_bytes_per_launch": rd + wr, "dram_read": rd, "dram_write": wr,
+                                "duration_us": val(r, "gpu__time_duration.sum")}
+    rec = {"source_digest": source_digest(HEADLINE_SOURCES), "sources": list(HEADLINE_SOURCES), "command": command,
+           "kernels": kernels}
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    with open(path, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    print(json.dumps(rec, indent=1))
+
+
 def run_suite(args):
     import torch
 
@@ -1172,7 +1220,12 @@ def main():
     ap.add_argument("--suite-steps", type=int, default=None,
                     help="timed steps (rounds) per suite measurement instead of each suite's own count "
                          "(short runs for profiling; the layer sweep keeps its graph of 16 steps)")
+    ap.add_argument("--record-traffic", default=None, metavar="REPORT",
+                    help="write profiles/ncu_traffic.json from an ncu report of the headline command and exit")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(args.record_traffic, TRAFFIC_COMMAND)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.suite:

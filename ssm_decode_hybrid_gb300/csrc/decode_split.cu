@@ -613,6 +613,7 @@ cudaError_t launch_vsplit(const M2Launch &a, cudaStream_t stream) {
     return e;
   prep<<<static_cast<unsigned>(a.B) * a.G, 32 * HpG, psm, stream>>>(a, stride);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (m2_verify_tc_eligible(a)) return launch_m2_verify_tc(a, stride, stream);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.H);
   cfg.blockDim = dim3(kThreads);

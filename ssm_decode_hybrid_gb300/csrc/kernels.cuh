@@ -62,6 +62,10 @@ constexpr int kM2VerifyHeader = 16;
 __host__ __device__ constexpr int m2_verify_stride_floats(int d, int P) { return (kM2VerifyHeader + P * d + 3) & ~3; }
 bool m2_verify_split_eligible(const M2Launch &a);
 cudaError_t launch_m2_verify_split(const M2Launch &a, cudaStream_t stream);
+// Its streaming half on the tensor cores (verify_tc.cu): n = 128, d = 64,
+// two heads of a group per block, bf16 inputs, T >= 5.
+bool m2_verify_tc_eligible(const M2Launch &a);
+cudaError_t launch_m2_verify_tc(const M2Launch &a, int stride, cudaStream_t stream);
 // One CTA per (sequence, head) with every load issued up front (decode_flat.cu).
 bool m2_decode_flat_eligible(const M2Launch &a);
 cudaError_t launch_m2_decode_flat(const M2Launch &a, bool fuse_flush, cudaStream_t stream);
@@ -106,6 +110,11 @@ __host__ __device__ constexpr int gdn_work_stride_floats(int dv, int P) {
 // value head, row block).  kind: Decode, DecodeFused or Verify.
 bool gdn_split_eligible(GdnKind kind, const GdnLaunch &a);
 cudaError_t launch_gdn_split(GdnKind kind, const GdnLaunch &a, cudaStream_t stream);
+// The streaming half of the two-launch GDN verify on the tensor cores
+// (verify_tc.cu): dk = dv = 128, bf16 inputs; reads the records the
+// precompute kernel left for window width P.
+bool gdn_verify_tc_eligible(const GdnLaunch &a);
+cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, cudaStream_t stream);
 
 cudaError_t launch_gdn(GdnKind kind, const GdnLaunch &a, cudaStream_t stream);
 

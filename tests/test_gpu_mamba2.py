@@ -201,7 +201,7 @@ def test_flush_anywhere_gpu():
         assert_close(y2, host(y1), what=f"step {t}")
 
 
-def run_spec(shape, T, rounds, seed, sample=None, workspace=True):
+def run_spec(shape, T, rounds, seed, sample=None, workspace=True, y_dtype=torch.float32):
     R = rs()
     init = wl.mamba2_init(shape, seed, fill_max=shape.L - T)
     idx = np.arange(shape.B) if sample is None else np.asarray(sample)
@@ -211,10 +211,10 @@ def run_spec(shape, T, rounds, seed, sample=None, workspace=True):
     for r in range(rounds):
         st = wl.mamba2_step(shape, seed, r, T=T)
         acc = wl.accepted_counts(shape.B, T, seed, r)
-        y = R.replay_spec_verify(state, *m2_step_dev(st, shape.in_dtype), A)
+        y = R.replay_spec_verify(state, *m2_step_dev(st, shape.in_dtype), A, y_dtype=y_dtype)
         Y_ref = orc.spec_verify(take(st.v, idx), take(st.k, idx), take(st.q, idx), take(st.dt, idx))
         np.testing.assert_array_equal(host(state.flag)[idx], orc.flag, err_msg=f"round {r}: flag")
-        assert_close(y[idx], Y_ref, what=f"round {r}: y")
+        assert_close(y[idx], Y_ref, *tol_for(y_dtype), what=f"round {r}: y")
         R.replay_spec_commit(dev(acc, torch.int32), state.count, T, shape.L, state.err)
         orc.commit(take(acc, idx), T)
         R.replay_flush(state, A)
@@ -237,6 +237,15 @@ def test_spec_verify_small_shapes():
     # two-launch verify: fp32 inputs with n = 32, ragged heads, bf16 with n = 64 and a 12-slot ring
     run_spec(wl.Mamba2Shape(B=4, H=6, G=3, d=20, n=32, L=8, in_dtype=wl.F32), 3, rounds=10, seed=5)
     run_spec(wl.Mamba2Shape(B=4, H=8, G=2, d=48, n=64, L=12, in_dtype=wl.BF16), 6, rounds=10, seed=6)
+
+
+@pytest.mark.parametrize("T", [3, 7])
+def test_spec_verify_bf16_out_tensor_core(T):
+    """bf16 outputs, eight heads per group; n = 128, d = 64 with T >= 5 takes
+    the tensor-core stream (two heads of a group per block), T = 3 the CUDA
+    cores."""
+    shape = wl.Mamba2Shape(B=6, H=16, G=2, d=64, n=128, L=16, in_dtype=wl.BF16)
+    run_spec(shape, T, rounds=8, seed=80 + T, y_dtype=torch.bfloat16)
 
 
 def test_spec_full_batch_sampled():
