@@ -9,8 +9,9 @@ two share only the seeded input generators, which hold no arithmetic of the
 method.
 
 Source of truth: the web page "ReplaySSM: Cache SSM Inputs, Not State"
-(papercache summary of Tri Dao's blog post).  Each function names the section
-and equation it follows.  Everything is computed in float64 with numpy, as
+(papercache summary of Tri Dao's blog post); for the convolution state that
+precedes the SSM (``conv.py``), the state layout of "Disaggregated Serving for
+Hybrid SSM Models".  Each function names the section and equation it follows.  Everything is computed in float64 with numpy, as
 plainly as the equations are written; loops over sequences and buffer entries
 are explicit.
 
