@@ -1153,6 +1153,51 @@ def suite_concurrency(R, peak, steps=None):
     return out
 
 
+def suite_conv(R, peak, steps=None):
+    """Convolution-state step of the Nemotron-H layer (x 32 x 64, B and C
+    8 x 128, W = 4, bf16) at batch 256, alone and followed by the fused decode
+    step it feeds (the layer's decode path from the in-projection's columns to
+    y).  The state and inputs (about 17 MB) stay in L2 between steps, so the
+    step's GB/s is an L2 figure; the decode step is not."""
+    import torch
+
+    K, W, P = steps or 1024, 16, 8
+    ms = wl.NEMOTRON_H_MAMBA2
+    cs = wl.ConvShape(B=ms.B, dx=ms.H * ms.d, dbc=ms.G * ms.n, W=4, io_dtype=wl.BF16)
+    cinit = wl.conv_init(cs, wl.SEED_NEMOTRON + 30)
+    state = _dev(cinit.state, _bf16())
+    weight, bias = _dev(cinit.weight), _dev(cinit.bias)
+    us = [_dev(wl.conv_input(cs, wl.SEED_NEMOTRON + 30, t), _bf16()) for t in range(P)]
+    outs = tuple(torch.empty(ms.B, n, dtype=torch.bfloat16, device="cuda") for n in (cs.dx, cs.dbc, cs.dbc))
+    conv_ms = _time_loop(lambda i: R.conv_state_update(state, us[i % P], weight, bias, cs.dx, cs.dbc, out=outs), K, W)
+    C = cs.dx + 2 * cs.dbc
+    conv_bytes = ms.B * C * (2 * 2 * (cs.W - 1) + 2 + 2) + C * (cs.W + 1) * 4
+    init = wl.mamba2_init(ms, wl.SEED_NEMOTRON + 31)
+    st = _m2_state(R, init).add_workspace()
+    A = _dev(init.A)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(wl.SEED_NEMOTRON + 32)
+    dts = [torch.nn.functional.softplus(torch.randn(ms.B, ms.H, generator=g, device="cuda")) for _ in range(P)]
+    y = torch.empty(ms.B, ms.H, ms.d, device="cuda")
+    v, k, q = outs[0].view(ms.B, ms.H, ms.d), outs[1].view(ms.B, ms.G, ms.n), outs[2].view(ms.B, ms.G, ms.n)
+
+    def layer(i):
+        R.conv_state_update(state, us[i % P], weight, bias, cs.dx, cs.dbc, out=outs)
+        R.replay_decode_step_fused(st, v, k, q, dts[i % P], A, y=y)
+
+    pair_ms = _time_loop(layer, K, W)
+    dec_ms = _time_loop(lambda i: R.replay_decode_step_fused(st, v, k, q, dts[i % P], A, y=y), K, W)
+    line = {"suite": "conv", "workload": "Nemotron-H convolution state B=256, x 2048 + B 1024 + C 1024 channels, "
+                                         "W=4, bf16; then the fused decode step",
+            "steps": K, "conv_ms_per_step": conv_ms, "conv_bytes_per_step": conv_bytes,
+            "conv_gbs": conv_bytes / (conv_ms * 1e-3) / 1e9, "conv_state_fits_l2": True,
+            "conv_plus_decode_ms_per_step": pair_ms, "decode_ms_per_step": dec_ms,
+            "conv_share": (pair_ms - dec_ms) / pair_ms,
+            "device_error_word": int(st.err.item())}
+    print(json.dumps(line), flush=True)
+    return [line]
+
+
 def record_traffic(report: str, command: str):
     """Write profiles/ncu_traffic.json from an ncu report of the headline
     command (read with `ncu -i`, no GPU needed): DRAM bytes and duration of
@@ -1202,7 +1247,7 @@ def run_suite(args):
     names = args.suite.split(",")
     for name in names:
         {"layers": suite_layers, "spec": suite_spec, "gdn": suite_gdn, "sweep": suite_sweep,
-         "concurrency": suite_concurrency}[name](R, peak, args.suite_steps)
+         "concurrency": suite_concurrency, "conv": suite_conv}[name](R, peak, args.suite_steps)
 
 
 def main():
@@ -1216,7 +1261,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", default=None,
                     help="instead of the headline line, print one JSON line per measurement of the other "
-                         "workloads: comma-separated subset of layers,spec,gdn,sweep,concurrency")
+                         "workloads: comma-separated subset of layers,spec,gdn,sweep,concurrency,conv")
     ap.add_argument("--suite-steps", type=int, default=None,
                     help="timed steps (rounds) per suite measurement instead of each suite's own count "
                          "(short runs for profiling; the layer sweep keeps its graph of 16 steps)")

@@ -341,6 +341,41 @@ RSSM_API rssm_status gdn_spec_verify_baseline(const rssm_gdn_dims *dims, int32_t
                                      const float *g, void *y, int32_t *err, rssm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Convolution state: the step before the SSM in a Mamba-2 layer             */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  int32_t B;        /* sequences */
+  int32_t dx;       /* channels of the x sub-projection (H d: the SSM's v) */
+  int32_t dbc;      /* channels of each of B and C (G n: the SSM's k and q) */
+  int32_t W;        /* convolution width, 2..8; the state keeps W - 1 columns */
+  int32_t io_dtype; /* dtype of state, u and the outputs: RSSM_BF16 or RSSM_F32 */
+  int32_t silu;     /* 1: SiLU on the outputs, 0: none */
+} rssm_conv_dims;
+
+/* Decode step of the convolution state ("Disaggregated Serving for Hybrid
+ * SSM Models", Mamba state layout: a per-sequence state of shape (conv_dim,
+ * state_len) in the DS layout, conv_dim = dx + 2 dbc, state_len = W - 1; the
+ * arithmetic is not on the pages -- this library reads it as the causal
+ * depthwise convolution of width W).  Per sequence b and channel c, with
+ * the state's columns oldest first and the new input u:
+ *   z = bias[c] + sum_{w<W-1} weight[c][w] state[b][c][w] + weight[c][W-1] u[b][c]
+ *   out = silu(z) = z / (1 + exp(-z))  (or z),  state[b][c] <- (state[b][c][1..], u[b][c])
+ * in fp32; out is rounded to io_dtype and split by channel into x, B, C.
+ *   state  io_dtype [B][dx + 2 dbc][W - 1]   (in/out, DS layout)
+ *   u      io_dtype [B][dx + 2 dbc]          (the in-projection's x|B|C columns)
+ *   weight float [dx + 2 dbc][W]   bias float [dx + 2 dbc] or NULL
+ *   out_x  io_dtype [B][dx]   out_b, out_c io_dtype [B][dbc]  (NULL if dbc = 0)
+ * The outputs have the layouts of replay_decode_step's v (H = dx / d heads)
+ * and k, q (G = dbc / n groups).  The caller owns all memory; pointers are
+ * device pointers aligned to their element size.  RSSM_ERR_INVALID_ARG for
+ * null or misaligned pointers or dims out of range (B, dx >= 1, dbc >= 0,
+ * 2 <= W <= 8, silu 0 or 1).                                                 */
+RSSM_API rssm_status conv_state_update(const rssm_conv_dims *dims, void *state, const void *u, const float *weight,
+                                       const float *bias, void *out_x, void *out_b, void *out_c,
+                                       rssm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Utilities                                                                  */
 /* ------------------------------------------------------------------------ */
 

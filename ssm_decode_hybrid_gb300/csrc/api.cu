@@ -104,6 +104,34 @@ int device_sm_count() {
 
 extern "C" {
 
+rssm_status conv_state_update(const rssm_conv_dims *dims, void *state, const void *u, const float *weight,
+                              const float *bias, void *out_x, void *out_b, void *out_c, rssm_stream_t stream) {
+  if (dims == nullptr) return RSSM_ERR_INVALID_ARG;
+  const rssm_conv_dims &d = *dims;
+  if (d.B < 1 || d.dx < 1 || d.dbc < 0 || d.W < 2 || d.W > 8 || !valid_dtype(d.io_dtype) ||
+      (d.silu != 0 && d.silu != 1))
+    return RSSM_ERR_INVALID_ARG;
+  if (static_cast<long long>(d.B) * (d.dx + 2ll * d.dbc) * d.W > 0x7fffffffLL * 16) return RSSM_ERR_UNSUPPORTED;
+  if (!ok_elem(state, d.io_dtype) || !ok_elem(u, d.io_dtype) || !ok4(weight) || (bias && !ok4(bias)) ||
+      !ok_elem(out_x, d.io_dtype) || (d.dbc > 0 && (!ok_elem(out_b, d.io_dtype) || !ok_elem(out_c, d.io_dtype))))
+    return RSSM_ERR_INVALID_ARG;
+  ConvLaunch a;
+  a.B = d.B;
+  a.dx = d.dx;
+  a.dbc = d.dbc;
+  a.W = d.W;
+  a.io_dtype = d.io_dtype;
+  a.silu = d.silu;
+  a.state = state;
+  a.u = u;
+  a.weight = weight;
+  a.bias = bias;
+  a.out_x = out_x;
+  a.out_b = out_b;
+  a.out_c = out_c;
+  return cuda_status(launch_conv_step(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int32_t rssm_version(void) { return 200; }
 
 const char *rssm_status_string(rssm_status s) {

@@ -118,6 +118,16 @@ cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, cudaStre
 
 cudaError_t launch_gdn(GdnKind kind, const GdnLaunch &a, cudaStream_t stream);
 
+// Convolution-state decode step (conv.cu).
+struct ConvLaunch {
+  int B, dx, dbc, W, io_dtype, silu;
+  void *state;
+  const void *u;
+  const float *weight, *bias;
+  void *out_x, *out_b, *out_c;
+};
+cudaError_t launch_conv_step(const ConvLaunch &a, cudaStream_t stream);
+
 // Flush of either family.  For Mamba-2 the per-entry log decay is A_i * dt_j
 // and the folded vector is dt_j * v_j; for GDN the log decay is g_j and the
 // vector u_j.

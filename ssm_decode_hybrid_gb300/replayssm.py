@@ -42,6 +42,10 @@ class GdnDims(ctypes.Structure):
     _fields_ = [(f, ctypes.c_int32) for f in ("B", "Hv", "Hk", "dk", "dv", "L", "in_dtype", "u_dtype", "y_dtype")]
 
 
+class ConvDims(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int32) for f in ("B", "dx", "dbc", "W", "io_dtype", "silu")]
+
+
 class GdnReplay(ctypes.Structure):
     _fields_ = [(f, ctypes.c_void_p) for f in
                 ("S0", "ring_u", "ring_k", "ring_g", "start", "count", "flag", "sync", "err", "work")] + \
@@ -56,7 +60,7 @@ EXPORTS = (
     "gdn_spec_verify_baseline", "rssm_version", "rssm_status_string", "rssm_last_cuda_error",
     "replay_decode_workspace_bytes", "replay_decode_step_fused_noalloc",
     "gdn_replay_decode_fused", "gdn_replay_workspace_bytes", "replay_verify_workspace_bytes",
-    "replay_seq_bytes", "gdn_replay_seq_bytes",
+    "replay_seq_bytes", "gdn_replay_seq_bytes", "conv_state_update",
 )
 
 
@@ -82,6 +86,7 @@ def _load() -> ctypes.CDLL:
         "gdn_replay_flush": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), P],
         "gdn_replay_verify": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), I, P, P, P, P, P, P, P],
         "gdn_spec_verify_baseline": [ctypes.POINTER(GdnDims), I, P, P, P, P, P, P, P, P, P, P],
+        "conv_state_update": [ctypes.POINTER(ConvDims), P, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -469,6 +474,25 @@ def gdn_spec_verify_baseline(slots, cur, q, k, v, beta, g, y=None, err=None, y_d
                                         _ptr(beta), _ptr(g), _ptr(y), _ptr(err), _stream()),
            "gdn_spec_verify_baseline")
     return y
+
+
+def conv_state_update(state, u, weight, bias, dx: int, dbc: int, silu: bool = True, out=None):
+    """Convolution-state decode step: state [B][dx+2dbc][W-1] (updated in
+    place), u [B][dx+2dbc] (same dtype, bf16 or f32), weight f32 [dx+2dbc][W],
+    bias f32 [dx+2dbc] or None.  Returns (x [B][dx], b [B][dbc], c [B][dbc])
+    in the state's dtype, or writes into `out` = (x, b, c)."""
+    B, C, Wm1 = state.shape
+    if C != dx + 2 * dbc or tuple(u.shape) != (B, C) or u.dtype != state.dtype:
+        raise ValueError("state/u shapes or dtypes do not match dx + 2 dbc channels")
+    _f32(weight, "weight")
+    if bias is not None:
+        _f32(bias, "bias")
+    if out is None:
+        out = tuple(torch.empty(B, n, dtype=state.dtype, device=state.device) for n in (dx, dbc, dbc))
+    dims = ConvDims(B, dx, dbc, Wm1 + 1, _dt(state), 1 if silu else 0)
+    _check(LIB.conv_state_update(ctypes.byref(dims), _ptr(state), _ptr(u), _ptr(weight), _ptr(bias),
+                                 *(_ptr(t) if t.numel() else None for t in out), _stream()), "conv_state_update")
+    return out
 
 
 def version() -> int:

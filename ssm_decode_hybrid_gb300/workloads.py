@@ -320,3 +320,40 @@ def accepted_counts_device(B: int, T: int, seed: int, device):
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     return torch.randint(0, T + 1, (B,), generator=g, device=device, dtype=torch.int32)
+
+
+@dataclasses.dataclass
+class ConvShape:
+    """Convolution state of a Mamba-2 layer: conv_dim = dx + 2 dbc channels,
+    width W (the state keeps W - 1 columns)."""
+
+    B: int
+    dx: int
+    dbc: int
+    W: int = 4
+    io_dtype: str = BF16
+
+
+@dataclasses.dataclass
+class ConvInit:
+    shape: ConvShape
+    state: np.ndarray  # [B, C, W-1] (values in io_dtype)
+    weight: np.ndarray  # [C, W] f32
+    bias: np.ndarray  # [C] f32
+
+
+def conv_init(shape: ConvShape, seed: int) -> ConvInit:
+    """State ~ N(0, 1) in io_dtype, weight ~ N(0, 0.5^2), bias ~ N(0, 0.1^2)."""
+    s = shape
+    C = s.dx + 2 * s.dbc
+    rng = np.random.default_rng([seed, 20])
+    state = round_to(rng.standard_normal((s.B, C, s.W - 1)).astype(np.float32), s.io_dtype)
+    weight = (0.5 * rng.standard_normal((C, s.W))).astype(np.float32)
+    bias = (0.1 * rng.standard_normal(C)).astype(np.float32)
+    return ConvInit(s, state, weight, bias)
+
+
+def conv_input(shape: ConvShape, seed: int, step: int) -> np.ndarray:
+    """The in-projection's x|B|C column of one decode step, N(0, 1) in io_dtype."""
+    rng = np.random.default_rng([seed, 21, step])
+    return round_to(rng.standard_normal((shape.B, shape.dx + 2 * shape.dbc)).astype(np.float32), shape.io_dtype)

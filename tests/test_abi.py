@@ -77,6 +77,16 @@ def test_host_validation_rejects_bad_arguments():
     badwork = R.M2Replay(*([fake] * 9), mis)  # misaligned decode workspace
     assert L.replay_decode_step(ctypes.byref(dims()), ctypes.byref(badwork), *args) == -1
     assert L.replay_decode_step_fused(ctypes.byref(dims()), ctypes.byref(badwork), *args) == -1
+    cd = R.ConvDims(2, 8, 4, 4, R.BF16, 1)
+    cargs = [fake, fake, fake, None, fake, fake, fake, None]
+    for bad in (R.ConvDims(2, 8, 4, 1, R.BF16, 1), R.ConvDims(2, 8, 4, 9, R.BF16, 1), R.ConvDims(0, 8, 4, 4, R.BF16, 1),
+                R.ConvDims(2, 0, 4, 4, R.BF16, 1), R.ConvDims(2, 8, -1, 4, R.BF16, 1), R.ConvDims(2, 8, 4, 4, 5, 1),
+                R.ConvDims(2, 8, 4, 4, R.BF16, 2)):
+        assert L.conv_state_update(ctypes.byref(bad), *cargs) == -1
+    assert L.conv_state_update(None, *cargs) == -1
+    assert L.conv_state_update(ctypes.byref(cd), fake, fake, P(0x10002), None, fake, fake, fake,
+                               None) == -1  # misaligned weight
+    assert L.conv_state_update(ctypes.byref(cd), fake, fake, fake, None, fake, None, fake, None) == -1  # no B output
     nosync = R.M2Replay(*([fake] * 7), None, fake)
     assert L.replay_decode_step(ctypes.byref(dims()), ctypes.byref(nosync), *args) == -1
     assert L.replay_flush(ctypes.byref(dims()), ctypes.byref(nosync), fake, None) == -1
