@@ -179,6 +179,12 @@ def test_chunked_verify_tensor_core_dtypes(T, u_dtype, y_dtype):
     run_verify(shape, T, rounds=8, seed=340 + T, y_dtype=y_dtype)
 
 
+def test_chunked_verify_window_equal_to_ring():
+    """T = L: every round starts from an empty buffer and flushes after it."""
+    run_verify(wl.GdnShape(B=4, Hv=8, Hk=4, dk=128, dv=128, L=4, in_dtype=wl.BF16), 4, rounds=8, seed=350)
+    run_verify(wl.GdnShape(B=3, Hv=4, Hk=2, dk=64, dv=64, L=2, in_dtype=wl.BF16), 2, rounds=8, seed=351)
+
+
 def test_chunked_verify_full_batch_sampled():
     """Batch 256, T = 4, accepted ~ U{0..4}: sampled sequences."""
     run_verify(wl.GDN_LAYER, 4, rounds=16, seed=wl.SEED_GDN + 50, sample=[1, 99, 254])

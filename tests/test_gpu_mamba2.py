@@ -248,6 +248,13 @@ def test_spec_verify_bf16_out_tensor_core(T):
     run_spec(shape, T, rounds=8, seed=80 + T, y_dtype=torch.bfloat16)
 
 
+def test_spec_window_equal_to_ring():
+    """T = L: every round starts with an empty buffer (fill 0), flags the early
+    flush, and folds exactly the accepted drafts."""
+    run_spec(wl.Mamba2Shape(B=5, H=8, G=2, d=64, n=128, L=4, in_dtype=wl.BF16), 4, rounds=8, seed=95)
+    run_spec(wl.Mamba2Shape(B=3, H=4, G=2, d=32, n=64, L=2, in_dtype=wl.F32), 2, rounds=8, seed=96)
+
+
 def test_spec_full_batch_sampled():
     """Batch 512, T = 4, L = 16, accepted ~ U{0..4}: sampled sequences."""
     run_spec(wl.SPEC_MAMBA2, 4, rounds=24, seed=wl.SEED_SPEC, sample=[0, 100, 311, 511])
