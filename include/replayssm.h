@@ -382,6 +382,24 @@ RSSM_API rssm_status conv_state_update(const rssm_conv_dims *dims, void *state, 
 /* Library version, e.g. 200 for 0.2.0.  Host-only; never fails. */
 RSSM_API int32_t rssm_version(void);
 
+/* Element counts of one layer's arrays, for allocation (host only).
+ * Mamba-2: S0 = B H d n, ring_v = B H L d, ring_k = B G L n, ring_dt = B H L,
+ * per_seq = B (each of start, count, flag, sync).  GDN: S0 = B Hv dv dk,
+ * ring_u = B Hv L dv, ring_k = B Hk L dk, ring_g = B Hv L, per_seq = B.
+ * RSSM_ERR_INVALID_ARG for null pointers or invalid dims (as the calls).     */
+typedef struct {
+  int64_t S0, ring_vec, ring_k, ring_decay, per_seq;
+} rssm_layout;
+RSSM_API rssm_status rssm_m2_layout_sizes(const rssm_m2_dims *dims, rssm_layout *out);
+RSSM_API rssm_status rssm_gdn_layout_sizes(const rssm_gdn_dims *dims, rssm_layout *out);
+
+/* Read the sticky device error word (`err` of a state, one int32 in device
+ * memory) into *value: an asynchronous copy on `stream`, then a wait for the
+ * stream -- the one call of this library that synchronises.  The word is not
+ * cleared.  RSSM_ERR_INVALID_ARG for null pointers, RSSM_ERR_CUDA if the copy
+ * or the wait fails (rssm_last_cuda_error tells which).                     */
+RSSM_API rssm_status rssm_read_error(const int32_t *err, int32_t *value, rssm_stream_t stream);
+
 /* Static description of a status code.  Host-only; never fails. */
 RSSM_API const char *rssm_status_string(rssm_status s);
 

@@ -146,6 +146,40 @@ const char *rssm_status_string(rssm_status s) {
 
 const char *rssm_last_cuda_error(void) { return g_last_cuda_error; }
 
+rssm_status rssm_m2_layout_sizes(const rssm_m2_dims *dims, rssm_layout *out) {
+  if (out == nullptr) return RSSM_ERR_INVALID_ARG;
+  const rssm_status st = check_m2_dims(dims);
+  if (st) return st;
+  const int64_t B = dims->B;
+  out->S0 = B * dims->H * dims->d * dims->n;
+  out->ring_vec = B * dims->H * dims->L * dims->d;
+  out->ring_k = B * dims->G * dims->L * dims->n;
+  out->ring_decay = B * dims->H * dims->L;
+  out->per_seq = B;
+  return RSSM_OK;
+}
+
+rssm_status rssm_gdn_layout_sizes(const rssm_gdn_dims *dims, rssm_layout *out) {
+  if (out == nullptr) return RSSM_ERR_INVALID_ARG;
+  const rssm_status st = check_gdn_dims(dims);
+  if (st) return st;
+  const int64_t B = dims->B;
+  out->S0 = B * dims->Hv * dims->dv * dims->dk;
+  out->ring_vec = B * dims->Hv * dims->L * dims->dv;
+  out->ring_k = B * dims->Hk * dims->L * dims->dk;
+  out->ring_decay = B * dims->Hv * dims->L;
+  out->per_seq = B;
+  return RSSM_OK;
+}
+
+rssm_status rssm_read_error(const int32_t *err, int32_t *value, rssm_stream_t stream) {
+  if (err == nullptr || value == nullptr || !ok4(err)) return RSSM_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(value, err, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return cuda_status(e);
+}
+
 // ------------------------------- Mamba-2 ---------------------------------
 
 int64_t replay_decode_workspace_bytes(const rssm_m2_dims *dims) {

@@ -42,6 +42,10 @@ class GdnDims(ctypes.Structure):
     _fields_ = [(f, ctypes.c_int32) for f in ("B", "Hv", "Hk", "dk", "dv", "L", "in_dtype", "u_dtype", "y_dtype")]
 
 
+class Layout(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int64) for f in ("S0", "ring_vec", "ring_k", "ring_decay", "per_seq")]
+
+
 class ConvDims(ctypes.Structure):
     _fields_ = [(f, ctypes.c_int32) for f in ("B", "dx", "dbc", "W", "io_dtype", "silu")]
 
@@ -61,6 +65,7 @@ EXPORTS = (
     "replay_decode_workspace_bytes", "replay_decode_step_fused_noalloc",
     "gdn_replay_decode_fused", "gdn_replay_workspace_bytes", "replay_verify_workspace_bytes",
     "replay_seq_bytes", "gdn_replay_seq_bytes", "conv_state_update",
+    "rssm_m2_layout_sizes", "rssm_gdn_layout_sizes", "rssm_read_error",
 )
 
 
@@ -87,6 +92,9 @@ def _load() -> ctypes.CDLL:
         "gdn_replay_verify": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), I, P, P, P, P, P, P, P],
         "gdn_spec_verify_baseline": [ctypes.POINTER(GdnDims), I, P, P, P, P, P, P, P, P, P, P],
         "conv_state_update": [ctypes.POINTER(ConvDims), P, P, P, P, P, P, P, P],
+        "rssm_m2_layout_sizes": [ctypes.POINTER(M2Dims), ctypes.POINTER(Layout)],
+        "rssm_gdn_layout_sizes": [ctypes.POINTER(GdnDims), ctypes.POINTER(Layout)],
+        "rssm_read_error": [P, ctypes.POINTER(ctypes.c_int32), P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -493,6 +501,24 @@ def conv_state_update(state, u, weight, bias, dx: int, dbc: int, silu: bool = Tr
     _check(LIB.conv_state_update(ctypes.byref(dims), _ptr(state), _ptr(u), _ptr(weight), _ptr(bias),
                                  *(_ptr(t) if t.numel() else None for t in out), _stream()), "conv_state_update")
     return out
+
+
+def layout_sizes(dims) -> Layout:
+    """Element counts of one layer's arrays (rssm_m2_layout_sizes or
+    rssm_gdn_layout_sizes, chosen by the type of dims)."""
+    out = Layout()
+    fn = LIB.rssm_gdn_layout_sizes if isinstance(dims, GdnDims) else LIB.rssm_m2_layout_sizes
+    _check(fn(ctypes.byref(dims), ctypes.byref(out)), "layout_sizes")
+    return out
+
+
+def read_error(err: torch.Tensor) -> int:
+    """The sticky device error word, read on torch's current stream (this
+    waits for the stream)."""
+    _i32(err, "err")
+    v = ctypes.c_int32(0)
+    _check(LIB.rssm_read_error(_ptr(err), ctypes.byref(v), _stream()), "rssm_read_error")
+    return int(v.value)
 
 
 def version() -> int:

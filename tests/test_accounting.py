@@ -76,3 +76,21 @@ def test_invalid_arguments_give_zero():
     bad = R.M2Dims(2, 3, 2, 64, 128, 16, R.BF16, R.F32)
     assert R.LIB.replay_seq_bytes(ctypes.byref(bad), 4, 0) == 0
     assert R.LIB.replay_seq_bytes(None, 4, 0) == 0
+
+
+def test_layout_sizes_match_allocated_tensors():
+    R = _R()
+    st = R.Mamba2State.empty(5, 8, 2, 48, 64, 12, device="cpu", workspace=False)
+    lay = R.layout_sizes(st.dims())
+    assert (lay.S0, lay.ring_vec, lay.ring_k, lay.ring_decay, lay.per_seq) == (
+        st.S0.numel(), st.ring_v.numel(), st.ring_k.numel(), st.ring_dt.numel(), st.start.numel())
+    gst = R.GdnState.empty(3, 8, 4, 128, 64, 16, device="cpu", workspace_T=0)
+    lay = R.layout_sizes(gst.dims())
+    assert (lay.S0, lay.ring_vec, lay.ring_k, lay.ring_decay, lay.per_seq) == (
+        gst.S0.numel(), gst.ring_u.numel(), gst.ring_k.numel(), gst.ring_g.numel(), gst.count.numel())
+    import ctypes
+
+    bad = R.M2Dims(2, 3, 2, 64, 128, 16, R.BF16, R.F32)
+    assert R.LIB.rssm_m2_layout_sizes(ctypes.byref(bad), ctypes.byref(R.Layout())) == -1
+    assert R.LIB.rssm_m2_layout_sizes(ctypes.byref(st.dims()), None) == -1
+    assert R.LIB.rssm_read_error(None, None, None) == -1

@@ -299,6 +299,7 @@ def test_device_error_bits():
     R.replay_decode_step(state, *m2_step_dev(st, shape.in_dtype), A, y=y)
     torch.cuda.synchronize()
     assert int(host(state.err)[0]) == R.EBIT_COUNT_RANGE
+    assert R.read_error(state.err) == R.EBIT_COUNT_RANGE
     np.testing.assert_array_equal(host(state.count), [8, 3, -1, 4])
     yh = host(y)
     assert np.all(np.isnan(yh[[0, 2]])) and np.all(np.isfinite(yh[[1, 3]]))
