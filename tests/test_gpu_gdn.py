@@ -212,3 +212,25 @@ def test_snapshot_baseline_parity(T):
     for b in range(shape.B):
         assert_close(slots[b, int(base.cur[b])], base.state(b), what=f"state {b}")
     assert int(host(err)[0]) == 0
+
+
+def test_tensor_core_verify_window_error_skips_the_sequence():
+    """A verify window that does not fit (count + T > L) on the tensor-core
+    path: the error bit is set, that sequence's outputs are left alone, the
+    other sequences follow the oracle; nothing faults."""
+    R = rs()
+    shape = wl.GdnShape(B=3, Hv=4, Hk=2, dk=128, dv=128, L=8, in_dtype=wl.BF16)
+    T = 4
+    init = wl.gdn_init(shape, 360, fill_max=shape.L - T)
+    init.count[:] = [2, 6, 0]  # 6 + 4 > 8
+    state = gdn_state(init)
+    orc = oracle_replay(init, np.array([0, 2]))
+    st = wl.gdn_step(shape, 360, 0, T=T)
+    y = torch.full((shape.B, T, shape.Hv, shape.dv), float("nan"), device="cuda")
+    R.gdn_replay_verify(state, *gdn_step_dev(st, shape.in_dtype), y=y)
+    assert R.read_error(state.err) == R.EBIT_WINDOW
+    yh = host(y)
+    assert np.all(np.isnan(yh[1]))
+    Y_ref = orc.verify(take(st.q, [0, 2]), take(st.k, [0, 2]), take(st.v, [0, 2]), take(st.beta, [0, 2]),
+                       take(st.g, [0, 2]))
+    assert_close(y[[0, 2]], Y_ref, what="valid sequences")

@@ -341,3 +341,23 @@ def test_checkpoint_resume_bit_identical():
         R.replay_flush(restored, A)
         assert torch.equal(y, ys[t])
     assert torch.equal(restored.S0, state.S0)
+
+
+def test_tensor_core_verify_window_error_skips_the_sequence():
+    """As above for the Mamba-2 tensor-core verify (T = 5)."""
+    R = rs()
+    shape = wl.Mamba2Shape(B=3, H=8, G=2, d=64, n=128, L=8, in_dtype=wl.BF16)
+    T = 5
+    init = wl.mamba2_init(shape, 97, fill_max=shape.L - T)
+    init.count[:] = [1, 4, 3]  # 4 + 5 > 8
+    state = m2_state(init)
+    orc = oracle_replay(init, np.array([0, 2]))
+    A = dev(init.A)
+    st = wl.mamba2_step(shape, 97, 0, T=T)
+    y = torch.full((shape.B, T, shape.H, shape.d), float("nan"), device="cuda")
+    R.replay_spec_verify(state, *m2_step_dev(st, shape.in_dtype), A, y=y)
+    assert R.read_error(state.err) == R.EBIT_WINDOW
+    yh = host(y)
+    assert np.all(np.isnan(yh[1]))
+    Y_ref = orc.spec_verify(take(st.v, [0, 2]), take(st.k, [0, 2]), take(st.q, [0, 2]), take(st.dt, [0, 2]))
+    assert_close(y[[0, 2]], Y_ref, what="valid sequences")
