@@ -62,7 +62,7 @@ struct GPrepSmem {
   __host__ __device__ GPrepSmem(int L, int N, int dv, int HpK, int P, int es, int eu) {
     k_ring = 0;
     u_ring = k_ring + L * N * es;
-    g_ring = u_ring + HpK * L * dv * eu;
+    g_ring = u_ring + (P > 1 ? HpK * L * dv * eu : 0);  // window width 1 reads u from global memory
     k_in = g_ring + HpK * L * 4;
     q_in = k_in + P * N * es;
     copied_end = q_in + P * N * es;
@@ -110,10 +110,11 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
     s_ptr[1] = sc;
     if (hc >= 1 && hc <= L && sc >= 0 && sc < L) {
       const int n1 = min(hc, L - sc), n2 = hc - n1;
-      mbar_expect_tx(&bar, static_cast<uint32_t>(hc) * (N * es + HpK * dv * eu));
+      mbar_expect_tx(&bar, static_cast<uint32_t>(hc) * (N * es + (NT > 1 ? HpK * dv * eu : 0)));
       const unsigned char *gk = static_cast<const unsigned char *>(a.ring_k) + bk * L * N * es;
       bulk_g2s(psm + lay.k_ring + sc * N * es, gk + static_cast<size_t>(sc) * N * es, n1 * N * es, &bar);
       if (n2 > 0) bulk_g2s(psm + lay.k_ring, gk, n2 * N * es, &bar);
+      if (NT > 1)  // wider windows stage the u rings; width 1 reads them from global memory
       for (int hw = 0; hw < HpK; ++hw) {
         const unsigned char *gu = static_cast<const unsigned char *>(a.ring_u) + (h0 + hw) * L * dv * eu;
         unsigned char *su = psm + lay.u_ring + static_cast<size_t>(hw) * L * dv * eu;
@@ -243,6 +244,50 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   __syncwarp();
 
   // buffer vectors of this value head: sum_{j<h} w_j (k_j . x_v) u_j[r]
+  if constexpr (NT == 1) {
+    // u read from global memory, eight entries of four rows per lane in
+    // flight at once: without the u rings in shared memory more precompute
+    // blocks fit on an SM, and the grid of a decode step takes fewer waves
+    const TU *gu = static_cast<const TU *>(a.ring_u) + bh * L * dv;
+    constexpr int RPL = 4;
+    for (int r0 = lane; r0 < dv; r0 += 32 * RPL) {
+      float acc[RPL][NV];
+#pragma unroll
+      for (int m = 0; m < RPL; ++m)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc[m][v] = 0.f;
+      for (int j0 = 0; j0 < h; j0 += 8) {
+        float uu[8][RPL];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          const int sl = wrapL(st + (j < h ? j : 0), L);
+#pragma unroll
+          for (int m = 0; m < RPL; ++m) {
+            const int r = r0 + 32 * m;
+            uu[jj][m] = (j < h && r < dv) ? load1(gu + static_cast<size_t>(sl) * dv + r) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          if (j < h) {
+#pragma unroll
+            for (int m = 0; m < RPL; ++m)
+#pragma unroll
+              for (int v = 0; v < NV; ++v) acc[m][v] = fmaf(scoef[v * kMaxL + j], uu[jj][m], acc[m][v]);
+          }
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < RPL; ++m) {
+        const int r = r0 + 32 * m;
+        if (r < dv)
+#pragma unroll
+          for (int v = 0; v < NV; ++v) wk[kGwBuf + v * dv + r] = acc[m][v];
+      }
+    }
+  } else
   for (int r = lane; r < dv; r += 32) {
     float acc[NV];
 #pragma unroll
