@@ -55,6 +55,12 @@ __device__ __forceinline__ float round_as<bf16>(float x) { return __bfloat162flo
 // ---------------------------------------------------------------------------
 // precompute: one CTA per (sequence, key head), one warp per value head
 // ---------------------------------------------------------------------------
+// Window widths up to this read the committed u entries from global memory
+// in the precompute (several in flight per lane) instead of staging the u
+// rings in shared memory: more precompute blocks fit on an SM.  Width 8
+// stages them (its 16 accumulators per row leave no registers to spare).
+constexpr int kUGlobalMaxP = 4;
+
 // Byte offsets in shared memory.  The first five parts are filled by bulk
 // copies (each 16-byte sized and aligned); the rest is scratch.
 struct GPrepSmem {
@@ -62,7 +68,7 @@ struct GPrepSmem {
   __host__ __device__ GPrepSmem(int L, int N, int dv, int HpK, int P, int es, int eu) {
     k_ring = 0;
     u_ring = k_ring + L * N * es;
-    g_ring = u_ring + (P > 1 ? HpK * L * dv * eu : 0);  // window width 1 reads u from global memory
+    g_ring = u_ring + (P > kUGlobalMaxP ? HpK * L * dv * eu : 0);  // narrow windows read u from global memory
     k_in = g_ring + HpK * L * 4;
     q_in = k_in + P * N * es;
     copied_end = q_in + P * N * es;
@@ -110,11 +116,11 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
     s_ptr[1] = sc;
     if (hc >= 1 && hc <= L && sc >= 0 && sc < L) {
       const int n1 = min(hc, L - sc), n2 = hc - n1;
-      mbar_expect_tx(&bar, static_cast<uint32_t>(hc) * (N * es + (NT > 1 ? HpK * dv * eu : 0)));
+      mbar_expect_tx(&bar, static_cast<uint32_t>(hc) * (N * es + (NT > kUGlobalMaxP ? HpK * dv * eu : 0)));
       const unsigned char *gk = static_cast<const unsigned char *>(a.ring_k) + bk * L * N * es;
       bulk_g2s(psm + lay.k_ring + sc * N * es, gk + static_cast<size_t>(sc) * N * es, n1 * N * es, &bar);
       if (n2 > 0) bulk_g2s(psm + lay.k_ring, gk, n2 * N * es, &bar);
-      if (NT > 1)  // wider windows stage the u rings; width 1 reads them from global memory
+      if (NT > kUGlobalMaxP)  // wider windows stage the u rings; narrow ones read them from global memory
       for (int hw = 0; hw < HpK; ++hw) {
         const unsigned char *gu = static_cast<const unsigned char *>(a.ring_u) + (h0 + hw) * L * dv * eu;
         unsigned char *su = psm + lay.u_ring + static_cast<size_t>(hw) * L * dv * eu;
@@ -244,12 +250,11 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   __syncwarp();
 
   // buffer vectors of this value head: sum_{j<h} w_j (k_j . x_v) u_j[r]
-  if constexpr (NT == 1) {
-    // u read from global memory, eight entries of four rows per lane in
-    // flight at once: without the u rings in shared memory more precompute
-    // blocks fit on an SM, and the grid of a decode step takes fewer waves
+  if constexpr (NT <= kUGlobalMaxP) {
+    // u read from global memory, eight entries of four (two for width 4)
+    // rows per lane in flight at once
     const TU *gu = static_cast<const TU *>(a.ring_u) + bh * L * dv;
-    constexpr int RPL = 4;
+    constexpr int RPL = NT == 1 ? 4 : 2;
     for (int r0 = lane; r0 < dv; r0 += 32 * RPL) {
       float acc[RPL][NV];
 #pragma unroll
