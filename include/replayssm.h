@@ -28,6 +28,15 @@
  *    out of range) sets a bit in the caller's sticky int32 error word *err
  *    (RSSM_EBIT_*) and that sequence is skipped; kernels never trap and never
  *    spin.  Read *err after synchronising; clear it yourself.
+ *  - Every wait inside a kernel is bounded (about one second) and sets
+ *    RSSM_EBIT_TIMEOUT when it runs out.  In the precompute kernel of a
+ *    two-launch call (a workspace is given) the affected sequence is skipped
+ *    as a whole: its pointers, checkpoint, ring and outputs stay as they were.
+ *    A wait that runs out in any other kernel leaves the affected sequences'
+ *    outputs and state undefined: restore them from a checkpoint.  The
+ *    environment variable RSSM_WAIT_LIMIT_NS (nanoseconds, read at every
+ *    call) replaces the precompute kernels' limit; 0 makes those waits count
+ *    as run out at once, which exercises the recovery path in tests.
  *  - Supported shapes (checked on the host, RSSM_ERR_UNSUPPORTED otherwise):
  *    n (Mamba-2 state size) and dk (GDN key size) in {16, 32, 64, 128};
  *    d and dv multiples of 4 with 4 <= d <= 256;
@@ -216,10 +225,12 @@ RSSM_API rssm_status replay_decode_step_fused(const rssm_m2_dims *dims, const rs
  * The pages have no counterpart: this is an interface variant of
  * replay_decode_step_fused, with the same outputs and state updates.
  * st->work is ignored; the two-launch kernels use a file-scope device array
- * of 8 MiB (2,097,152 floats) inside the library, whose address is looked up
- * once per device.  Requires B * H * 4 * ceil((d + L + 4) / 4) <= 2,097,152
- * (RSSM_ERR_UNSUPPORTED otherwise).  All calls on one device share that
- * array, so they must be ordered (one stream, or synchronised streams).
+ * of 8 MiB (2,097,152 floats) inside the library, whose address in the
+ * current context is looked up on every call (no allocation).  Requires
+ * B * H * 4 * ceil((d + L + 4) / 4) <= 2,097,152 (RSSM_ERR_UNSUPPORTED
+ * otherwise, before anything is launched).  All calls on one device share
+ * that array, so they must be ordered (one stream, or synchronised streams):
+ * calls that overlap on the GPU race on it.
  * Arguments as replay_decode_step.                                            */
 RSSM_API rssm_status replay_decode_step_fused_noalloc(const rssm_m2_dims *dims, const rssm_m2_replay *st,
                                                       const void *v, const void *k, const void *q,

@@ -2,9 +2,9 @@
 // one kernel launch on the caller's stream.  Nothing here allocates memory or
 // synchronises.
 #include <cstdio>
+#include <cstdlib>
 #include <algorithm>
 #include <cstring>
-#include <mutex>
 
 #include "kernels.cuh"
 
@@ -50,6 +50,18 @@ rssm_status check_gdn_dims(const rssm_gdn_dims *dm) {
   return RSSM_OK;
 }
 
+// Limit of the precompute kernels' data waits: about one second, or the
+// value of the environment variable RSSM_WAIT_LIMIT_NS (nanoseconds), read
+// at every call.  0 makes every such wait count as run out, which exercises
+// the path that gives a sequence up (RSSM_EBIT_TIMEOUT).
+uint64_t precompute_wait_ns() {
+  const char *e = std::getenv("RSSM_WAIT_LIMIT_NS");
+  if (e == nullptr || *e == '\0') return kWaitLimitNs;
+  char *end = nullptr;
+  const unsigned long long v = std::strtoull(e, &end, 10);
+  return (end != nullptr && *end == '\0') ? static_cast<uint64_t>(v) : kWaitLimitNs;
+}
+
 M2Launch m2_launch(const rssm_m2_dims &d) {
   M2Launch a;
   std::memset(&a, 0, sizeof(a));
@@ -62,6 +74,7 @@ M2Launch m2_launch(const rssm_m2_dims &d) {
   a.T = 1;
   a.in_dtype = d.in_dtype;
   a.y_dtype = d.y_dtype;
+  a.wait_ns = precompute_wait_ns();
   return a;
 }
 
@@ -78,6 +91,7 @@ GdnLaunch gdn_launch(const rssm_gdn_dims &d) {
   a.in_dtype = d.in_dtype;
   a.u_dtype = d.u_dtype;
   a.y_dtype = d.y_dtype;
+  a.wait_ns = precompute_wait_ns();
   return a;
 }
 
@@ -589,24 +603,15 @@ namespace {
 constexpr size_t kStaticWorkFloats = size_t(1) << 21;  // 8 MiB
 __device__ __align__(256) float g_static_work[kStaticWorkFloats];
 
-constexpr int kMaxCachedDevices = 64;
-std::mutex g_static_work_mu;
-float *g_static_work_ptr[kMaxCachedDevices] = {};
-
-// Device address of g_static_work on the current device, looked up once per device.
+// Device address of g_static_work in the current context.  A __device__
+// variable's address belongs to the context that loaded the module, so it is
+// looked up on every call (a table lookup in the runtime, no allocation):
+// after cudaDeviceReset, or under another context, the fresh address is used.
 cudaError_t static_work_ptr(float **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_work);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxCachedDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_static_work_mu);
-  if (g_static_work_ptr[dev] == nullptr) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_work);
-    if (e != cudaSuccess) return e;
-    g_static_work_ptr[dev] = static_cast<float *>(p);
-  }
-  *out = g_static_work_ptr[dev];
+  *out = static_cast<float *>(p);
   return cudaSuccess;
 }
 

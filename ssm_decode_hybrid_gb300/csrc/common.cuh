@@ -199,6 +199,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
+// Bounded wait with a limit chosen at launch.  A limit of 0 counts the wait
+// as run out without polling: the host sets it only to exercise the recovery
+// path of the caller (which must still drain its copies with mbar_wait).
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns == 0) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
 // Bulk (non-tensor) asynchronous copy global -> shared; completion is counted
 // in bytes on `bar`.  dst, src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -230,6 +242,23 @@ __device__ __forceinline__ bool named_bar_or(int id, int threads, bool pred) {
       : "r"(id), "r"(threads), "r"(pred ? 1u : 0u)
       : "memory");
   return out != 0;
+}
+
+// Whether the precompute kernel left a valid record for every group of one
+// sequence.  The records of the sequence's heads are `stride` floats apart
+// from `first`; a group's precompute block writes the records of its `hpg`
+// heads, so the first head of each group speaks for the block; its int info
+// word sits at float `info_off` and carries `valid_bit` when the block
+// finished.  A block that gave up (a wait that ran out, pointers out of range)
+// clears it, and every streaming block of that sequence then skips the
+// sequence.  Call with the whole warp; the answer is the same in every lane.
+__device__ __forceinline__ bool group_records_valid(const float *first, int groups, int hpg, int stride, int info_off,
+                                                    int valid_bit) {
+  const int lane = threadIdx.x & 31;
+  bool ok = true;
+  for (int g = lane; g < groups; g += 32)
+    ok = ok && (reinterpret_cast<const int *>(first + static_cast<size_t>(g) * hpg * stride)[info_off] & valid_bit);
+  return __all_sync(kFull, ok);
 }
 
 }  // namespace rssm

@@ -96,9 +96,13 @@ __global__ void __launch_bounds__(1024) m2_prep_kernel(M2Launch a, int stride) {
   pdl_launch_dependents();
   const float dt_in = a.dt[bh];
   const float Ai = a.A[i];
+  float *wk = a.work + bh * stride;
   __syncthreads();  // barrier initialised, pointers read
-  const bool arrived = mbar_wait(&bar, 0);
+  const bool arrived = mbar_wait_limit(&bar, 0, a.wait_ns);
   if (__syncthreads_or(!arrived)) {
+    // give the sequence up: no valid record, so every streaming block of it
+    // skips it and its pointers, S_0 and y stay as they were
+    if (lane == 0) reinterpret_cast<int *>(wk)[1] = 0;
     if (tid == 0) {
       set_err(a.err, RSSM_EBIT_TIMEOUT);
       mbar_wait(&bar, 0);  // bounded: the copies must land before shared memory is released
@@ -107,7 +111,6 @@ __global__ void __launch_bounds__(1024) m2_prep_kernel(M2Launch a, int stride) {
   }
 
   const int h = s_ptr[0], st = s_ptr[1];
-  float *wk = a.work + bh * stride;
   if (h < 0 || h >= L || st < 0 || st >= L) {
     if (lane == 0) reinterpret_cast<int *>(wk)[1] = 0;
     if (tid == 0) set_err(a.err, RSSM_EBIT_COUNT_RANGE);
@@ -235,7 +238,10 @@ __global__ void __launch_bounds__(kThreads, 4) m2_stream_kernel(M2Launch a, int 
   pdl_wait();  // the precompute grid has finished: workspace, ring and pointers are final
   const int info = reinterpret_cast<const int *>(wk)[1];
   const float abar = wk[0];
-  if (!(info & kInfoValid)) return;
+  const int HpG = a.H / a.G;
+  if (!group_records_valid(a.work + static_cast<size_t>(b) * a.H * stride, a.G, HpG, stride, 1, kInfoValid) ||
+      !(info & kInfoValid))
+    return;
   if (i == 0 && tid == 0) {
     // every precompute block has read this sequence's pointers: advance them
     const int p = (info & 0xff) + 1;
@@ -445,10 +451,13 @@ __global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) 
   pdl_launch_dependents();
   const float Ai = a.A[i];
   const float dt_draft = (lane < T) ? a.dt[(static_cast<size_t>(b) * T + lane) * a.H + i] : 0.f;
+  float *wk = a.work + bh * stride;
   __syncthreads();  // barrier initialised, pointers read
   bool arrived = true;
-  if (w == 0) arrived = mbar_wait(&bar, 0);
+  if (w == 0) arrived = mbar_wait_limit(&bar, 0, a.wait_ns);
   if (__syncthreads_or(!arrived)) {
+    // give the sequence up: no valid record, so the streaming kernel skips it
+    if (lane == 0) reinterpret_cast<int *>(wk)[kVwInfo] = 0;
     if (tid == 0) {
       set_err(a.err, RSSM_EBIT_TIMEOUT);
       mbar_wait(&bar, 0);  // bounded: the copies must land before shared memory is released
@@ -456,7 +465,6 @@ __global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) 
     return;
   }
   const int h = s_ptr[0], st = s_ptr[1];
-  float *wk = a.work + bh * stride;
   if (h < 0 || st < 0 || st >= L || h + T > L) {
     if (lane == 0) reinterpret_cast<int *>(wk)[kVwInfo] = 0;
     if (tid == 0) set_err(a.err, RSSM_EBIT_WINDOW);
@@ -575,7 +583,10 @@ __global__ void __launch_bounds__(kThreads, NT == 8 ? 2 : 4) m2_vstream_kernel(M
                       : make_float4(0.f, 0.f, 0.f, 0.f);
   pdl_wait();  // the precompute grid has finished
   const int info = reinterpret_cast<const int *>(wk)[kVwInfo];
-  if (!(info & kInfoValid)) return;
+  if (!group_records_valid(a.work + static_cast<size_t>(b) * a.H * stride, a.G, a.H / a.G, stride, kVwInfo,
+                           kInfoValid) ||
+      !(info & kInfoValid))
+    return;
   if (i == 0 && tid == 0) a.flag[b] = ((info & 0xff) + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
 
   // S_0 q_s, PB passes x NT drafts reduced together; the reducing lane writes y

@@ -136,11 +136,15 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   const size_t tv = (static_cast<size_t>(b) * T + (lane < T ? lane : 0)) * a.Hv + i;  // draft `lane` of this head
   const float g_m = (lane < T) ? a.g[tv] : 0.f;
   const float beta_m = (lane < T) ? a.beta[tv] : 0.f;
+  float *wk = a.work + bh * stride;
   __syncthreads();  // barrier initialised, pointers read
   // one warp waits for the copies; the block barrier passes them on to the rest
   bool arrived = true;
-  if (w == 0) arrived = mbar_wait(&bar, 0);
+  if (w == 0) arrived = mbar_wait_limit(&bar, 0, a.wait_ns);
   if (__syncthreads_or(!arrived)) {
+    // give the sequence up: no valid record, so every streaming block of it
+    // skips it and its pointers, S_0, ring and y stay as they were
+    if (lane == 0) reinterpret_cast<int *>(wk)[kGwInfo] = 0;
     if (tid == 0) {
       set_err(a.err, RSSM_EBIT_TIMEOUT);
       mbar_wait(&bar, 0);  // bounded: the copies must land before shared memory is released
@@ -149,7 +153,6 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   }
 
   const int h = s_ptr[0], st = s_ptr[1];
-  float *wk = a.work + bh * stride;
   const bool ok = kDecode ? (h >= 0 && h < L && st >= 0 && st < L) : (h >= 0 && st >= 0 && st < L && h + T <= L);
   if (!ok) {
     if (lane == 0) reinterpret_cast<int *>(wk)[kGwInfo] = 0;
@@ -443,6 +446,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 8 ? 1 : 2)) gdn
     }
   }
   if (tid < kGwBuf) shdr[tid] = wk[tid];
+  const bool groups_ok =
+      group_records_valid(a.work + static_cast<size_t>(b) * a.Hv * stride, a.Hk, HpK, stride, kGwInfo, kInfoValid);
   gdn_row_dots<N, NT>(s, xv, sx, 0, row0, lane);  // the register half
   __syncthreads();  // barrier initialised, header staged
   // one warp waits for the copy; the block barrier passes it on to the rest
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 8 ? 1 : 2)) gdn
     return;
   }
   const int info = __float_as_int(shdr[kGwInfo]);
-  if (!(info & kInfoValid)) return;
+  if (!(info & kInfoValid) || !groups_ok) return;
   const int h = info & 0xff, st = (info >> 8) & 0xff;
   if (i == 0 && rb == 0 && tid == 0) {
     // every precompute block has read this sequence's pointers: advance them

@@ -35,6 +35,7 @@ struct M2Launch {
   void *y;
   float *work;         // workspace of the two-launch decode, or null
   int64_t work_bytes;  // its size
+  uint64_t wait_ns;    // limit of the precompute kernels' data wait (0: the wait counts as run out)
 };
 
 // Floats per (sequence, head) record of the two-launch decode workspace:
@@ -91,6 +92,7 @@ struct GdnLaunch {
   void *y;
   float *work;         // workspace of the two-launch decode / verify, or null
   int64_t work_bytes;  // its size
+  uint64_t wait_ns;    // limit of the precompute kernel's data wait (0: the wait counts as run out)
 };
 
 enum class GdnKind { Baseline, Decode, DecodeFused, Verify, SnapshotVerify };

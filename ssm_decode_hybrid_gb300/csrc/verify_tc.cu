@@ -235,6 +235,8 @@ __global__ void __launch_bounds__(kVtThreads, 3) gdn_verify_tc_kernel(GdnLaunch 
   pdl_wait();  // the precompute grid has finished: workspace, drafts' k and g, pointers
   const float *wk = a.work + bh * stride;
   for (int c = tid; c < kGdnWorkHeader; c += kVtThreads) shdr[c] = wk[c];
+  const bool groups_ok = group_records_valid(a.work + static_cast<size_t>(b) * a.Hv * stride, a.Hk, a.Hv / a.Hk,
+                                             stride, kGwInfo, kInfoValid);
   bool ok = tc_lo(t, &hi_bar, &mma_bar, tid, warp);
   // the solve's per-row inputs, loaded while the MMAs run
   const int r = tid;
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(kVtThreads, 3) gdn_verify_tc_kernel(GdnLaunch 
   const int info = __float_as_int(shdr[kGwInfo]);
   if (!ok) {
     if (tid == 0) set_err(a.err, RSSM_EBIT_TIMEOUT);
-  } else if (info & kInfoValid) {
+  } else if ((info & kInfoValid) && groups_ok) {
     if (i == 0 && tid == 0) a.flag[b] = ((info & 0xff) + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
     if (rowt) {
       float z[16];
@@ -319,6 +321,8 @@ __global__ void __launch_bounds__(kVtThreads, 3) m2_verify_tc_kernel(M2Launch a,
   }
   tc_hi(t, &s_tmem, &hi_bar, tid, warp);
   pdl_wait();  // the precompute grid has finished: workspace, drafts' entries, pointers
+  const bool groups_ok = group_records_valid(a.work + static_cast<size_t>(b) * a.H * stride, a.G, a.H / a.G, stride,
+                                             kMaxT, kInfoValid);
   bool ok = tc_lo(t, &hi_bar, &mma_bar, tid, warp);
   const int r = tid;
   const bool rowt = r < 2 * d;
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(kVtThreads, 3) m2_verify_tc_kernel(M2Launch a,
   } else if (rowt) {
     float z[16];
     tc_read(t, warp, z);
-    if (info & kInfoValid) {
+    if ((info & kInfoValid) && groups_ok) {
       if (i0 == 0 && tid == 0) a.flag[b] = ((info & 0xff) + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
       TO *y = static_cast<TO *>(a.y);
 #pragma unroll

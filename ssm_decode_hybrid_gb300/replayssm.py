@@ -20,7 +20,7 @@ LIB_PATH = os.environ.get("REPLAYSSM_LIB") or os.path.join(_HERE, "libreplayssm.
 
 F32, BF16 = 0, 1
 SEQ_REPLAY, SEQ_SNAPSHOT = 0, 1
-EBIT_COUNT_RANGE, EBIT_WINDOW, EBIT_ACCEPTED, EBIT_CUR = 1, 2, 4, 8
+EBIT_COUNT_RANGE, EBIT_WINDOW, EBIT_ACCEPTED, EBIT_CUR, EBIT_TIMEOUT = 1, 2, 4, 8, 16
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
 

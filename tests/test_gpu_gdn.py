@@ -234,3 +234,32 @@ def test_tensor_core_verify_window_error_skips_the_sequence():
     Y_ref = orc.verify(take(st.q, [0, 2]), take(st.k, [0, 2]), take(st.v, [0, 2]), take(st.beta, [0, 2]),
                        take(st.g, [0, 2]))
     assert_close(y[[0, 2]], Y_ref, what="valid sequences")
+
+
+def test_gdn_layer_fused_full_batch_sampled():
+    """gdn_replay_decode_fused with the workspace (the launch pair the GDN
+    benchmark times) at its own size: batch 256, Hv = 32, Hk = 16,
+    d_k = d_v = 128, L = 16, random fill, 40 steps (every sequence folds at
+    least twice).  Eight sampled sequences against the oracle, the first and
+    last of the grid among them; every sequence's pointers against their closed
+    form (the fused step folds a full buffer in place: start never moves)."""
+    shape = wl.GDN_LAYER
+    R = rs()
+    init = wl.gdn_init(shape, wl.SEED_GDN)
+    idx = np.array([0, 1, 63, 77, 128, 200, 254, 255])
+    state = gdn_state(init)
+    orc = oracle_replay(init, idx)
+    start0, count0 = init.start.astype(np.int64), init.count.astype(np.int64)
+    for t in range(40):
+        st = wl.gdn_step(shape, wl.SEED_GDN, t)
+        y = R.gdn_replay_decode_fused(state, *gdn_step_dev(st, shape.in_dtype))
+        y_ref = orc.decode_step(take(st.q, idx), take(st.k, idx), take(st.v, idx), take(st.beta, idx),
+                                take(st.g, idx))
+        orc.flush()
+        assert_close(y[idx], y_ref, what=f"step {t}")
+        tot = count0 + t + 1
+        np.testing.assert_array_equal(host(state.count), tot % shape.L, err_msg=f"step {t}: count")
+        np.testing.assert_array_equal(host(state.start), start0, err_msg=f"step {t}: start")
+        np.testing.assert_array_equal(host(state.flag), np.zeros(shape.B), err_msg=f"step {t}: flag")
+    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0

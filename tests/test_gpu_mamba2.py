@@ -361,3 +361,64 @@ def test_tensor_core_verify_window_error_skips_the_sequence():
     assert np.all(np.isnan(yh[1]))
     Y_ref = orc.spec_verify(take(st.v, [0, 2]), take(st.k, [0, 2]), take(st.q, [0, 2]), take(st.dt, [0, 2]))
     assert_close(y[[0, 2]], Y_ref, what="valid sequences")
+
+
+def run_fused_sampled(shape, seed, steps, idx, graph_steps=0):
+    """replay_decode_step_fused with a workspace (the launch pair the benchmark
+    times) over `steps` steps: sampled sequences' outputs and final S_0 against
+    the oracle, every sequence's pointers against their closed form (the fused
+    step folds a full buffer in place, so start never moves and count cycles
+    through 0..L-1).  The last `graph_steps` steps are captured once in a CUDA
+    graph per step and replayed, as the benchmark does."""
+    R = rs()
+    init = wl.mamba2_init(shape, seed)
+    state = m2_state(init)
+    orc = oracle_replay(init, idx)
+    A = dev(init.A)
+    start0, count0 = init.start.astype(np.int64), init.count.astype(np.int64)
+    y = torch.empty(shape.B, shape.H, shape.d, device="cuda")
+    for t in range(steps):
+        st = wl.mamba2_step(shape, seed, t)
+        inp = m2_step_dev(st, shape.in_dtype)
+        if t >= steps - graph_steps:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            snap = {f: getattr(state, f).clone() for f in ("S0", "ring_v", "ring_k", "ring_dt", "start", "count")}
+            with torch.cuda.graph(g, stream=s):
+                R.replay_decode_step_fused(state, *inp, A, y=y)
+            torch.cuda.current_stream().wait_stream(s)
+            for f, v in snap.items():  # capture does not run the kernels, but be explicit
+                assert torch.equal(getattr(state, f), v)
+            g.replay()
+        else:
+            R.replay_decode_step_fused(state, *inp, A, y=y)
+        y_ref = orc.decode_step(take(st.v, idx), take(st.k, idx), take(st.q, idx), take(st.dt, idx))
+        orc.flush()
+        assert_close(y[idx], y_ref, what=f"step {t}")
+        tot = count0 + t + 1
+        np.testing.assert_array_equal(host(state.count), tot % shape.L, err_msg=f"step {t}: count")
+        np.testing.assert_array_equal(host(state.start), start0, err_msg=f"step {t}: start")
+        np.testing.assert_array_equal(host(state.flag), np.zeros(shape.B), err_msg=f"step {t}: flag")
+    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0
+    assert int(host(state.sync).sum()) == 0
+
+
+def test_nemotron_layer_fused_full_batch_sampled():
+    """The benchmarked step at its own size: batch 256, H = 32, G = 8, d = 64,
+    n = 128, L = 16, random fill, replay_decode_step_fused with the workspace
+    (precompute + S_0 stream of 8192 blocks, several waves), 48 steps so every
+    sequence folds three times; the last 8 steps replayed from CUDA graphs.
+    Ten sampled sequences, the first and last blocks of the grid among them."""
+    run_fused_sampled(wl.NEMOTRON_H_MAMBA2, wl.SEED_NEMOTRON, 48,
+                      np.array([0, 1, 31, 37, 64, 128, 191, 200, 254, 255]), graph_steps=8)
+
+
+@pytest.mark.parametrize("L", [4, 32])
+def test_layer_sweep_fused_points(L):
+    """The layer-sweep points at the sweep's dims (H = 32, G = 8, d = 64,
+    n = 128) with the smallest and largest ring, batch 64, fused with a
+    workspace: 2L + 8 steps, eight sampled sequences."""
+    shape = wl.Mamba2Shape(B=64, H=32, G=8, d=64, n=128, L=L, in_dtype=wl.BF16)
+    run_fused_sampled(shape, wl.SEED_SWEEP + L, 2 * L + 8, np.array([0, 5, 17, 32, 40, 51, 62, 63]))
