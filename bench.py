@@ -67,6 +67,12 @@ def m2_fused_flush_extra_bytes(s: wl.Mamba2Shape) -> int:
     return 4 * s.H * s.d * s.n
 
 
+def m2_fused_fold_bytes(s: wl.Mamba2Shape, c: int) -> int:
+    """A flush of c entries folded into the next verify's S_0 stream: the S_0
+    write and the entries' read (S_0 itself is read for the verify anyway)."""
+    return 4 * s.H * s.d * s.n + c * m2_entry_bytes(s)
+
+
 def m2_baseline_bytes(s: wl.Mamba2Shape) -> int:
     e = 2 if s.in_dtype == wl.BF16 else 4
     return 8 * s.H * s.d * s.n + s.H * s.d * e + 2 * s.G * s.n * e + s.H * 4 + 4 * s.H * s.d
@@ -122,9 +128,9 @@ def measured_peaks():
 
 HEADLINE_SOURCES = ("decode_split.cu", "common.cuh", "kernels.cuh")  # the headline kernels and their headers
 # the capture the recorded DRAM traffic comes from (run after the same command without ncu exited 0)
-TRAFFIC_COMMAND = ("python bench.py --no-cpu-baseline --steps 64 --warmup 8 --e2e-steps 16 && "
-                   "ncu --set full --import-source no --clock-control none -k regex:\"m2_(prep|stream)_kernel\" -s 8 -c 2 "
-                   "-o prof python bench.py --no-cpu-baseline --steps 64 --warmup 8 --e2e-steps 16")
+HEADLINE_SMALL = "python bench.py --no-cpu-baseline --no-extra --windows 1 --steps 64 --warmup 8 --e2e-steps 16"
+TRAFFIC_COMMAND = (f"{HEADLINE_SMALL} && ncu --set full --import-source no --clock-control none "
+                   f"-k regex:\"m2_(prep|stream)_kernel\" -s 8 -c 2 -o prof {HEADLINE_SMALL}")
 
 
 def source_digest(names=None) -> str:
@@ -264,6 +270,53 @@ def oracle_throughput(seconds: float = 12.0, seqs_per_worker: int = 2):
 # ---------------------------------------------------------------------------
 
 
+def workload_config(world: int) -> dict:
+    """The benchmarked workload, shared by both arms of the benchmark."""
+    s = wl.NEMOTRON_H_MAMBA2
+    return {"workload": WORKLOAD, "batch_per_gpu": s.B, "H": s.H, "G": s.G, "d": s.d, "n": s.n, "L": s.L,
+            "inputs": "bf16 v/k/q, f32 dt/A, f32 S_0", "fill": "random 0..15 at start",
+            "l2": "inputs larger than L2 (S_0 is 256 MiB per GPU; no L2 flush)",
+            "parallelism": f"replicas x{world} (independent batches, no collective)"}
+
+
+STEP_DESCRIPTION = ("replay_decode_step_fused with the decode workspace: a precompute launch and an S_0 streaming "
+                    "launch (programmatic dependent launch) that also folds full buffers; the K steps of a window "
+                    "are captured once in a CUDA graph and the graph is replayed, as a serving loop does")
+
+
+def graph_windows(step, K: int, reps: int, world: int, dev, sync_ranks):
+    """Capture step(t), t = 0..K-1, in one CUDA graph on a side stream, replay
+    it once untimed, then `reps` timed windows of exactly K steps, each
+    bracketed by a barrier and a device synchronisation, timed with CUDA
+    events on the replaying stream; returns each window's milliseconds, the
+    maximum over ranks."""
+    import torch
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for t in range(K):
+            step(t)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    out = []
+    for _ in range(reps):
+        sync_ranks()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(max_over_ranks(e0.elapsed_time(e1), dev))
+    del g
+    return out
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -275,6 +328,10 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+
+    def sync_ranks():
+        if world > 1:
+            dist.barrier()
 
     # the oracle baseline runs before the first CUDA work of this process
     cpu = None
@@ -306,24 +363,21 @@ def run_gpu(args):
     y = torch.empty(shape.B, shape.H, shape.d, device=dev)
     stream = torch.cuda.current_stream()
 
-    W, K = args.warmup, args.steps
-    total_steps = W + K
-    trace = fill_trace(init.count, shape.L, total_steps + W + K)
+    W, K, REPS = args.warmup, args.steps, args.windows
+    # steps run in order: W warm-up, one eager window of K, the graph's untimed
+    # replay of K, then REPS timed windows of K
+    trace = fill_trace(init.count, shape.L, W + K * (2 + REPS))
+    per_h = np.array([m2_decode_bytes(shape, h) for h in range(shape.L)], dtype=np.int64)
 
-    def step(t, inp):
-        R.replay_decode_step_fused(state, *inp, A, y=y)
+    def window_bytes(first):
+        h = trace[first:first + K]
+        return int(per_h[h].sum()) + int((h + 1 == shape.L).sum()) * m2_fused_flush_extra_bytes(shape)
 
     for t in range(W):
-        step(t, dev_in[t % POOL])
+        R.replay_decode_step_fused(state, *dev_in[t % POOL], A, y=y)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    sync_ranks()
 
-    # timed region: K steps, events around every decode launch
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    dec_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    dec_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     gpu_index = None
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis and vis.split(",")[local_rank].strip().isdigit():
@@ -331,93 +385,87 @@ def run_gpu(args):
     elif vis is None:
         gpu_index = local_rank
     with ClockSampler(gpu_index) as clk:
+        # one window with every step launched from the host through the public call
         torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
         for t in range(K):
-            inp = dev_in[(W + t) % POOL]
-            dec_a[t].record(stream)
-            R.replay_decode_step_fused(state, *inp, A, y=y)
-            dec_b[t].record(stream)
+            R.replay_decode_step_fused(state, *dev_in[(W + t) % POOL], A, y=y)
         ev1.record(stream)
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    dec_ms = [a.elapsed_time(b) for a, b in zip(dec_a, dec_b)]
+        eager_ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
+        # the headline: the same steps captured once, replayed as timed windows of K steps
+        first = W + K
+        win_ms = graph_windows(lambda t: R.replay_decode_step_fused(state, *dev_in[(first + t) % POOL], A, y=y),
+                               K, REPS, world, dev, sync_ranks)
+    sync_ranks()
     clocks = clk.summary()
-    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     err = int(state.err.item())
+    win_bytes = [window_bytes(W + K * (2 + r)) for r in range(REPS)]
+    order = np.argsort(win_ms)
+    med = int(order[len(order) // 2])
+    elapsed_ms = win_ms[med]
+    step_bytes = win_bytes[med] / K
+    achieved = step_bytes / (elapsed_ms / K * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    value = whole_job_throughput(shape.B * K, world, elapsed_ms)
+    flushed_share = (win_bytes[med] - int(per_h[trace[W + K * (2 + med):W + K * (3 + med)]].sum())) / win_bytes[med]
 
-    # algorithmic bytes of the timed launches (decode + fused flush)
-    h_timed = trace[W:W + K]
-    per_h = np.array([m2_decode_bytes(shape, h) for h in range(shape.L)], dtype=np.int64)
-    dec_bytes_total = int(per_h[h_timed].sum())
-    flushed = int((h_timed + 1 == shape.L).sum())
-    step_bytes_total = dec_bytes_total + flushed * m2_fused_flush_extra_bytes(shape)
-    dec_avg_ms = float(np.mean(dec_ms))
-    dec_bytes_per_launch = step_bytes_total / K
-
-    # the same steps as two launches: decode step, then the separate flush
+    # the same steps as two calls: decode step, then the separate flush
     for t in range(W):
         R.replay_decode_step(state, *dev_in[t % POOL], A, y=y)
         R.replay_flush(state, A)
     torch.cuda.synchronize()
-    u0 = torch.cuda.Event(enable_timing=True)
-    u1 = torch.cuda.Event(enable_timing=True)
-    u0.record(stream)
-    for t in range(K):
-        R.replay_decode_step(state, *dev_in[(W + t) % POOL], A, y=y)
+
+    def unfused(t):
+        R.replay_decode_step(state, *dev_in[t % POOL], A, y=y)
         R.replay_flush(state, A)
-    u1.record(stream)
-    torch.cuda.synchronize()
-    unfused_ms = u0.elapsed_time(u1) / K
-    peak, peak_kind = measured_peaks()
-    achieved = dec_bytes_per_launch / (dec_avg_ms * 1e-3) / 1e9
 
-    value = whole_job_throughput(shape.B * K, world, elapsed_ms)
+    unfused_ms = statistics.median(graph_windows(unfused, K, REPS, world, dev, sync_ranks)) / K
 
-    # baseline kernel on the same inputs (reads + writes the whole state)
+    # baseline kernel on the same inputs (reads + writes the whole state), timed the same way
     S = to(init.S0)
     for t in range(W):
         R.ssm_state_update_baseline(S, *dev_in[t % POOL], A, y=y)
     torch.cuda.synchronize()
-    b0 = torch.cuda.Event(enable_timing=True)
-    b1 = torch.cuda.Event(enable_timing=True)
-    b0.record(stream)
-    for t in range(K):
-        R.ssm_state_update_baseline(S, *dev_in[(W + t) % POOL], A, y=y)
-    b1.record(stream)
-    torch.cuda.synchronize()
-    base_ms = b0.elapsed_time(b1) / K
+    base_ms = statistics.median(graph_windows(
+        lambda t: R.ssm_state_update_baseline(S, *dev_in[t % POOL], A, y=y), K, REPS, world, dev, sync_ranks)) / K
     base_gbs = m2_baseline_bytes(shape) * shape.B / (base_ms * 1e-3) / 1e9
     del S
 
-    # end to end through the public calls with host buffers: H2D inputs, step, D2H y
+    # end to end through the public call with host buffers: H2D inputs, step, D2H y
     y_host = torch.empty(shape.B, shape.H, shape.d, dtype=torch.float32).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in host_in[0])
     d2h = y_host.numel() * y_host.element_size()
     staging = [tuple(torch.empty_like(x, device=dev) for x in host_in[0]) for _ in range(2)]
     Ke = min(K, args.e2e_steps)
-    for t in range(W):
+
+    def e2e_step(t):
         buf = staging[t % 2]
         for dst, src in zip(buf, host_in[t % POOL]):
             dst.copy_(src, non_blocking=True)
-        step(t, buf)
+        R.replay_decode_step_fused(state, *buf, A, y=y)
         y_host.copy_(y, non_blocking=True)
+
+    for t in range(W):
+        e2e_step(t)
     torch.cuda.synchronize()
+    sync_ranks()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for t in range(Ke):
-        buf = staging[t % 2]
-        for dst, src in zip(buf, host_in[(W + t) % POOL]):
-            dst.copy_(src, non_blocking=True)
-        step(t, buf)
-        y_host.copy_(y, non_blocking=True)
+        e2e_step(W + t)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = whole_job_throughput(shape.B * Ke, world, e2e_ms)
+
+    # the speculative (B = 512, T = 4) and GDN (B = 256) workloads, short graph-timed runs
+    extra = {}
+    if not args.no_extra:
+        extra = extra_workloads(R, peak)
 
     if rank == 0:
         traffic = recorded_traffic("m2_prep_kernel<fused>", "m2_stream_kernel<fused>")
@@ -434,21 +482,20 @@ def run_gpu(args):
             "vs_baseline": None,
             "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch_per_gpu": shape.B, "H": shape.H, "G": shape.G, "d": shape.d,
-                       "n": shape.n, "L": shape.L, "inputs": "bf16 v/k/q, f32 dt/A, f32 S_0",
-                       "fill": "random 0..15 at start",
-                       "step": "replay_decode_step_fused with the decode workspace: a precompute launch "
-                               "and an S_0 streaming launch that also folds full buffers",
-                       "l2": "inputs larger than L2 (S_0 is 256 MiB per GPU; no L2 flush)",
-                       "parallelism": f"replicas x{world} (independent batches, no collective)"},
-            "hbm_gbs_step": step_bytes_total / (elapsed_ms * 1e-3) / 1e9,
+            "config": workload_config(world),
+            "step": STEP_DESCRIPTION,
+            "windows": {"count": REPS, "steps_each": K, "reported": "median window",
+                        "ms": win_ms, "median_ms": elapsed_ms, "min_ms": min(win_ms), "max_ms": max(win_ms)},
+            "hbm_gbs_step": achieved,
             "roofline": {"bound": "hbm",
                          "kernel": "one decode step: m2_prep_kernel<fused> + m2_stream_kernel<fused> "
                                    "(replay_decode_step_fused), timed together",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_kind": peak_kind, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": dec_bytes_per_launch,
-                         "avg_launch_ms": dec_avg_ms},
+                         "algorithmic_bytes_per_launch": step_bytes,
+                         "avg_launch_ms": elapsed_ms / K},
+            "eager_window": {"calls": "every step launched from the host through the public call",
+                             "ms_per_step": eager_ms / K, "tokens_per_s": shape.B * world / (eager_ms / K * 1e-3)},
             "baseline_kernel": {"name": "ssm_state_update_baseline", "ms_per_step": base_ms,
                                 "tokens_per_s": shape.B * world / (base_ms * 1e-3), "gbs": base_gbs,
                                 "frac": base_gbs / peak},
@@ -456,17 +503,50 @@ def run_gpu(args):
             "unfused_two_launch_step": {"calls": "replay_decode_step + replay_flush", "ms_per_step": unfused_ms,
                                         "tokens_per_s": shape.B * world / (unfused_ms * 1e-3),
                                         "replay_over_baseline": base_ms / unfused_ms},
-            "flush_share_bytes": flushed * m2_fused_flush_extra_bytes(shape) / step_bytes_total,
+            "flush_share_bytes": flushed_share,
+            **extra,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": Ke},
+                    "steps": Ke, "calls": "replay_decode_step_fused launched from the host each step"},
             "gpu_launches": LAUNCHES_PER_STEP * K,
+            "gpu_launches_note": "per timed window of K steps (precompute + stream per step)",
             "clocks": clocks,
             "device_error_word": err,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def extra_workloads(R, peak) -> dict:
+    """Keys for the speculative workload (Mamba-2 layer, B = 512, T = 4) and
+    the GDN layer (B = 256; decode and T = 4 verify), from short CUDA-graph
+    timed runs of the window sweep restricted to T = 4."""
+    rows = suite_sweep(R, peak, steps=4, Ts=(4,), emit=False)
+    m2 = next(r for r in rows if r["model"] == "mamba2")
+    gd = next(r for r in rows if r["model"] == "gdn")
+    return {
+        "spec_round_b512_t4": {
+            "workload": m2["workload"], "calls": m2["calls"],
+            "timing": m2["timing"], "rounds": m2["rounds"], "ms_per_round": m2["ms_per_round"],
+            "unfused_ms_per_round": m2["unfused_ms_per_round"],
+            "unfused_calls": "replay_spec_verify + replay_spec_commit + replay_flush",
+            "gbs": m2["gbs"], "frac": m2["frac_of_peak"], "accepted_tokens_per_s": m2["accepted_tokens_per_s"],
+            "snapshot_baseline_ms_per_round": m2["baseline_ms_per_round"],
+            "replay_over_snapshot": m2["replay_over_baseline"], "round_over_decode": m2["round_over_decode"],
+            "device_error_word": m2["device_error_word"]},
+        "gdn_b256": {
+            "workload": "GDN layer B=256, Hv=32, Hk=16, d_k=d_v=128, L=16, u f32",
+            "decode_fused_ms_per_step": gd["decode_step_ms"], "decode_gbs": gd["decode_gbs"],
+            "decode_frac": gd["decode_gbs"] / peak,
+            "baseline_decode_ms_per_step": gd["baseline_decode_step_ms"],
+            "decode_replay_over_baseline": gd["baseline_decode_step_ms"] / gd["decode_step_ms"],
+            "verify_t4_ms_per_round": gd["ms_per_round"], "verify_round_over_decode": gd["round_over_decode"],
+            "verify_gbs": gd["gbs"], "verify_frac": gd["frac_of_peak"],
+            "snapshot_baseline_ms_per_round": gd["baseline_ms_per_round"],
+            "verify_replay_over_snapshot": gd["replay_over_baseline"],
+            "device_error_word": gd["device_error_word"]},
+    }
 
 
 def run_reference(args):
@@ -500,9 +580,8 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch_per_gpu": wl.NEMOTRON_H_MAMBA2.B, "H": 32, "G": 8, "d": 64, "n": 128,
-                   "L": 16, "step": "oracle decode step + flush (fp64, CPU)",
-                   "parallelism": "host cores"},
+        "config": workload_config(world),
+        "step": "oracle decode step + flush (fp64, CPU, host cores)",
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {cores} spawned processes x 1 sequence for {per_step:.1f} s"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -617,27 +696,41 @@ def _dev(x, dt=None):
 
 def suite_layers(R, peak, steps=None):
     """Layer-stack sweep: 23 independent Nemotron-H Mamba-2 layers per step,
-    batch B and ring capacity L swept; fused decode step per layer.  The
-    23-layer step is captured in a CUDA graph (as a serving loop would), so
-    small batches measure the GPU rather than host launch overhead; byte
-    accounting follows each sequence's fill level through the replays."""
+    batch B in {1, 8, 64, 256, 512} and ring capacity L in {4, 8, 16, 32}
+    (the buffer-capacity trade-off of "Results -- standard decoding", Fig. 7).
+    Every variant of a point is a 23-layer step captured in a CUDA graph of 16
+    steps (as a serving loop would), replayed until 512 steps are timed; byte
+    accounting follows each sequence's fill level through the replays.
+    Variants: the fused decode step with a workspace (the reported one), the
+    same without a workspace (one launch per layer), the decode step plus a
+    separate replay_flush, the decode step alone with every layer's counts
+    restored after each step (no buffer ever fills, same mean fill: what the
+    step costs without any flush), and the baseline state update.  The flush
+    cost share of a point is (decode + flush - decode alone) / (decode +
+    flush), and for the fused step (fused - decode alone) / fused, next to
+    the share of the bytes the flush moves.  A last line names the best L
+    per batch."""
     import torch
 
     LAYERS, out = 23, []
+    K, W = 16, 3
+    reps = max(1, (steps or 512) // K)
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    best = {}
     for bi, B in enumerate((1, 8, 64, 256, 512)):
         base_ms = None
         for li, L in enumerate((4, 8, 16, 32)):
             shape = wl.Mamba2Shape(B=B, H=32, G=8, d=64, n=128, L=L, in_dtype=wl.BF16)
             seed = wl.SEED_SWEEP + 100 * (bi * 4 + li)
-            layers, counts0 = [], []
+            layers = []
+            count_all = torch.empty(LAYERS, B, dtype=torch.int32, device="cuda")
             for layer in range(LAYERS):
                 t = wl.mamba2_state_tensors_device(shape, seed + layer, "cuda")
+                count_all[layer].copy_(t["count"])
                 z = lambda n: torch.zeros(n, dtype=torch.int32, device="cuda")  # noqa: E731
-                st = R.Mamba2State(t["S0"], t["ring_v"], t["ring_k"], t["ring_dt"], t["start"], t["count"], z(B),
-                                   z(B), z(1)).add_workspace()
+                st = R.Mamba2State(t["S0"], t["ring_v"], t["ring_k"], t["ring_dt"], t["start"], count_all[layer],
+                                   z(B), z(B), z(1)).add_workspace()
                 layers.append((st, t["A"]))
-                counts0.append(t["count"].cpu().numpy())
             g = torch.Generator(device="cuda")
             g.manual_seed(seed + 999)
             pool = [(torch.randn(B, 32, 64, generator=g, device="cuda").to(torch.bfloat16),
@@ -646,24 +739,52 @@ def suite_layers(R, peak, steps=None):
                      torch.nn.functional.softplus(torch.randn(B, 32, generator=g, device="cuda")))
                     for _ in range(4)]
             y = torch.empty(B, 32, 64, device="cuda")
+            per_h = np.array([m2_decode_bytes(shape, h) for h in range(L)], dtype=np.int64)
+            steps_run = 1 + K * (W + reps)  # _time_graph: one eager call, then W + reps replays of K
 
-            def step(i):
+            def timed_trace():
+                """Fill levels of the timed steps, from every layer's counts now."""
+                c = count_all.cpu().numpy()
+                return [fill_trace(c[layer], L, steps_run)[-reps * K:] for layer in range(LAYERS)]
+
+            def fused(i):
                 for st, A in layers:
                     R.replay_decode_step_fused(st, *pool[i % 4], A, y=y)
 
-            K, W, reps = 16, 3, 8
-            ms = _time_graph(step, K, W, reps)
-            per_h = np.array([m2_decode_bytes(shape, h) for h in range(L)], dtype=np.int64)
-            nbytes = 0
-            for c0 in counts0:  # capture ran one eager step first, then W + reps replays of K steps
-                tr = fill_trace(c0, L, 1 + K * (W + reps))[1 + K * W:]
-                nbytes += int(per_h[tr].sum()) + int((tr + 1 == L).sum()) * m2_fused_flush_extra_bytes(shape)
-            nbytes = nbytes / reps
+            trs = timed_trace()
+            ms = _time_graph(fused, K, W, reps)
+            dec_b = sum(int(per_h[tr].sum()) for tr in trs) / (reps * K)
+            fold_b = sum(int((tr + 1 == L).sum()) for tr in trs) * m2_fused_flush_extra_bytes(shape) / (reps * K)
+            nbytes = dec_b + fold_b
+
+            def pair(i):
+                for st, A in layers:
+                    R.replay_decode_step(st, *pool[i % 4], A, y=y)
+                    R.replay_flush(st, A)
+
+            trs = timed_trace()
+            pair_ms = _time_graph(pair, K, W, reps)
+            pair_flush_b = sum(int((tr + 1 == L).sum()) for tr in trs) * m2_flush_bytes(shape, L) / (reps * K)
+            pair_dec_b = sum(int(per_h[tr].sum()) for tr in trs) / (reps * K)
+
+            count0 = count_all.clone()
+
+            def frozen(i):
+                for st, A in layers:
+                    R.replay_decode_step(st, *pool[i % 4], A, y=y)
+                count_all.copy_(count0)
+
+            def restore_only(i):
+                count_all.copy_(count0)
+
+            dec_ms = _time_graph(frozen, K, W, reps) - _time_graph(restore_only, K, W, reps)
+            for st, _ in layers:  # flags the frozen steps left: a full buffer flags every step
+                st.flag.zero_()
             # the same step without a workspace: one launch per layer
             works = [st.work for st, _ in layers]
             for st, _ in layers:
                 st.work = None
-            one_ms = _time_graph(step, K, W, reps)
+            one_ms = _time_graph(fused, K, W, reps)
             for (st, _), wkt in zip(layers, works):
                 st.work = wkt
             err = max(int(st.err.item()) for st, _ in layers)
@@ -676,19 +797,30 @@ def suite_layers(R, peak, steps=None):
 
                 base_ms = _time_graph(bstep, K, W, reps)
                 del Ss
-            gbs = nbytes / K / (ms * 1e-3) / 1e9
-            out.append({"suite": "layers", "workload": f"{LAYERS} Mamba-2 layers (H=32, G=8, d=64, n=128), B={B}, L={L}",
-                        "B": B, "L": L, "layers": LAYERS, "steps": K * reps, "timing": "CUDA graph of 16 steps",
-                        "ms_per_step": ms,
-                        "tokens_per_s": B / (ms * 1e-3), "gbs": gbs, "frac_of_peak": gbs / peak,
-                        "one_launch_ms_per_step": one_ms,
-                        "baseline_ms_per_step": base_ms, "replay_over_baseline": base_ms / ms,
-                        "state_bytes": LAYERS * B * 32 * 64 * 128 * 4,
-                        "state_fits_l2": LAYERS * B * 32 * 64 * 128 * 4 <= l2, "device_error_word": err})
-            print(json.dumps(out[-1]), flush=True)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            line = {"suite": "layers", "workload": f"{LAYERS} Mamba-2 layers (H=32, G=8, d=64, n=128), B={B}, L={L}",
+                    "B": B, "L": L, "layers": LAYERS, "steps": K * reps,
+                    "timing": f"CUDA graph of {K} steps, {reps} replays timed",
+                    "ms_per_step": ms, "tokens_per_s": B / (ms * 1e-3), "gbs": gbs, "frac_of_peak": gbs / peak,
+                    "decode_plus_flush_ms_per_step": pair_ms, "decode_alone_ms_per_step": dec_ms,
+                    "flush_cost_share": (pair_ms - dec_ms) / pair_ms,
+                    "flush_byte_share": pair_flush_b / (pair_dec_b + pair_flush_b),
+                    "fused_fold_cost_share": (ms - dec_ms) / ms,
+                    "fused_fold_byte_share": fold_b / nbytes,
+                    "one_launch_ms_per_step": one_ms,
+                    "baseline_ms_per_step": base_ms, "replay_over_baseline": base_ms / ms,
+                    "state_bytes": LAYERS * B * 32 * 64 * 128 * 4,
+                    "state_fits_l2": LAYERS * B * 32 * 64 * 128 * 4 <= l2, "device_error_word": err}
+            out.append(line)
+            print(json.dumps(line), flush=True)
+            if B not in best or line["tokens_per_s"] > best[B]["tokens_per_s"]:
+                best[B] = line
             del layers, pool
             torch.cuda.empty_cache()
-    return out
+    summary = {"suite": "layers_best_L", "best_L_per_B": {str(B): r["L"] for B, r in best.items()},
+               "tokens_per_s_at_best": {str(B): r["tokens_per_s"] for B, r in best.items()}}
+    print(json.dumps(summary), flush=True)
+    return out + [summary]
 
 
 def _spec_pool(shape, seed, T, n):
@@ -926,7 +1058,7 @@ def spec_trace(count0: np.ndarray, accs: list, T: int, L: int):
 SWEEP_ROUNDS = 8  # rounds captured per CUDA graph (each with its own inputs and accepted counts)
 
 
-def suite_sweep(R, peak, steps=None):
+def suite_sweep(R, peak, steps=None, Ts=range(1, 7), emit=True):
     """Speculative rounds against the window T = 1..6 (the shape of "Results --
     speculative decoding", Fig. 9): each round is verify + device commit +
     flush of the early-flagged sequences, captured in a CUDA graph with the
@@ -952,7 +1084,10 @@ def suite_sweep(R, peak, steps=None):
             dinp = [tuple(x[:, 0].contiguous() for x in wl.mamba2_round_device(shape, 50 + i, 1, "cuda"))
                     for i in range(K)]
             y1 = torch.empty(shape.B, shape.H, shape.d, device="cuda")
+            c0 = dst.count.cpu().numpy()
             dec_ms = _time_graph(lambda i: R.replay_decode_step_fused(dst, *dinp[i % K], A, y=y1), K, W, reps)
+            per_h = np.array([m2_decode_bytes(shape, h) for h in range(shape.L)], dtype=np.int64)
+            fold_extra = m2_fused_flush_extra_bytes(shape)
             Sb = t["S0"].clone()
             base_dec_ms = _time_graph(lambda i: R.ssm_state_update_baseline(Sb, *dinp[i % K], A, y=y1), K, W, reps)
             del dst, Sb
@@ -965,12 +1100,19 @@ def suite_sweep(R, peak, steps=None):
             dinp = [tuple(x[:, 0].contiguous() for x in wl.gdn_round_device(shape, 50 + i, 1, "cuda"))
                     for i in range(K)]
             y1 = torch.empty(shape.B, shape.Hv, shape.dv, device="cuda")
+            c0 = dst.count.cpu().numpy()
             dec_ms = _time_graph(lambda i: R.gdn_replay_decode_fused(dst, *dinp[i % K], y=y1), K, W, reps)
+            per_h = np.array([gdn_decode_bytes(shape, h) for h in range(shape.L)], dtype=np.int64)
+            fold_extra = 4 * shape.Hv * shape.dv * shape.dk
             Sb = t["S0"].clone()
             base_dec_ms = _time_graph(lambda i: R.gdn_state_update_baseline(Sb, *dinp[i % K], y=y1), K, W, reps)
             del dst, Sb
         torch.cuda.empty_cache()
-        for T in range(1, 7):
+        # decode steps run: one eager, then W + reps replays of K; the last reps x K are timed
+        tr = fill_trace(c0, shape.L, 1 + K * (W + reps))[-reps * K:]
+        dec_gbs = (int(per_h[tr].sum()) + int((tr + 1 == shape.L).sum()) * fold_extra) / (reps * K) / \
+            (dec_ms * 1e-3) / 1e9
+        for T in Ts:
             fill = dict(fill_max=shape.L - T)
             accs = [wl.accepted_counts_device(shape.B, T, 900 + 10 * T + i, "cuda") for i in range(K)]
             if model == "mamba2":
@@ -981,12 +1123,17 @@ def suite_sweep(R, peak, steps=None):
                 y = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
 
                 def rnd(i):
+                    R.replay_spec_verify_fused(st, *inp[i % K], A, y=y)
+                    R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
+
+                def rnd_unfused(i):
                     R.replay_spec_verify(st, *inp[i % K], A, y=y)
                     R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
                     R.replay_flush(st, A)
 
                 vb = lambda h: m2_verify_bytes(shape, h, T)  # noqa: E731
-                fb = lambda c: m2_flush_bytes(shape, c)  # noqa: E731
+                fb = lambda c: m2_fused_fold_bytes(shape, c)  # noqa: E731
+                calls = "replay_spec_verify_fused + replay_spec_commit"
                 snap_round_bytes = m2_snapshot_verify_bytes(shape, T) * shape.B
                 slot_shape = (shape.B, T + 1, shape.H, shape.d, shape.n)
             else:
@@ -1001,17 +1148,29 @@ def suite_sweep(R, peak, steps=None):
                     R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
                     R.gdn_replay_flush(st)
 
+                rnd_unfused = None
                 vb = lambda h: gdn_verify_bytes(shape, h, T)  # noqa: E731
                 fb = lambda c: gdn_flush_bytes(shape, c)  # noqa: E731
+                calls = "gdn_replay_verify + replay_spec_commit + gdn_replay_flush"
                 snap_round_bytes = gdn_snapshot_verify_bytes(shape, T) * shape.B
                 slot_shape = (shape.B, T + 1, shape.Hv, shape.dv, shape.dk)
             count0 = st.count.cpu().numpy()
             acc_h = [a.cpu().numpy() for a in accs]
             ms = _time_graph(rnd, K, W, reps)
             err = int(st.err.item())
+            unfused_ms = None
+            if rnd_unfused is not None:
+                R.replay_flush(st, A)  # the fused rounds leave their last flags pending
+                unfused_ms = _time_graph(rnd_unfused, K, W, reps)
+                err |= int(st.err.item())
             # rounds run: one eager, then W + reps replays of the K captured rounds; the last reps x K are timed
             seq = [acc_h[0]] + [acc_h[i] for _ in range(W + reps) for i in range(K)]
             hs, folds = spec_trace(count0, seq, T, shape.L)
+            if rnd_unfused is not None:
+                # a fused round folds what the previous round flagged, and verifies from
+                # the emptied window; the rounds' fill levels are the same
+                folds = [np.full_like(folds[0], -1)] + folds[:-1]
+                hs = [np.where(f >= 0, 0, h) for h, f in zip(hs, folds)]
             per_h = {x: vb(x) for x in range(shape.L + 1)}
             per_c = {x: fb(x) for x in range(shape.L + 1)}
             nbytes = 0
@@ -1040,16 +1199,18 @@ def suite_sweep(R, peak, steps=None):
             line = {"suite": "sweep", "model": model,
                     "workload": (f"Mamba-2 layer B={shape.B}, H=32, G=8, d=64, n=128" if model == "mamba2" else
                                  f"GDN layer B={shape.B}, Hv=32, Hk=16, d_k=d_v=128") + f", L=16, T={T}",
-                    "T": T, "rounds": reps * K, "timing": f"CUDA graph of {K} rounds (verify + commit + flush)",
+                    "T": T, "rounds": reps * K, "timing": f"CUDA graph of {K} rounds", "calls": calls,
                     "ms_per_round": ms, "accepted_tokens_per_s": shape.B * mean_acc / (ms * 1e-3),
+                    "unfused_ms_per_round": unfused_ms,
                     "gbs": gbs, "frac_of_peak": gbs / peak,
-                    "decode_step_ms": dec_ms, "round_over_decode": ms / dec_ms,
+                    "decode_step_ms": dec_ms, "decode_gbs": dec_gbs, "round_over_decode": ms / dec_ms,
                     "baseline_ms_per_round": bms, "baseline_decode_step_ms": base_dec_ms,
                     "baseline_round_over_decode": bms / base_dec_ms,
                     "baseline_gbs": snap_round_bytes / (bms * 1e-3) / 1e9,
                     "replay_over_baseline": bms / ms, "device_error_word": err}
             out.append(line)
-            print(json.dumps(line), flush=True)
+            if emit:
+                print(json.dumps(line), flush=True)
             del slots, inp, y
             torch.cuda.empty_cache()
     return out
@@ -1206,8 +1367,13 @@ def record_traffic(report: str, command: str):
     import csv
     import io
 
-    out = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], capture_output=True, text=True, check=True)
-    rows = list(csv.reader(io.StringIO(out.stdout)))
+    if report.endswith(".csv"):  # the raw page already exported (ncu -i REPORT --page raw --csv)
+        with open(report) as f:
+            text = f.read()
+    else:
+        text = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], capture_output=True, text=True,
+                              check=True).stdout
+    rows = list(csv.reader(io.StringIO(text)))
     head, units = rows[0], rows[1]
     col = {n: i for i, n in enumerate(head)}
 
@@ -1237,6 +1403,99 @@ def record_traffic(report: str, command: str):
     print(json.dumps(rec, indent=1))
 
 
+def suite_kernels(R, peak, steps=None):
+    """A few eager calls of every hot kernel at its benchmark workload, one
+    JSON line each with the mean milliseconds per call: the command the ncu
+    captures of single kernels run (one kernel per capture, selected with
+    -k).  Mamba-2 baseline and fused decode (B = 256), the speculative round
+    at B = 512, T = 4 (verify, commit, flush: the tensor-core flush), the
+    tensor-core Mamba-2 verify (B = 512, T = 6), the round with the flush
+    fused into the verify (B = 512, T = 4), the GDN baseline and fused
+    decode (B = 256) and the GDN T = 4 round (tensor-core verify, flush)."""
+    import torch
+
+    n = steps or 3
+    z = lambda k: torch.zeros(k, dtype=torch.int32, device="cuda")  # noqa: E731
+
+    def timed(name, fn):
+        fn(0)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            fn(1 + i)
+        e1.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"suite": "kernels", "workload": name, "calls": n, "ms_per_call": e0.elapsed_time(e1) / n}),
+              flush=True)
+
+    def m2(shape, seed, T=None):
+        t = wl.mamba2_state_tensors_device(shape, seed, "cuda", fill_max=None if T is None else shape.L - T)
+        st = R.Mamba2State(t["S0"], t["ring_v"], t["ring_k"], t["ring_dt"], t["start"], t["count"], z(shape.B),
+                           z(shape.B), z(1)).add_workspace(max_T=T or 0)
+        return st, t["A"]
+
+    shape = wl.NEMOTRON_H_MAMBA2
+    st, A = m2(shape, 11)
+    inp = [tuple(x[:, 0].contiguous() for x in wl.mamba2_round_device(shape, 20 + i, 1, "cuda")) for i in range(4)]
+    y = torch.empty(shape.B, shape.H, shape.d, device="cuda")
+    S = st.S0.clone()
+    timed("m2_baseline B=256", lambda i: R.ssm_state_update_baseline(S, *inp[i % 4], A, y=y))
+    timed("m2_decode_fused B=256", lambda i: R.replay_decode_step_fused(st, *inp[i % 4], A, y=y))
+    del st, S
+    shape = wl.SPEC_MAMBA2
+    for T in (4, 6):
+        st, A = m2(shape, 12 + T, T)
+        rin = [wl.mamba2_round_device(shape, 30 + i, T, "cuda") for i in range(4)]
+        acc = [wl.accepted_counts_device(shape.B, T, 40 + i, "cuda") for i in range(4)]
+        yv = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
+
+        def rnd(i, st=st, A=A, rin=rin, acc=acc, yv=yv, T=T):
+            R.replay_spec_verify(st, *rin[i % 4], A, y=yv)
+            R.replay_spec_commit(acc[i % 4], st.count, T, shape.L, st.err)
+            R.replay_flush(st, A)
+
+        timed(f"m2_spec_round B=512 T={T}", rnd)
+        del st
+    T = 4
+    st, A = m2(shape, 16, T)
+    rin = [wl.mamba2_round_device(shape, 80 + i, T, "cuda") for i in range(4)]
+    acc = [wl.accepted_counts_device(shape.B, T, 90 + i, "cuda") for i in range(4)]
+    yv = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
+
+    def frnd(i):
+        R.replay_spec_verify_fused(st, *rin[i % 4], A, y=yv)
+        R.replay_spec_commit(acc[i % 4], st.count, T, shape.L, st.err)
+
+    timed("m2_spec_round_fused B=512 T=4", frnd)
+    del st
+    shape = wl.GDN_LAYER
+    t = wl.gdn_state_tensors_device(shape, 13, "cuda")
+    st = R.GdnState(t["S0"], t["ring_u"], t["ring_k"], t["ring_g"], t["start"], t["count"], z(shape.B), z(shape.B),
+                    z(1)).add_workspace(4)
+    ginp = [tuple(x[:, 0].contiguous() for x in wl.gdn_round_device(shape, 50 + i, 1, "cuda")) for i in range(4)]
+    yg = torch.empty(shape.B, shape.Hv, shape.dv, device="cuda")
+    Sg = t["S0"].clone()
+    timed("gdn_baseline B=256", lambda i: R.gdn_state_update_baseline(Sg, *ginp[i % 4], y=yg))
+    timed("gdn_decode_fused B=256", lambda i: R.gdn_replay_decode_fused(st, *ginp[i % 4], y=yg))
+    del st, Sg, t
+    T = 4
+    t = wl.gdn_state_tensors_device(shape, 14, "cuda", fill_max=shape.L - T)
+    st = R.GdnState(t["S0"], t["ring_u"], t["ring_k"], t["ring_g"], t["start"], t["count"], z(shape.B), z(shape.B),
+                    z(1)).add_workspace(T)
+    vin = [wl.gdn_round_device(shape, 60 + i, T, "cuda") for i in range(4)]
+    acc = [wl.accepted_counts_device(shape.B, T, 70 + i, "cuda") for i in range(4)]
+    yv = torch.empty(shape.B, T, shape.Hv, shape.dv, device="cuda")
+
+    def grnd(i):
+        R.gdn_replay_verify(st, *vin[i % 4], y=yv)
+        R.replay_spec_commit(acc[i % 4], st.count, T, shape.L, st.err)
+        R.gdn_replay_flush(st)
+
+    timed("gdn_verify_round B=256 T=4", grnd)
+    return []
+
+
 def run_suite(args):
     import torch
 
@@ -1247,7 +1506,8 @@ def run_suite(args):
     names = args.suite.split(",")
     for name in names:
         {"layers": suite_layers, "spec": suite_spec, "gdn": suite_gdn, "sweep": suite_sweep,
-         "concurrency": suite_concurrency, "conv": suite_conv}[name](R, peak, args.suite_steps)
+         "concurrency": suite_concurrency, "conv": suite_conv, "kernels": suite_kernels}[name](R, peak,
+                                                                                              args.suite_steps)
 
 
 def main():
@@ -1259,9 +1519,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--windows", type=int, default=5,
+                    help="timed windows of --steps steps each; the line reports the median window")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="leave out the speculative and GDN keys of the headline line")
     ap.add_argument("--suite", default=None,
                     help="instead of the headline line, print one JSON line per measurement of the other "
-                         "workloads: comma-separated subset of layers,spec,gdn,sweep,concurrency,conv")
+                         "workloads: comma-separated subset of layers,spec,gdn,sweep,concurrency,conv,kernels")
     ap.add_argument("--suite-steps", type=int, default=None,
                     help="timed steps (rounds) per suite measurement instead of each suite's own count "
                          "(short runs for profiling; the layer sweep keeps its graph of 16 steps)")

@@ -31,7 +31,9 @@
  *  - Every wait inside a kernel is bounded (about one second) and sets
  *    RSSM_EBIT_TIMEOUT when it runs out.  In the precompute kernel of a
  *    two-launch call (a workspace is given) the affected sequence is skipped
- *    as a whole: its pointers, checkpoint, ring and outputs stay as they were.
+ *    as a whole: its pointers, checkpoint and committed ring entries stay as
+ *    they were (the outputs of its heads are undefined: each is either left
+ *    untouched or what the ordinary call writes).
  *    A wait that runs out in any other kernel leaves the affected sequences'
  *    outputs and state undefined: restore them from a checkpoint.  The
  *    environment variable RSSM_WAIT_LIMIT_NS (nanoseconds, read at every
@@ -95,6 +97,8 @@ typedef int32_t rssm_status;
 #define RSSM_EBIT_ACCEPTED 4    /* accepted outside [0, T] or count + accepted > L  */
 #define RSSM_EBIT_CUR 8         /* snapshot slot index outside [0, T]              */
 #define RSSM_EBIT_TIMEOUT 16    /* a bounded wait inside a pipelined kernel ran out */
+#define RSSM_EBIT_BOUNDS 32     /* an index check of the bounds-checked build
+                                   (compiled with -DRSSM_CHECKED) failed     */
 
 /* kinds of replay_seq_bytes / gdn_replay_seq_bytes */
 #define RSSM_SEQ_REPLAY 0   /* checkpoint S_0, ring buffer, pointers, workspace share */
@@ -176,7 +180,7 @@ RSSM_API rssm_status replay_decode_step(const rssm_m2_dims *dims, const rssm_m2_
 RSSM_API int64_t replay_decode_workspace_bytes(const rssm_m2_dims *dims);
 
 /* Bytes of the optional workspace for replay_spec_verify with up to T drafts:
- * B * H * 4 * ceil((16 + P d) / 4) with P = 1 for T = 1, 4 for T <= 4, 8 for
+ * B * H * 4 * ceil((48 + P d) / 4) with P = 1 for T = 1, 4 for T <= 4, 8 for
  * T <= 8.  0 for invalid arguments.  Host only.                               */
 RSSM_API int64_t replay_verify_workspace_bytes(const rssm_m2_dims *dims, int32_t T);
 
@@ -253,6 +257,24 @@ RSSM_API rssm_status replay_spec_verify(const rssm_m2_dims *dims, const rssm_m2_
                                const void *v, const void *k, const void *q, const float *dt,
                                const float *A, void *y, rssm_stream_t stream);
 
+/* Speculative verify with the pending flush fused in ("Algorithm -- speculative
+ * decoding", flush decision: the early flush that the previous round flagged):
+ * the same outputs and state as replay_flush followed by replay_spec_verify.
+ * A sequence whose flag is set has its c = count[b] committed entries folded
+ * into S_0 (S_0 <- abar S_0 + sum_j s_j v_j k_j^T) by the launch that streams
+ * S_0 for the drafts, from the tile it already holds; the round then starts
+ * from an empty window at start + c (start <- (start + c) mod L, count <- 0),
+ * and the flag is set again by the early-flush rule.  So a speculative round
+ * is this call and replay_spec_commit, with no separate flush: the flush that
+ * round r flags is carried out by round r + 1.  Requires st->sync (zero, left
+ * zero).  The fused launches apply with a workspace of
+ * replay_verify_workspace_bytes(dims, T) bytes, L a multiple of 4 and the
+ * CUDA-core verify stream (T <= 4 at d = 64, n = 128); otherwise the call
+ * runs the flush and then the verify.  Arguments as replay_spec_verify.      */
+RSSM_API rssm_status replay_spec_verify_fused(const rssm_m2_dims *dims, const rssm_m2_replay *st, int32_t T,
+                                              const void *v, const void *k, const void *q, const float *dt,
+                                              const float *A, void *y, rssm_stream_t stream);
+
 /* Device-side commit ("Supplementary design for CUDA Graphs", device commit):
  * count[b] += accepted[b] for b < B; rejected drafts are rolled back by not
  * moving the pointer over them.  accepted outside [0, T] or count + accepted > L
@@ -311,7 +333,7 @@ RSSM_API rssm_status gdn_replay_decode_fused(const rssm_gdn_dims *dims, const rs
                                              void *y, rssm_stream_t stream);
 
 /* Bytes of the optional GDN workspace (rssm_gdn_replay.work) for calls with
- * up to T drafts (T = 1 for decode): B * Hv * 4 * ceil((180 + 2 P dv) / 4)
+ * up to T drafts (T = 1 for decode): B * Hv * 4 * ceil((184 + 2 P dv) / 4)
  * with P = 1 for T = 1, 4 for T <= 4, 8 for T <= 8.  0 for invalid
  * arguments.  Host only.                                                      */
 RSSM_API int64_t gdn_replay_workspace_bytes(const rssm_gdn_dims *dims, int32_t T);
@@ -342,6 +364,21 @@ RSSM_API rssm_status gdn_replay_flush(const rssm_gdn_dims *dims, const rssm_gdn_
 RSSM_API rssm_status gdn_replay_verify(const rssm_gdn_dims *dims, const rssm_gdn_replay *st, int32_t T, const void *q,
                               const void *k, const void *v, const float *beta, const float *g, void *y,
                               rssm_stream_t stream);
+
+/* GDN chunked verify with the pending flush fused in: the same outputs and
+ * state as gdn_replay_flush followed by gdn_replay_verify.  A sequence whose
+ * flag is set has its c = count[b] committed entries folded into S_0
+ * (S_0 <- (prod alpha_j) S_0 + sum_j (prod_{i>j} alpha_i) u_j k_j^T) by the
+ * launch that streams S_0 for the drafts, from the block it already holds;
+ * the round then starts from an empty window at start + c.  A speculative
+ * round is this call and replay_spec_commit.  Requires st->sync (zero, left
+ * zero).  The fused launches apply with a workspace of
+ * gdn_replay_workspace_bytes(dims, T) bytes on the tensor-core verify
+ * (bf16 inputs, d_k = d_v = 128, 2 <= T); otherwise the call runs the flush
+ * and then the verify.  Arguments as gdn_replay_verify.                      */
+RSSM_API rssm_status gdn_replay_verify_fused(const rssm_gdn_dims *dims, const rssm_gdn_replay *st, int32_t T,
+                                             const void *q, const void *k, const void *v, const float *beta,
+                                             const float *g, void *y, rssm_stream_t stream);
 
 /* Baseline GDN speculative verify: serial correction-form updates per draft
  * with a full snapshot per draft (T+1 slots, as ssm_spec_verify_baseline).

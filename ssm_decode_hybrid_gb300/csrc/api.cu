@@ -387,6 +387,45 @@ rssm_status replay_spec_verify(const rssm_m2_dims *dims, const rssm_m2_replay *s
   return cuda_status(launch_m2(M2Kind::Verify, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+rssm_status replay_spec_verify_fused(const rssm_m2_dims *dims, const rssm_m2_replay *s, int32_t T, const void *v,
+                                     const void *k, const void *q, const float *dt, const float *A, void *y,
+                                     rssm_stream_t stream) {
+  rssm_status st = check_m2_dims(dims);
+  if (st) return st;
+  const rssm_m2_dims &d = *dims;
+  if (T < 1 || T > d.L) return RSSM_ERR_INVALID_ARG;
+  if (T > kMaxT) return RSSM_ERR_UNSUPPORTED;
+  if (!m2_replay_ok(d, s, true) || !ok_elem(v, d.in_dtype) || !ok16(k) || !ok16(q) || !ok4(dt) || !ok4(A) ||
+      !ok_elem(y, d.y_dtype))
+    return RSSM_ERR_INVALID_ARG;
+  M2Launch a = m2_launch(d);
+  a.T = T;
+  a.S = s->S0;
+  a.ring_v = s->ring_v;
+  a.ring_k = s->ring_k;
+  a.ring_dt = s->ring_dt;
+  a.start = s->start;
+  a.count = s->count;
+  a.flag = s->flag;
+  a.sync = s->sync;
+  a.err = s->err;
+  a.v = v;
+  a.k = k;
+  a.q = q;
+  a.dt = dt;
+  a.A = A;
+  a.y = y;
+  a.work = s->work;
+  a.work_bytes = s->work_bytes;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_m2(M2Kind::VerifyFused, a, cs);
+  if (e != cudaErrorNotSupported) return cuda_status(e);
+  // outside the fused kernels: the flush, then the verify
+  e = launch_flush(m2_flush_launch(d, s, A), cs);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_m2(M2Kind::Verify, a, cs));
+}
+
 rssm_status replay_spec_commit(int32_t B, int32_t T, int32_t L, const int32_t *accepted, int32_t *count,
                                int32_t *err, rssm_stream_t stream) {
   if (B < 1 || T < 1 || L < 1 || T > L || !ok4(accepted) || !ok4(count) || (err && !aligned(err, 4)))
@@ -565,6 +604,34 @@ rssm_status gdn_replay_verify(const rssm_gdn_dims *dims, const rssm_gdn_replay *
   a.g = g;
   a.y = y;
   return cuda_status(launch_gdn(GdnKind::Verify, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rssm_status gdn_replay_verify_fused(const rssm_gdn_dims *dims, const rssm_gdn_replay *s, int32_t T, const void *q,
+                                    const void *k, const void *v, const float *beta, const float *g, void *y,
+                                    rssm_stream_t stream) {
+  rssm_status st = check_gdn_dims(dims);
+  if (st) return st;
+  const rssm_gdn_dims &d = *dims;
+  if (T < 1 || T > d.L) return RSSM_ERR_INVALID_ARG;
+  if (T > kMaxT) return RSSM_ERR_UNSUPPORTED;
+  if (!gdn_replay_ok(d, s, true) || !ok16(q) || !ok16(k) || !ok_elem(v, d.in_dtype) || !ok4(beta) || !ok4(g) ||
+      !ok_elem(y, d.y_dtype))
+    return RSSM_ERR_INVALID_ARG;
+  GdnLaunch a = gdn_replay_launch(d, s);
+  a.T = T;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.beta = beta;
+  a.g = g;
+  a.y = y;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_gdn(GdnKind::VerifyFused, a, cs);
+  if (e != cudaErrorNotSupported) return cuda_status(e);
+  // outside the fused kernels: the flush, then the verify
+  e = launch_flush(gdn_flush_launch(d, s), cs);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_gdn(GdnKind::Verify, a, cs));
 }
 
 rssm_status gdn_spec_verify_baseline(const rssm_gdn_dims *dims, int32_t T, float *slots, const int32_t *cur,

@@ -100,6 +100,31 @@ __device__ __forceinline__ void set_err(int32_t *err, int bit) {
   if (err) atomicOr(err, bit);
 }
 
+// Bounds-checked build (compiled with -DRSSM_CHECKED; a stand-in for a memory
+// sanitizer, which this library's tests cannot run): every ring slot a kernel
+// writes and every pointer value it decodes from a workspace record is checked
+// against its extent.  A failed check ORs RSSM_EBIT_BOUNDS into the error
+// word; an item-level check (rssm_check) then skips the item, a slot check
+// (checked_slot) redirects the access to slot 0 of the same ring so that no
+// access leaves the caller's arrays.  Neither traps.  In the ordinary build
+// both compile to nothing.
+#ifdef RSSM_CHECKED
+__device__ __forceinline__ bool rssm_check(bool ok, int32_t *err) {
+  if (!ok) set_err(err, RSSM_EBIT_BOUNDS);
+  return ok;
+}
+__device__ __forceinline__ int checked_slot(int s, int L, int32_t *err) {
+  if (static_cast<unsigned>(s) >= static_cast<unsigned>(L)) {
+    set_err(err, RSSM_EBIT_BOUNDS);
+    return 0;
+  }
+  return s;
+}
+#else
+__device__ __forceinline__ bool rssm_check(bool, int32_t *) { return true; }
+__device__ __forceinline__ int checked_slot(int s, int, int32_t *) { return s; }
+#endif
+
 // Arrival counter of a sequence's thread blocks.  Every block of sequence b
 // calls this once, after it has read start/count/flag of b; it returns true
 // in exactly one block, the last to arrive, which may then rewrite the
@@ -251,14 +276,24 @@ __device__ __forceinline__ bool named_bar_or(int id, int threads, bool pred) {
 // word sits at float `info_off` and carries `valid_bit` when the block
 // finished.  A block that gave up (a wait that ran out, pointers out of range)
 // clears it, and every streaming block of that sequence then skips the
-// sequence.  Call with the whole warp; the answer is the same in every lane.
-__device__ __forceinline__ bool group_records_valid(const float *first, int groups, int hpg, int stride, int info_off,
-                                                    int valid_bit) {
+// sequence.  group_records_load issues this lane's loads (call it early: the
+// answer is needed only before the first write), group_records_valid combines
+// them over the warp (call with the whole warp; the same answer in every lane).
+__device__ __forceinline__ bool group_records_load(const float *first, int groups, int hpg, int stride, int info_off,
+                                                   int valid_bit) {
   const int lane = threadIdx.x & 31;
-  bool ok = true;
+  int all = valid_bit;
   for (int g = lane; g < groups; g += 32)
-    ok = ok && (reinterpret_cast<const int *>(first + static_cast<size_t>(g) * hpg * stride)[info_off] & valid_bit);
-  return __all_sync(kFull, ok);
+    all &= reinterpret_cast<const int *>(first + static_cast<size_t>(g) * hpg * stride)[info_off];
+  return all != 0;
+}
+__device__ __forceinline__ bool group_records_valid(bool lane_ok) { return __all_sync(kFull, lane_ok); }
+// Both at once, for a block about to change the sequence's state.  Not
+// inlined, and called where little else is live: the streaming kernels sit at
+// their register caps, and inlined its loads made them spill.
+static __device__ __noinline__ bool sequence_records_valid(const float *first, int groups, int hpg, int stride,
+                                                       int info_off, int valid_bit) {
+  return group_records_valid(group_records_load(first, groups, hpg, stride, info_off, valid_bit));
 }
 
 }  // namespace rssm

@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 4) m2_decode_flat_kernel(M2Launch a)
   // 3. y = abar (S_0 q) + sum_j c_j v_j with four threads per row; appended entry
   const float abar = s_abar;
   TO *y = static_cast<TO *>(a.y) + bh * d;
-  const int slot_new = (st + h) % L;
+  const int slot_new = checked_slot((st + h) % L, L, a.err);
   TI *rv_out = static_cast<TI *>(a.ring_v) + (bh * L + slot_new) * d;
   for (int rb = 0; rb < d; rb += kThreads / 4) {
     const int r = rb + (tid >> 2), part = tid & 3;

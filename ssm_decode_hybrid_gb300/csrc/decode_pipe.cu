@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) m2_decode_pipe_kernel(M2Launc
       named_bar(1 + gi, kGroupThreads);
       const float abar = sc.abar;
       const size_t bh = static_cast<size_t>(b) * H + i;
-      const int slot = wrap(st + h, L);
+      const int slot = checked_slot(wrap(st + h, L), L, a.err);
       TO *y = static_cast<TO *>(a.y) + bh * d;
       TI *rv_out = static_cast<TI *>(a.ring_v) + (bh * L + slot) * d;
       // two adjacent lanes per row, each summing every other entry

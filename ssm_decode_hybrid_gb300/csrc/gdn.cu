@@ -290,18 +290,18 @@ __global__ void __launch_bounds__(kThreads) gdn_replay_kernel(GdnLaunch a) {
         for (int mp = 0; mp < NT; ++mp)
           if (mp <= m) ym = fmaf(expf(Gm - s_G[mp]) * s_kx[mp][NT + m], u[mp], ym);
         store1(y + (tv0 + static_cast<size_t>(m) * a.Hv) * dv + r, ym);
-        store1(ru + static_cast<size_t>((st + h + m) % L) * dv + r, um);
+        store1(ru + static_cast<size_t>(checked_slot((st + h + m) % L, L, a.err)) * dv + r, um);
       } else {
         u[m] = 0.f;
       }
     }
   }
-  if (tid < T) a.ring_g[bh * L + (st + h + tid) % L] = a.g[tv0 + static_cast<size_t>(tid) * a.Hv];
+  if (tid < T) a.ring_g[bh * L + checked_slot((st + h + tid) % L, L, a.err)] = a.g[tv0 + static_cast<size_t>(tid) * a.Hv];
   if (i % HpK == 0) {
     TI *rk = static_cast<TI *>(a.ring_k) + bk * L * N;
     for (int idx = tid; idx < T * N; idx += kThreads) {
       const int m = idx / N, c = idx - m * N;
-      copy1(rk + static_cast<size_t>((st + h + m) % L) * N + c, kin + (tk0 + static_cast<size_t>(m) * a.Hk) * N + c);
+      copy1(rk + static_cast<size_t>(checked_slot((st + h + m) % L, L, a.err)) * N + c, kin + (tk0 + static_cast<size_t>(m) * a.Hk) * N + c);
     }
   }
 }
@@ -430,6 +430,8 @@ cudaError_t launch_gdn_u(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) 
 cudaError_t launch_gdn(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) {
   if ((kind == GdnKind::Decode || kind == GdnKind::Verify) && gdn_split_eligible(kind, a))
     return launch_gdn_split(kind, a, stream);
+  if (kind == GdnKind::VerifyFused)  // only the fused two-launch verify; the caller flushes and verifies otherwise
+    return gdn_split_eligible(kind, a) ? launch_gdn_split(kind, a, stream) : cudaErrorNotSupported;
   if (kind == GdnKind::DecodeFused) return cudaErrorNotSupported;  // caller: decode, then flush
   if (a.in_dtype == RSSM_F32 && a.y_dtype == RSSM_F32) return launch_gdn_u<float, float>(kind, a, stream);
   if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_F32) return launch_gdn_u<bf16, float>(kind, a, stream);

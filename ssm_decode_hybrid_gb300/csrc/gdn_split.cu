@@ -28,17 +28,6 @@ namespace rssm {
 
 namespace {
 
-constexpr int kGwAbar = 0;                      // exp(sum_{m<h} g_m)
-constexpr int kGwInfo = 1;                      // int: h | start << 8 | flags
-constexpr int kGwAbarFold = 2;                  // abar e^{g_t} (fused fold)
-constexpr int kGwW = 4;                         // [kMaxL] fold weights, window order
-constexpr int kGwEG = kGwW + kMaxL;             // [kMaxT] e^{G_m}
-constexpr int kGwBeta = kGwEG + kMaxT;          // [kMaxT] beta_m
-constexpr int kGwA = kGwBeta + kMaxT;           // [kMaxT][kMaxT] A[m][m'], m' < m
-constexpr int kGwY = kGwA + kMaxT * kMaxT;      // [kMaxT][kMaxT] Y[m][m'], m' <= m
-constexpr int kGwBuf = kGwY + kMaxT * kMaxT;    // [2P][dv] buffer vectors
-static_assert(kGwBuf == kGdnWorkHeader, "workspace header size");
-
 constexpr int kInfoValid = 1 << 16;
 
 constexpr int kInfoFold = 1 << 17;
@@ -86,7 +75,10 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   constexpr int es = sizeof(TI), eu = sizeof(TU);
   extern __shared__ __align__(128) unsigned char psm[];
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_ptr[2];
+  __shared__ int s_ptr[4];
+  // a verify with the flush fused in: a flagged sequence folds its committed
+  // entries first and verifies from the emptied window
+  constexpr bool kVFuse = !kDecode && kFuse;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int HpK = a.Hv / a.Hk;
   const int b = blockIdx.x / a.Hk, kh = blockIdx.x - b * a.Hk;
@@ -112,9 +104,12 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
       bulk_g2s(psm + lay.q_in + m * N * es, static_cast<const unsigned char *>(a.q) + off, N * es, &bar);
     }
     const int hc = a.count[b], sc = a.start[b];
-    s_ptr[0] = hc;
-    s_ptr[1] = sc;
-    if (hc >= 1 && hc <= L && sc >= 0 && sc < L) {
+    const bool vfold = kVFuse && a.flag[b] != 0;
+    s_ptr[0] = vfold ? 0 : hc;
+    s_ptr[1] = vfold ? ((hc >= 0 && hc <= L && sc >= 0 && sc < L) ? (sc + hc) % L : -1) : sc;
+    s_ptr[2] = vfold ? hc : -1;
+    s_ptr[3] = sc;
+    if (!vfold && hc >= 1 && hc <= L && sc >= 0 && sc < L) {
       const int n1 = min(hc, L - sc), n2 = hc - n1;
       mbar_expect_tx(&bar, static_cast<uint32_t>(hc) * (N * es + (NT > kUGlobalMaxP ? HpK * dv * eu : 0)));
       const unsigned char *gk = static_cast<const unsigned char *>(a.ring_k) + bk * L * N * es;
@@ -153,12 +148,28 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   }
 
   const int h = s_ptr[0], st = s_ptr[1];
+  const int fc = s_ptr[2], fst = s_ptr[3];  // fused verify: fold count (-1: no fold), the window's old start
   const bool ok = kDecode ? (h >= 0 && h < L && st >= 0 && st < L) : (h >= 0 && st >= 0 && st < L && h + T <= L);
   if (!ok) {
     if (lane == 0) reinterpret_cast<int *>(wk)[kGwInfo] = 0;
-    if (tid == 0) set_err(a.err, kDecode ? RSSM_EBIT_COUNT_RANGE : RSSM_EBIT_WINDOW);
+    if (tid == 0) set_err(a.err, (kDecode || fc >= 0) ? RSSM_EBIT_COUNT_RANGE : RSSM_EBIT_WINDOW);
     return;
   }
+  const bool vfold = kVFuse && fc >= 0;
+  if (vfold) {
+    // the fold of the pending flush, this warp's value head:
+    // w^f_j = exp(sum_{j<m<c} g_m), abar_f = exp(sum_{m<c} g_m)
+    const float *fg = reinterpret_cast<const float *>(psm + lay.g_ring) + w * L;
+    const float gl = (lane < fc) ? fg[wrapL(fst + lane, L)] : 0.f;
+    float tot;
+    const float ex = excl_suffix_sum(gl, lane, tot);
+    if (lane < L) wk[kGwW + lane] = (lane < fc) ? expf(ex) : 0.f;
+    if (lane == 0) {
+      wk[kGwAbarFold] = expf(tot);
+      reinterpret_cast<int *>(wk)[kGwFoldCS] = fc | (fst << 8);
+    }
+  }
+  if (kVFuse && w == 0 && lane == 0) reinterpret_cast<int *>(wk)[kGwCtr] = 0;  // the key head's arrival counter
   const TI *kring = reinterpret_cast<const TI *>(psm + lay.k_ring);
   const TU *uring = reinterpret_cast<const TU *>(psm + lay.u_ring) + static_cast<size_t>(w) * L * dv;
   const float *gring = reinterpret_cast<const float *>(psm + lay.g_ring) + w * L;
@@ -247,8 +258,8 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   if (kDecode && kFuse) wk[kGwW + lane] = (lane < h) ? wj * eg0 : (lane == h ? 1.f : 0.f);
   if (lane == 0) {
     wk[kGwAbar] = abar;
-    wk[kGwAbarFold] = abar * eg0;
-    reinterpret_cast<int *>(wk)[kGwInfo] = h | (st << 8) | kInfoValid | (fold ? kInfoFold : 0);
+    if (kDecode) wk[kGwAbarFold] = abar * eg0;  // a fused verify's slot holds the pending flush's abar
+    reinterpret_cast<int *>(wk)[kGwInfo] = h | (st << 8) | kInfoValid | ((fold || vfold) ? kInfoFold : 0);
   }
   __syncwarp();
 
@@ -311,12 +322,15 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
     for (int v = 0; v < NV; ++v) wk[kGwBuf + v * dv + r] = acc[v];
   }
 
-  // tentative / appended entries: the drafts' k (per key head) and g (per value head)
-  if (lane < T) a.ring_g[bh * L + wrapL(st + h + lane, L) % L] = g_m;
+  // tentative / appended entries: the drafts' k (per key head) and g (per value
+  // head); with a fold pending the streaming kernel writes them once the fold
+  // has read the ring
+  if (vfold) return;
+  if (lane < T) a.ring_g[bh * L + checked_slot(wrapL(st + h + lane, L) % L, L, a.err)] = g_m;
   if (w == 0) {
     for (int m = 0; m < T; ++m) {
       uint32_t *dst =
-          reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_k) + (bk * L + (st + h + m) % L) * N);
+          reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_k) + (bk * L + checked_slot((st + h + m) % L, L, a.err)) * N);
       const uint32_t *src = reinterpret_cast<const uint32_t *>(kin + m * N);
       for (int c = lane; c < N * es / 4; c += 32) dst[c] = src[c];
     }
@@ -446,8 +460,6 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 8 ? 1 : 2)) gdn
     }
   }
   if (tid < kGwBuf) shdr[tid] = wk[tid];
-  const bool groups_ok =
-      group_records_valid(a.work + static_cast<size_t>(b) * a.Hv * stride, a.Hk, HpK, stride, kGwInfo, kInfoValid);
   gdn_row_dots<N, NT>(s, xv, sx, 0, row0, lane);  // the register half
   __syncthreads();  // barrier initialised, header staged
   // one warp waits for the copy; the block barrier passes it on to the rest
@@ -461,18 +473,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 8 ? 1 : 2)) gdn
     return;
   }
   const int info = __float_as_int(shdr[kGwInfo]);
-  if (!(info & kInfoValid) || !groups_ok) return;
+  if (!(info & kInfoValid)) return;
   const int h = info & 0xff, st = (info >> 8) & 0xff;
-  if (i == 0 && rb == 0 && tid == 0) {
-    // every precompute block has read this sequence's pointers: advance them
-    if (kDecode) {
-      const int p = h + 1;
-      a.count[b] = (kFuse && p == L) ? 0 : p;  // fused: a filled buffer is folded below
-      a.flag[b] = (!kFuse && p == L) ? 1 : 0;
-    } else {
-      a.flag[b] = (h + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
-    }
-  }
+  if (!rssm_check(st < L && h + T <= L, a.err)) return;
+  // outputs and the entries past the committed window are written whatever the
+  // other groups' precompute blocks did; a block that changes the sequence's
+  // state (S_0 by a fold, the pointers) first makes sure that every group's
+  // precompute block finished, so that a sequence given up keeps its state whole
+  const float *first = a.work + static_cast<size_t>(b) * a.Hv * stride;
+  bool checked = false;
   if (rows2 > 0) {  // the shared-memory half
     float4 t2[kPass];
 #pragma unroll
@@ -508,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 8 ? 1 : 2)) gdn
 #pragma unroll
           for (int mp = 0; mp <= m; ++mp) ym = fmaf(shdr[kGwY + m * kMaxT + mp], u[mp], ym);
           store1(y + tvm * dv + rs, ym);
-          store1(ru + static_cast<size_t>((st + h + m) % L) * dv + rs, um);
+          store1(ru + static_cast<size_t>(checked_slot((st + h + m) % L, L, a.err)) * dv + rs, um);
           u_last = round_as<TU>(um);
         }
       }
@@ -517,7 +526,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 8 ? 1 : 2)) gdn
   }
 
   if constexpr (kDecode && kFuse) {
-    if (info & kInfoFold) {
+    if ((info & kInfoFold) && sequence_records_valid(first, a.Hk, HpK, stride, kGwInfo, kInfoValid)) {
+      checked = true;
       // every slot holds an entry: the L - 1 committed ones and this step's.
       // The block's rows of the u ring and the group's keys are staged raw, in
       // window order j, with copies issued together; this step's u (slot j = h)
@@ -595,6 +605,17 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 8 ? 1 : 2)) gdn
       }
     }
   }
+  if (i == 0 && rb == 0 && warp == 0 &&
+      (checked || sequence_records_valid(first, a.Hk, HpK, stride, kGwInfo, kInfoValid)) && lane == 0) {
+    // every precompute block has read this sequence's pointers: advance them
+    if (kDecode) {
+      const int p = h + 1;
+      a.count[b] = (kFuse && p == L) ? 0 : p;  // fused: a filled buffer is folded above
+      a.flag[b] = (!kFuse && p == L) ? 1 : 0;
+    } else {
+      a.flag[b] = (h + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
+    }
+  }
 }
 
 template <int N, int NT, bool kDecode, bool kFuse, typename TU, typename TO>
@@ -613,7 +634,7 @@ cudaError_t launch_gs(const GdnLaunch &a, cudaStream_t stream) {
     return e;
   prep<<<static_cast<unsigned>(a.B) * a.Hk, 32 * HpK, psm, stream>>>(a, stride);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (!kDecode && gdn_verify_tc_eligible(a)) return launch_gdn_verify_tc(a, stride, NT, stream);
+  if (!kDecode && gdn_verify_tc_eligible(a)) return launch_gdn_verify_tc(a, stride, NT, kFuse, stream);
   const int nrb = (a.dv + CHUNK - 1) / CHUNK;
   const size_t ssm = GStreamSmem<N, NT>::bytes(kDecode && kFuse, a.L, eu, es);
   auto strm = gdn_stream_kernel<N, NT, kDecode, kFuse, TI, TU, TO>;
@@ -642,6 +663,10 @@ template <int N, typename TU, typename TO>
 cudaError_t launch_gs_kind(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) {
   if (kind == GdnKind::Decode) return launch_gs<N, 1, true, false, TU, TO>(a, stream);
   if (kind == GdnKind::DecodeFused) return launch_gs<N, 1, true, true, TU, TO>(a, stream);
+  if (kind == GdnKind::VerifyFused) {  // the tensor-core stream only (gdn_verify_fused_eligible)
+    if (gdn_window_width(a.T) == 4) return launch_gs<N, 4, false, true, TU, TO>(a, stream);
+    return launch_gs<N, 8, false, true, TU, TO>(a, stream);
+  }
   switch (gdn_window_width(a.T)) {
     case 1: return launch_gs<N, 1, false, false, TU, TO>(a, stream);
     case 4: return launch_gs<N, 4, false, false, TU, TO>(a, stream);
@@ -658,9 +683,13 @@ cudaError_t launch_gs_n(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) {
 }  // namespace
 
 bool gdn_split_eligible(GdnKind kind, const GdnLaunch &a) {
-  if (kind != GdnKind::Decode && kind != GdnKind::DecodeFused && kind != GdnKind::Verify) return false;
+  if (kind != GdnKind::Decode && kind != GdnKind::DecodeFused && kind != GdnKind::Verify &&
+      kind != GdnKind::VerifyFused)
+    return false;
   if (a.in_dtype != RSSM_BF16 || (a.dk != 64 && a.dk != 128)) return false;
-  const int T = kind == GdnKind::Verify ? a.T : 1;
+  // the fused verify folds in the tensor-core stream
+  if (kind == GdnKind::VerifyFused && (!gdn_verify_tc_eligible(a) || a.L > 255)) return false;
+  const int T = (kind == GdnKind::Verify || kind == GdnKind::VerifyFused) ? a.T : 1;
   if (T < 1 || T > kMaxT) return false;
   const int P = gdn_window_width(T);
   const int eu = a.u_dtype == RSSM_BF16 ? 2 : 4;

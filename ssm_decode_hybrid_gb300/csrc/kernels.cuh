@@ -43,7 +43,7 @@ struct M2Launch {
 // rounded up to 16 bytes.
 __host__ __device__ constexpr int work_stride_floats(int d, int L) { return (4 + L + d + 3) & ~3; }
 
-enum class M2Kind { Baseline, Decode, DecodeFused, Verify, SnapshotVerify };
+enum class M2Kind { Baseline, Decode, DecodeFused, Verify, VerifyFused, SnapshotVerify };
 
 cudaError_t launch_m2(M2Kind kind, const M2Launch &a, cudaStream_t stream);
 
@@ -57,12 +57,17 @@ bool m2_decode_split_eligible(const M2Launch &a);
 cudaError_t launch_m2_decode_split(const M2Launch &a, bool fuse_flush, cudaStream_t stream);
 // Speculative verify through the caller's workspace (decode_split.cu): a
 // precompute kernel per (sequence, group), then a kernel streaming S_0 per
-// (sequence, head) for all T drafts.  Record per (sequence, head): a 16-float
-// header (abar_s, info), then P buffer vectors of d rows, P = 1, 4 or 8 >= T.
-constexpr int kM2VerifyHeader = 16;
+// (sequence, head) for all T drafts.  Record per (sequence, head): a 48-float
+// header (abar_s, info, the fold of a pending flush: its abar, count, start
+// and up to kMaxL weights), then P buffer vectors of d rows, P = 1, 4 or 8 >= T.
+constexpr int kM2VerifyHeader = 48;
 __host__ __device__ constexpr int m2_verify_stride_floats(int d, int P) { return (kM2VerifyHeader + P * d + 3) & ~3; }
 bool m2_verify_split_eligible(const M2Launch &a);
-cudaError_t launch_m2_verify_split(const M2Launch &a, cudaStream_t stream);
+// fuse_flush: a sequence flagged for a flush has its committed entries folded
+// into S_0 by the streaming kernel first (replay_flush, then the verify); only
+// on the CUDA-core stream (m2_verify_fused_eligible).
+bool m2_verify_fused_eligible(const M2Launch &a);
+cudaError_t launch_m2_verify_split(const M2Launch &a, bool fuse_flush, cudaStream_t stream);
 // Its streaming half on the tensor cores (verify_tc.cu): n = 128, d = 64,
 // two heads of a group per block, bf16 inputs, T >= 5.
 bool m2_verify_tc_eligible(const M2Launch &a);
@@ -95,14 +100,27 @@ struct GdnLaunch {
   uint64_t wait_ns;    // limit of the precompute kernel's data wait (0: the wait counts as run out)
 };
 
-enum class GdnKind { Baseline, Decode, DecodeFused, Verify, SnapshotVerify };
+enum class GdnKind { Baseline, Decode, DecodeFused, Verify, VerifyFused, SnapshotVerify };
 
 // Window width P of the GDN two-launch kernels for a call with T drafts
 // (T = 1 also covers decode), and the floats of one (sequence, value head)
 // workspace record: a 180-float header of per-head scalars, then the 2P
 // buffer-term vectors of dv rows.
 __host__ __device__ constexpr int gdn_window_width(int T) { return T <= 1 ? 1 : (T <= 4 ? 4 : 8); }
-constexpr int kGdnWorkHeader = 180;
+// Header of a GDN workspace record (written by the precompute kernel of
+// gdn_split.cu, read by the streaming kernels), in floats:
+constexpr int kGwAbar = 0;                    // exp(sum_{m<h} g_m)
+constexpr int kGwInfo = 1;                    // int: h | start << 8 | flags
+constexpr int kGwAbarFold = 2;                // the fold's abar (fused decode: abar e^{g_t}; fused verify: the flush's)
+constexpr int kGwFoldCS = 3;                  // int: fused verify: fold count | old start << 8
+constexpr int kGwW = 4;                       // [kMaxL] fold weights, window order
+constexpr int kGwEG = kGwW + kMaxL;           // [kMaxT] e^{G_m}
+constexpr int kGwBeta = kGwEG + kMaxT;        // [kMaxT] beta_m
+constexpr int kGwA = kGwBeta + kMaxT;         // [kMaxT][kMaxT] A[m][m'], m' < m
+constexpr int kGwY = kGwA + kMaxT * kMaxT;    // [kMaxT][kMaxT] Y[m][m'], m' <= m
+constexpr int kGwCtr = kGwY + kMaxT * kMaxT;  // int: fused verify: head blocks of the key head that staged their fold
+constexpr int kGwBuf = kGwCtr + 4;            // [2P][dv] buffer vectors
+constexpr int kGdnWorkHeader = kGwBuf;
 __host__ __device__ constexpr int gdn_work_stride_floats(int dv, int P) {
   return (kGdnWorkHeader + 2 * P * dv + 3) & ~3;
 }
@@ -116,7 +134,9 @@ cudaError_t launch_gdn_split(GdnKind kind, const GdnLaunch &a, cudaStream_t stre
 // (verify_tc.cu): dk = dv = 128, bf16 inputs; reads the records the
 // precompute kernel left for window width P.
 bool gdn_verify_tc_eligible(const GdnLaunch &a);
-cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, cudaStream_t stream);
+// fuse_flush: a sequence flagged for a flush has its committed entries folded
+// into S_0 first (gdn_replay_flush, then the verify).
+cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, bool fuse_flush, cudaStream_t stream);
 
 cudaError_t launch_gdn(GdnKind kind, const GdnLaunch &a, cudaStream_t stream);
 

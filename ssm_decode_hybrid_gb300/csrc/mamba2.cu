@@ -248,14 +248,14 @@ __global__ void __launch_bounds__(kThreads) m2_replay_kernel(M2Launch a) {
   TI *rv = static_cast<TI *>(a.ring_v) + bh * L * d;
   for (int idx = tid; idx < T * d; idx += kThreads) {
     const int m = idx / d, r = idx - m * d;
-    copy1(rv + static_cast<size_t>((st + h + m) % L) * d + r, vin + (in_h + static_cast<size_t>(m) * a.H) * d + r);
+    copy1(rv + static_cast<size_t>(checked_slot((st + h + m) % L, L, a.err)) * d + r, vin + (in_h + static_cast<size_t>(m) * a.H) * d + r);
   }
-  if (tid < T) a.ring_dt[bh * L + (st + h + tid) % L] = a.dt[in_h + static_cast<size_t>(tid) * a.H];
+  if (tid < T) a.ring_dt[bh * L + checked_slot((st + h + tid) % L, L, a.err)] = a.dt[in_h + static_cast<size_t>(tid) * a.H];
   if (i % HpG == 0) {
     TI *rk = static_cast<TI *>(a.ring_k) + bg * L * N;
     for (int idx = tid; idx < T * N; idx += kThreads) {
       const int m = idx / N, c = idx - m * N;
-      copy1(rk + static_cast<size_t>((st + h + m) % L) * N + c, kin + (in_g + static_cast<size_t>(m) * a.G) * N + c);
+      copy1(rk + static_cast<size_t>(checked_slot((st + h + m) % L, L, a.err)) * N + c, kin + (in_g + static_cast<size_t>(m) * a.G) * N + c);
     }
   }
 }
@@ -384,7 +384,9 @@ cudaError_t launch_m2_t(M2Kind kind, const M2Launch &a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_m2(M2Kind kind, const M2Launch &a, cudaStream_t stream) {
-  if (kind == M2Kind::Verify && m2_verify_split_eligible(a)) return launch_m2_verify_split(a, stream);
+  if (kind == M2Kind::Verify && m2_verify_split_eligible(a)) return launch_m2_verify_split(a, false, stream);
+  if (kind == M2Kind::VerifyFused)  // only the fused two-launch verify; the caller flushes and verifies otherwise
+    return m2_verify_fused_eligible(a) ? launch_m2_verify_split(a, true, stream) : cudaErrorNotSupported;
   if ((kind == M2Kind::Decode || kind == M2Kind::DecodeFused) && m2_decode_split_eligible(a))
     return launch_m2_decode_split(a, kind == M2Kind::DecodeFused, stream);
   if ((kind == M2Kind::Decode || kind == M2Kind::DecodeFused) && m2_decode_flat_eligible(a))

@@ -59,8 +59,9 @@ class GdnReplay(ctypes.Structure):
 EXPORTS = (
     "ssm_state_update_baseline", "replay_decode_step", "replay_decode_step_fused", "replay_flush",
     "replay_spec_verify",
-    "replay_spec_commit", "ssm_spec_verify_baseline", "ssm_spec_commit_baseline",
+    "replay_spec_verify_fused", "replay_spec_commit", "ssm_spec_verify_baseline", "ssm_spec_commit_baseline",
     "gdn_state_update_baseline", "gdn_replay_decode", "gdn_replay_flush", "gdn_replay_verify",
+    "gdn_replay_verify_fused",
     "gdn_spec_verify_baseline", "rssm_version", "rssm_status_string", "rssm_last_cuda_error",
     "replay_decode_workspace_bytes", "replay_decode_step_fused_noalloc",
     "gdn_replay_decode_fused", "gdn_replay_workspace_bytes", "replay_verify_workspace_bytes",
@@ -82,6 +83,7 @@ def _load() -> ctypes.CDLL:
         "replay_decode_step_fused_noalloc": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), P, P, P, P, P, P, P],
         "replay_flush": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), P, P],
         "replay_spec_verify": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), I, P, P, P, P, P, P, P],
+        "replay_spec_verify_fused": [ctypes.POINTER(M2Dims), ctypes.POINTER(M2Replay), I, P, P, P, P, P, P, P],
         "replay_spec_commit": [I, I, I, P, P, P, P],
         "ssm_spec_verify_baseline": [ctypes.POINTER(M2Dims), I, P, P, P, P, P, P, P, P, P, P],
         "ssm_spec_commit_baseline": [I, I, P, P, P, P],
@@ -90,6 +92,7 @@ def _load() -> ctypes.CDLL:
         "gdn_replay_decode_fused": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), P, P, P, P, P, P, P],
         "gdn_replay_flush": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), P],
         "gdn_replay_verify": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), I, P, P, P, P, P, P, P],
+        "gdn_replay_verify_fused": [ctypes.POINTER(GdnDims), ctypes.POINTER(GdnReplay), I, P, P, P, P, P, P, P],
         "gdn_spec_verify_baseline": [ctypes.POINTER(GdnDims), I, P, P, P, P, P, P, P, P, P, P],
         "conv_state_update": [ctypes.POINTER(ConvDims), P, P, P, P, P, P, P, P],
         "rssm_m2_layout_sizes": [ctypes.POINTER(M2Dims), ctypes.POINTER(Layout)],
@@ -391,6 +394,20 @@ def replay_spec_verify(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch
     return y
 
 
+def replay_spec_verify_fused(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+    """replay_flush, then replay_spec_verify, with the flush of each flagged
+    sequence folded in by the launch that streams S_0.  Arguments as
+    replay_spec_verify."""
+    B, H, G, d, n, L = state.shape
+    T = v.shape[1]
+    y = _out(y, (B, T, H, d), y_dtype, state.S0.device)
+    dims = state.dims(y.dtype)
+    st = state.struct()
+    _check(LIB.replay_spec_verify_fused(ctypes.byref(dims), ctypes.byref(st), T, _ptr(v), _ptr(k), _ptr(q),
+                                        _ptr(dt), _ptr(A), _ptr(y), _stream()), "replay_spec_verify_fused")
+    return y
+
+
 def replay_spec_commit(accepted, count, T: int, L: int, err=None):
     _i32(accepted, "accepted")
     _i32(count, "count")
@@ -468,6 +485,20 @@ def gdn_replay_verify(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.f
     st = state.struct()
     _check(LIB.gdn_replay_verify(ctypes.byref(dims), ctypes.byref(st), T, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
                                  _ptr(g), _ptr(y), _stream()), "gdn_replay_verify")
+    return y
+
+
+def gdn_replay_verify_fused(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+    """gdn_replay_flush, then gdn_replay_verify, with the flush of each flagged
+    sequence folded in by the launch that streams S_0.  Arguments as
+    gdn_replay_verify."""
+    B, Hv, Hk, dk, dv, L = state.shape
+    T = v.shape[1]
+    y = _out(y, (B, T, Hv, dv), y_dtype, state.S0.device)
+    dims = state.dims(y.dtype)
+    st = state.struct()
+    _check(LIB.gdn_replay_verify_fused(ctypes.byref(dims), ctypes.byref(st), T, _ptr(q), _ptr(k), _ptr(v),
+                                       _ptr(beta), _ptr(g), _ptr(y), _stream()), "gdn_replay_verify_fused")
     return y
 
 

@@ -263,3 +263,55 @@ def test_gdn_layer_fused_full_batch_sampled():
         np.testing.assert_array_equal(host(state.flag), np.zeros(shape.B), err_msg=f"step {t}: flag")
     assert_close(state.S0[idx], orc.S0, what="final S0")
     assert int(host(state.err)[0]) == 0
+
+
+def run_verify_fused(shape, T, rounds, seed, sample=None, workspace_T=8):
+    """Rounds of gdn_replay_verify_fused + replay_spec_commit (no separate
+    flush) against the oracle doing flush, verify, commit: outputs within
+    tolerance, pointers bit-exact every round, final S_0 after a last flush."""
+    R = rs()
+    init = wl.gdn_init(shape, seed, fill_max=shape.L - T)
+    idx = np.arange(shape.B) if sample is None else np.asarray(sample)
+    state = gdn_state(init, workspace_T)
+    orc = oracle_replay(init, idx)
+    rtol, atol = (1e-2, 1e-3) if shape.u_dtype == wl.BF16 else (1e-3, 1e-4)
+    for r in range(rounds):
+        st = wl.gdn_step(shape, seed, r, T=T)
+        acc = wl.accepted_counts(shape.B, T, seed, r)
+        y = R.gdn_replay_verify_fused(state, *gdn_step_dev(st, shape.in_dtype))
+        orc.flush()
+        Y_ref = orc.verify(take(st.q, idx), take(st.k, idx), take(st.v, idx), take(st.beta, idx), take(st.g, idx))
+        assert_close(y[idx], Y_ref, rtol, atol, what=f"round {r}: y")
+        check_pointers(state, orc, idx, f"round {r}")
+        R.replay_spec_commit(dev(acc, torch.int32), state.count, T, shape.L, state.err)
+        orc.commit(take(acc, idx), T)
+    R.gdn_replay_flush(state)
+    orc.flush()
+    check_pointers(state, orc, idx, "final flush")
+    assert_close(state.S0[idx], orc.S0, rtol, atol, what="final S0")
+    assert int(host(state.err)[0]) == 0
+    assert int(host(state.sync).sum()) == 0
+
+
+@pytest.mark.parametrize("workspace_T", WORKSPACE)
+@pytest.mark.parametrize("T", [1, 2, 4, 6, 8])
+def test_chunked_verify_fused_parity(T, workspace_T):
+    """gdn_replay_verify_fused == gdn_replay_flush + gdn_replay_verify, over
+    rounds whose early flushes fold windows that the next drafts overwrite;
+    T = 1 and the one-launch path take the unfused fallback."""
+    shape = wl.GdnShape(B=8, Hv=8, Hk=4, dk=128, dv=128, L=16, in_dtype=wl.BF16)
+    run_verify_fused(shape, T, rounds=12, seed=340 + T, workspace_T=workspace_T)
+
+
+def test_chunked_verify_fused_dtypes_and_window_equal_to_ring():
+    # bf16 u and bf16 keys in the fold; T = L = 4: every round folds what it committed
+    run_verify_fused(wl.GdnShape(B=4, Hv=4, Hk=2, dk=128, dv=128, L=8, in_dtype=wl.BF16, u_dtype=wl.BF16), 4,
+                     rounds=10, seed=350)
+    run_verify_fused(wl.GdnShape(B=5, Hv=4, Hk=4, dk=128, dv=128, L=4, in_dtype=wl.BF16), 4, rounds=8, seed=351)
+
+
+def test_chunked_verify_fused_full_batch_sampled():
+    """The GDN layer at its own size (B = 256, Hv = 32, Hk = 16, T = 4, L = 16),
+    verify with the flush fused in + commit, 16 rounds, eight sampled sequences."""
+    run_verify_fused(wl.GDN_LAYER, 4, rounds=16, seed=wl.SEED_GDN + 60,
+                     sample=[0, 1, 63, 128, 200, 230, 254, 255], workspace_T=4)

@@ -422,3 +422,57 @@ def test_layer_sweep_fused_points(L):
     workspace: 2L + 8 steps, eight sampled sequences."""
     shape = wl.Mamba2Shape(B=64, H=32, G=8, d=64, n=128, L=L, in_dtype=wl.BF16)
     run_fused_sampled(shape, wl.SEED_SWEEP + L, 2 * L + 8, np.array([0, 5, 17, 32, 40, 51, 62, 63]))
+
+
+def run_spec_fused(shape, T, rounds, seed, sample=None, workspace=True):
+    """Rounds of replay_spec_verify_fused + replay_spec_commit (no separate
+    flush) against the oracle doing flush, verify, commit: outputs within
+    tolerance, pointers bit-exact every round, final S_0 after a last flush."""
+    R = rs()
+    init = wl.mamba2_init(shape, seed, fill_max=shape.L - T)
+    idx = np.arange(shape.B) if sample is None else np.asarray(sample)
+    state = m2_state(init, workspace)
+    orc = oracle_replay(init, idx)
+    A = dev(init.A)
+    for r in range(rounds):
+        st = wl.mamba2_step(shape, seed, r, T=T)
+        acc = wl.accepted_counts(shape.B, T, seed, r)
+        y = R.replay_spec_verify_fused(state, *m2_step_dev(st, shape.in_dtype), A)
+        orc.flush()
+        Y_ref = orc.spec_verify(take(st.v, idx), take(st.k, idx), take(st.q, idx), take(st.dt, idx))
+        assert_close(y[idx], Y_ref, what=f"round {r}: y")
+        check_pointers(state, orc, idx, f"round {r}")
+        R.replay_spec_commit(dev(acc, torch.int32), state.count, T, shape.L, state.err)
+        orc.commit(take(acc, idx), T)
+        np.testing.assert_array_equal(host(state.count)[idx], orc.count, err_msg=f"round {r}: count after commit")
+    R.replay_flush(state, A)
+    orc.flush()
+    check_pointers(state, orc, idx, "final flush")
+    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0
+    assert int(host(state.sync).sum()) == 0
+
+
+@pytest.mark.parametrize("workspace", WORKSPACE)
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 6])
+def test_spec_verify_fused_parity(T, workspace):
+    """replay_spec_verify_fused == replay_flush + replay_spec_verify, over
+    rounds whose early flushes fold windows that the next drafts overwrite
+    (c + T > L); T = 6 and the one-launch path take the unfused fallback."""
+    shape = wl.Mamba2Shape(B=12, H=8, G=2, d=64, n=128, L=16, in_dtype=wl.BF16)
+    run_spec_fused(shape, T, rounds=14, seed=140 + T, workspace=workspace)
+
+
+def test_spec_verify_fused_small_shapes():
+    # fp32 inputs with n = 32, ragged heads; T = L (every round folds what it committed)
+    run_spec_fused(wl.Mamba2Shape(B=4, H=6, G=3, d=20, n=32, L=8, in_dtype=wl.F32), 3, rounds=10, seed=141)
+    run_spec_fused(wl.Mamba2Shape(B=5, H=8, G=2, d=64, n=128, L=4, in_dtype=wl.BF16), 4, rounds=8, seed=142)
+    run_spec_fused(wl.Mamba2Shape(B=4, H=8, G=1, d=48, n=64, L=12, in_dtype=wl.BF16), 4, rounds=10, seed=143)
+
+
+def test_spec_fused_full_batch_sampled():
+    """The speculative workload at its own size: B = 512, T = 4, L = 16,
+    accepted ~ U{0..4}, verify with the flush fused in + commit, 24 rounds;
+    ten sampled sequences against the oracle."""
+    run_spec_fused(wl.SPEC_MAMBA2, 4, rounds=24, seed=wl.SEED_SPEC,
+                   sample=[0, 1, 100, 255, 256, 311, 400, 480, 510, 511])
