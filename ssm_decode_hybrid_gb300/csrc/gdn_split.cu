@@ -634,6 +634,7 @@ cudaError_t launch_gs(const GdnLaunch &a, cudaStream_t stream) {
     return e;
   prep<<<static_cast<unsigned>(a.B) * a.Hk, 32 * HpK, psm, stream>>>(a, stride);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!kDecode && !kFuse && gdn_verify_pipe_eligible(a)) return launch_gdn_verify_pipe(a, stride, NT, stream);
   if (!kDecode && gdn_verify_tc_eligible(a)) return launch_gdn_verify_tc(a, stride, NT, kFuse, stream);
   const int nrb = (a.dv + CHUNK - 1) / CHUNK;
   const size_t ssm = GStreamSmem<N, NT>::bytes(kDecode && kFuse, a.L, eu, es);

@@ -137,6 +137,10 @@ bool gdn_verify_tc_eligible(const GdnLaunch &a);
 // fuse_flush: a sequence flagged for a flush has its committed entries folded
 // into S_0 first (gdn_replay_flush, then the verify).
 cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, bool fuse_flush, cudaStream_t stream);
+// The same streaming half as a persistent, warp-specialised TMA + tcgen05
+// pipeline (verify_pipe.cu): dk = dv = 128, bf16 inputs, 2 <= T.
+bool gdn_verify_pipe_eligible(const GdnLaunch &a);
+cudaError_t launch_gdn_verify_pipe(const GdnLaunch &a, int stride, int P, cudaStream_t stream);
 
 cudaError_t launch_gdn(GdnKind kind, const GdnLaunch &a, cudaStream_t stream);
 

@@ -1,0 +1,427 @@
+// GDN chunked speculative verify, the S_0 stream as a persistent,
+// warp-specialised TMA + tcgen05 pipeline (sm_103a).
+//
+// "ReplaySSM: Cache SSM Inputs, Not State" -- appendix "GDN: speculative
+// decoding": per (sequence, value head) the checkpoint meets the window's 2T
+// vectors once, Z = S_0 [k_1 .. k_T, q_1 .. q_T], and every output row follows
+// from its row of Z and the terms the precompute kernel of gdn_split.cu left
+// in the workspace (the solve is the one of verify_tc.cu).
+//
+// One CTA per SM walks the (sequence, value head) items of the grid.  Each
+// item's 128 x 128 fp32 block is four 128-row x 32-column chunks.  Roles:
+//   warp 0     TMA producer: each chunk lands in a stage of a five-stage ring,
+//              already in the 128-byte-swizzled K-major layout of the MMA's A
+//              operand (one cp.async.bulk.tensor box of 16 KB);
+//   warps 2-3  split: lo = S - tf32(S) of each landed chunk into the stage's
+//              second half (the tensor core reads fp32 as tf32 by dropping the
+//              low 13 mantissa bits, so hi is the landed chunk itself and
+//              hi + lo carries S to about 2^-21), and the item's window
+//              vectors (bf16, exact in tf32) into one of two B-operand slots;
+//   warp 1     MMA issuer: per chunk four tf32 MMAs on hi and four on lo
+//              (M = 128 rows, N = 16 vectors, K = 8) into one of two TMEM
+//              accumulators; a commit frees the stage once they have read it;
+//   warps 4-19 epilogue, four groups of four warps taking every fourth item,
+//              each with its own TMEM accumulator: once an item's accumulator
+//              is complete, thread r of its group reads row r (tcgen05.ld) and
+//              solves it as verify_tc.cu does (four groups, so that the loads
+//              of the solve's inputs of several items are in flight at once).
+// So the S_0 loads of later items are always in flight while earlier items
+// are split, multiplied and solved; no thread holds S_0 in registers.
+// Every wait is bounded (RSSM_EBIT_TIMEOUT); after one runs out each role
+// stops at its next wait, in-flight copies are drained and TMEM is released.
+#include <cudaTypedefs.h>
+
+#include <cuda.h>
+
+#include "kernels.cuh"
+#include "tc05.cuh"
+
+namespace rssm {
+
+namespace {
+
+constexpr int kPvStages = 5;
+constexpr int kPvRows = 128;                        // dv: MMA M, TMEM lanes
+constexpr int kPvK = 128;                           // dk
+constexpr int kPvChunks = 4;                        // 32-column chunks of a row
+constexpr uint32_t kPvChunkBytes = kPvRows * 128;   // 16 KB: one TMA box
+constexpr uint32_t kPvStageBytes = 2 * kPvChunkBytes;  // hi, lo
+constexpr int kPvN = 16;                            // 8 key columns, 8 query columns
+constexpr uint32_t kPvXChunkBytes = kPvN * 128;     // 2 KB
+constexpr uint32_t kPvXBytes = kPvChunks * kPvXChunkBytes;  // 8 KB per slot
+constexpr uint32_t kPvStagesOff = 0;
+constexpr uint32_t kPvXOff = kPvStagesOff + kPvStages * kPvStageBytes;
+constexpr uint32_t kPvHdrOff = kPvXOff + 2 * kPvXBytes;
+constexpr int kPvGroups = 4;                        // epilogue groups of 128 threads
+constexpr uint32_t kPvSmem = kPvHdrOff + kPvGroups * kGdnWorkHeader * 4 + 1024;  // + alignment slack
+constexpr int kPvThreads = 128 + kPvGroups * 128;
+constexpr uint32_t kPvTmemCols = kPvGroups * 16;    // one accumulator of 16 columns per group
+constexpr int kInfoValid = 1 << 16;
+
+// kind::tf32, fp32 accumulator, A and B tf32, both K-major, M = 128, N = 16.
+constexpr uint32_t kPvIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(kPvN >> 3) << 17) |
+                              (static_cast<uint32_t>(kPvRows >> 4) << 24);
+
+// Shared-memory descriptor of a K-major operand in the 128-byte swizzle layout
+// (8-row x 128-byte atoms stacked at 1024 B; bits [61,64) = 2).
+__device__ __forceinline__ uint64_t pv_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void pv_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kPvIdesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
+// 2-D tiled bulk tensor copy global -> shared, completion counted in bytes on bar.
+__device__ __forceinline__ void pv_tma_load(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void pv_lds4(uint32_t a, float4 &v) {
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+}
+__device__ __forceinline__ void pv_sts4(uint32_t a, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+}
+__device__ __forceinline__ float pv_trunc(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
+__device__ __forceinline__ void pv_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bounded wait that also gives up as soon as another role has given up.
+__device__ __forceinline__ bool pv_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+struct PvBars {
+  uint64_t full[kPvStages];   // TMA landed (tx bytes)
+  uint64_t conv[kPvStages];   // lo written (64 split threads)
+  uint64_t empty[kPvStages];  // MMAs have read the stage (commit)
+  uint64_t xfull[2];          // window vectors written (64 split threads)
+  uint64_t xempty[2];         // MMAs of the slot's item done (commit)
+  uint64_t afull[kPvGroups];  // accumulator complete (commit)
+  uint64_t aempty[kPvGroups]; // accumulator read (the group's 128 threads)
+  uint64_t drain;             // every MMA issued has completed (commit)
+};
+
+template <typename TI, typename TU, typename TO>
+__global__ void __launch_bounds__(kPvThreads, 1)
+    gdn_verify_pipe_kernel(const __grid_constant__ CUtensorMap s0map, GdnLaunch a, int stride, int P) {
+  extern __shared__ unsigned char pv_raw[];
+  __shared__ PvBars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t base = (smem_addr(pv_raw) + 1023u) & ~1023u;
+  const int T = a.T, L = a.L;
+  const int HpK = a.Hv / a.Hk;
+  const int items = a.B * a.Hv;
+  volatile int *abort = &s_abort;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kPvStages; ++s) {
+      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.conv[s], 64);
+      mbar_init(&bars.empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.xfull[x], 64);
+      mbar_init(&bars.xempty[x], 1);
+    }
+    for (int g = 0; g < kPvGroups; ++g) {
+      mbar_init(&bars.afull[g], 1);
+      mbar_init(&bars.aempty[g], 128);
+    }
+    mbar_init(&bars.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc05::alloc(&s_tmem, kPvTmemCols);
+    tc05::relinquish();
+  }
+  tc05::fence_before_sync();
+  __syncthreads();
+  tc05::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ---- TMA producer -------------------------------------------------------
+    if (lane == 0) {
+      int q = 0;
+      for (int it = blockIdx.x; it < items && !*abort; it += gridDim.x) {
+        for (int c = 0; c < kPvChunks; ++c, ++q) {
+          const int s = q % kPvStages;
+          if (!pv_wait(&bars.empty[s], ((q / kPvStages) & 1) ^ 1, abort)) break;
+          mbar_arrive_expect_tx(&bars.full[s], kPvChunkBytes);
+          pv_tma_load(base + kPvStagesOff + s * kPvStageBytes, &s0map, c * 32, it * kPvRows, &bars.full[s]);
+        }
+      }
+      // drain: the last copy issued to each stage must land before the CTA ends
+      for (int k = 1; k <= kPvStages && q - k >= 0; ++k) {
+        const int qq = q - k;
+        mbar_wait(&bars.full[qq % kPvStages], (qq / kPvStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer -----------------------------------------------------------
+    if (lane == 0) {
+      int q = 0, k = 0;
+      for (int it = blockIdx.x; it < items && !*abort; it += gridDim.x, ++k) {
+        const int sl = k & 1, ag = k % kPvGroups;
+        if (!pv_wait(&bars.aempty[ag], ((k / kPvGroups) & 1) ^ 1, abort)) break;
+        if (!pv_wait(&bars.xfull[sl], (k >> 1) & 1, abort)) break;
+        tc05::fence_after_sync();
+        const uint32_t d = tmem + static_cast<uint32_t>(ag * kPvN);
+        const uint32_t xb = base + kPvXOff + sl * kPvXBytes;
+        bool ok = true;
+        for (int c = 0; c < kPvChunks; ++c, ++q) {
+          const int s = q % kPvStages;
+          if (!pv_wait(&bars.conv[s], (q / kPvStages) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after_sync();
+          const uint32_t hi = base + kPvStagesOff + s * kPvStageBytes, lo = hi + kPvChunkBytes;
+#pragma unroll
+          for (int s2 = 0; s2 < 4; ++s2)
+            pv_mma(d, pv_desc(hi + s2 * 32), pv_desc(xb + c * kPvXChunkBytes + s2 * 32), c > 0 || s2 > 0);
+#pragma unroll
+          for (int s2 = 0; s2 < 4; ++s2) pv_mma(d, pv_desc(lo + s2 * 32), pv_desc(xb + c * kPvXChunkBytes + s2 * 32), true);
+          tc05::commit(&bars.empty[s]);
+        }
+        if (!ok) break;
+        tc05::commit(&bars.afull[ag]);
+        tc05::commit(&bars.xempty[sl]);
+      }
+      // every MMA issued must be complete before TMEM is released
+      tc05::commit(&bars.drain);
+      mbar_wait(&bars.drain, 0);
+    }
+  } else if (warp < 4) {
+    // ---- split: lo of each landed chunk, and the window vectors ---------------
+    // The next item's vectors are loaded into registers while the current
+    // item's chunks are split, so that the split never waits on global memory.
+    const int ct = tid - 64;  // 0..63
+    constexpr int kXUnits = kPvN * (kPvK / 4) / 64;  // 16-byte units of the vectors per thread
+    uint2 xr[kXUnits];
+    auto load_x = [&](int it) {
+      const int b = it / a.Hv, kh = (it - b * a.Hv) / HpK;
+#pragma unroll
+      for (int j = 0; j < kXUnits; ++j) {
+        const int idx = ct + 64 * j, v = idx / (kPvK / 4), u = idx % (kPvK / 4), m = v & 7;
+        xr[j] = make_uint2(0u, 0u);
+        if (m < T)
+          xr[j] = *reinterpret_cast<const uint2 *>(static_cast<const TI *>(v < 8 ? a.k : a.q) +
+                                                   ((static_cast<size_t>(b) * T + m) * a.Hk + kh) * kPvK + 4 * u);
+      }
+    };
+    static_assert(sizeof(TI) == 2, "bf16 window vectors");
+    if (blockIdx.x < items) load_x(blockIdx.x);
+    int q = 0, k = 0;
+    for (int it = blockIdx.x; it < items && !*abort; it += gridDim.x, ++k) {
+      const int sl = k & 1;
+      if (!pv_wait(&bars.xempty[sl], ((k >> 1) & 1) ^ 1, abort)) break;
+      // vector v: key v (v < 8) or query v - 8, zero past T; 16-byte unit u of
+      // chunk u / 8 at atom v / 8, row v % 8, unit (u % 8) ^ (v % 8); bf16 to fp32 is exact
+      const uint32_t xb = base + kPvXOff + sl * kPvXBytes;
+#pragma unroll
+      for (int j = 0; j < kXUnits; ++j) {
+        const int idx = ct + 64 * j, v = idx / (kPvK / 4), u = idx % (kPvK / 4);
+        const int cc = u >> 3, lu = u & 7;
+        const float4 x = make_float4(__uint_as_float(xr[j].x << 16), __uint_as_float(xr[j].x & 0xffff0000u),
+                                     __uint_as_float(xr[j].y << 16), __uint_as_float(xr[j].y & 0xffff0000u));
+        pv_sts4(xb + cc * kPvXChunkBytes + (v >> 3) * 1024 + (v & 7) * 128 + ((lu ^ (v & 7)) << 4), x);
+      }
+      tc05::fence_proxy_async_smem();
+      mbar_arrive(&bars.xfull[sl]);
+      if (it + static_cast<int>(gridDim.x) < items) load_x(it + gridDim.x);  // in flight during the splits
+      bool ok = true;
+      for (int c = 0; c < kPvChunks; ++c, ++q) {
+        const int s = q % kPvStages;
+        if (!pv_wait(&bars.full[s], (q / kPvStages) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        const uint32_t hi = base + kPvStagesOff + s * kPvStageBytes, lo = hi + kPvChunkBytes;
+        // elementwise, so the swizzle of the layout does not matter
+#pragma unroll 4
+        for (int u = ct; u < static_cast<int>(kPvChunkBytes / 16); u += 64) {
+          float4 x;
+          pv_lds4(hi + u * 16, x);
+          pv_sts4(lo + u * 16, make_float4(x.x - pv_trunc(x.x), x.y - pv_trunc(x.y), x.z - pv_trunc(x.z),
+                                           x.w - pv_trunc(x.w)));
+        }
+        tc05::fence_proxy_async_smem();
+        mbar_arrive(&bars.conv[s]);
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ---- epilogue: group g solves items k = g, g + 4, ...; thread r row r -------
+    const int g = (warp - 4) / 4;   // group
+    const int r = (tid - 128) % 128;  // TMEM lane, state row
+    const int ew = warp % 4;          // this warp reads TMEM lanes 32 ew .. 32 ew + 31
+    float *shdr = reinterpret_cast<float *>(pv_raw + (base - smem_addr(pv_raw)) + kPvHdrOff) + g * kGdnWorkHeader;
+    pdl_wait();  // the precompute grid has finished: workspace, drafts' k and g, pointers
+    // the group's 128 threads take every decision to stop together (named
+    // barriers with an OR), since a named barrier has no time limit
+    int k = g;
+    for (int it = blockIdx.x + g * gridDim.x; it < items; it += kPvGroups * gridDim.x, k += kPvGroups) {
+      const int b = it / a.Hv, i = it - b * a.Hv;
+      const size_t bh = static_cast<size_t>(b) * a.Hv + i;
+      const float *wk = a.work + bh * stride;
+      if (named_bar_or(1 + 2 * g, 128, *abort != 0)) break;  // the previous item's header is no longer read
+      for (int c = r; c < kGdnWorkHeader; c += 128) shdr[c] = wk[c];
+      float pk[kMaxT], pq[kMaxT], pv[kMaxT];
+#pragma unroll
+      for (int m = 0; m < kMaxT; ++m) {
+        pk[m] = pq[m] = pv[m] = 0.f;
+        if (m < T) {
+          pk[m] = wk[kGwBuf + m * kPvRows + r];
+          pq[m] = wk[kGwBuf + (P + m) * kPvRows + r];  // the record holds P key vectors, then the queries
+          pv[m] = load1(static_cast<const TI *>(a.v) + ((static_cast<size_t>(b) * T + m) * a.Hv + i) * kPvRows + r);
+        }
+      }
+      const bool failed = !pv_wait(&bars.afull[g], (k / kPvGroups) & 1, abort);
+      if (named_bar_or(2 + 2 * g, 128, failed)) break;  // the header is in place; the accumulator is complete
+      tc05::fence_after_sync();
+      float z[16];
+      pv_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(g * kPvN), z);
+      tc05::fence_before_sync();
+      mbar_arrive(&bars.aempty[g]);
+      const int info = __float_as_int(shdr[kGwInfo]);
+      if ((info & kInfoValid) && rssm_check(((info >> 8) & 0xff) < L && (info & 0xff) + T <= L, a.err)) {
+        const int h = info & 0xff, st = (info >> 8) & 0xff;
+        const float abar = shdr[kGwAbar];
+        TO *y = static_cast<TO *>(a.y);
+        TU *ru = static_cast<TU *>(a.ring_u) + bh * L * kPvRows;
+        float u[kMaxT];
+#pragma unroll
+        for (int m = 0; m < kMaxT; ++m) {
+          u[m] = 0.f;
+          if (m < T) {
+            const size_t tvm = (static_cast<size_t>(b) * T + m) * a.Hv + i;
+            const float Shk = fmaf(abar, z[m], pk[m]);
+            const float Shq = fmaf(abar, z[8 + m], pq[m]);
+            const float eG = shdr[kGwEG + m];
+            float um = shdr[kGwBeta + m] * (pv[m] - eG * Shk);
+#pragma unroll
+            for (int mp = 0; mp < m; ++mp) um = fmaf(-shdr[kGwA + m * kMaxT + mp], u[mp], um);
+            u[m] = um;
+            float ym = eG * Shq;
+#pragma unroll
+            for (int mp = 0; mp <= m; ++mp) ym = fmaf(shdr[kGwY + m * kMaxT + mp], u[mp], ym);
+            store1(y + tvm * kPvRows + r, ym);
+            store1(ru + static_cast<size_t>(checked_slot((st + h + m) % L, L, a.err)) * kPvRows + r, um);
+          }
+        }
+        // the flag, once every group's precompute block of the sequence finished
+        if (i == 0 && ew == 0 &&
+            sequence_records_valid(a.work + static_cast<size_t>(b) * a.Hv * stride, a.Hk, HpK, stride, kGwInfo,
+                                   kInfoValid) &&
+            lane == 0)
+          a.flag[b] = (h + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
+      }
+    }
+  }
+  if (tid == 0 && *abort) set_err(a.err, RSSM_EBIT_TIMEOUT);
+  tc05::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc05::dealloc(tmem, kPvTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+template <typename TU, typename TO>
+cudaError_t launch_pv(const GdnLaunch &a, int stride, int P, cudaStream_t stream) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // S_0 as a 2-D fp32 tensor: 128 columns (d_k), B Hv 128 rows; boxes of
+  // 128 rows x 32 columns (128 bytes) in the 128-byte swizzle
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kPvK), static_cast<cuuint64_t>(a.B) * a.Hv * kPvRows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kPvK) * 4};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kPvRows)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.S, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+      CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  auto kern = gdn_verify_pipe_kernel<bf16, TU, TO>;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kPvSmem))) !=
+      cudaSuccess)
+    return e;
+  const int items = a.B * a.Hv;
+  const int grid = items < sm_count() ? items : sm_count();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kPvThreads);
+  cfg.dynamicSmemBytes = kPvSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, map, a, stride, P);
+}
+
+}  // namespace
+
+bool gdn_verify_pipe_eligible(const GdnLaunch &a) {
+  return a.dk == kPvK && a.dv == kPvRows && a.in_dtype == RSSM_BF16 && a.T >= 2 && a.T <= kMaxT &&
+         static_cast<long long>(a.B) * a.Hv * kPvRows < (1ll << 31) && (reinterpret_cast<uintptr_t>(a.S) & 15u) == 0 &&
+         encode_fn() != nullptr;
+}
+
+cudaError_t launch_gdn_verify_pipe(const GdnLaunch &a, int stride, int P, cudaStream_t stream) {
+  const bool ub = a.u_dtype == RSSM_BF16, yb = a.y_dtype == RSSM_BF16;
+  if (ub && yb) return launch_pv<bf16, bf16>(a, stride, P, stream);
+  if (ub) return launch_pv<bf16, float>(a, stride, P, stream);
+  if (yb) return launch_pv<float, bf16>(a, stride, P, stream);
+  return launch_pv<float, float>(a, stride, P, stream);
+}
+
+}  // namespace rssm
