@@ -402,6 +402,7 @@ bool flush_tc_eligible(const FlushLaunch &a) {
 }
 
 cudaError_t launch_flush(const FlushLaunch &a, cudaStream_t stream) {
+  if (flush_pipe_eligible(a)) return launch_flush_pipe(a, stream);
   if (flush_tc_eligible(a))
     return a.vec_dtype == RSSM_BF16 ? launch_flush_tc<bf16>(a, stream) : launch_flush_tc<float>(a, stream);
   const bool vb = a.vec_dtype == RSSM_BF16, kb = a.key_dtype == RSSM_BF16;

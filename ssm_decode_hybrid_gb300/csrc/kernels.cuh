@@ -172,6 +172,10 @@ struct FlushLaunch {
 };
 
 cudaError_t launch_flush(const FlushLaunch &a, cudaStream_t stream);
+// The flush as a persistent TMA + tcgen05 pipeline (flush_pipe.cu): n = 128,
+// bf16 keys, d = 64 or 128, L <= 16.
+bool flush_pipe_eligible(const FlushLaunch &a);
+cudaError_t launch_flush_pipe(const FlushLaunch &a, cudaStream_t stream);
 // The tensor-core flush applies (n = 128, bf16 keys, d a multiple of 32).
 bool flush_tc_eligible(const FlushLaunch &a);
 
