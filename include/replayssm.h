@@ -333,7 +333,7 @@ RSSM_API rssm_status gdn_replay_decode_fused(const rssm_gdn_dims *dims, const rs
                                              void *y, rssm_stream_t stream);
 
 /* Bytes of the optional GDN workspace (rssm_gdn_replay.work) for calls with
- * up to T drafts (T = 1 for decode): B * Hv * 4 * ceil((184 + 2 P dv) / 4)
+ * up to T drafts (T = 1 for decode): B * Hv * 4 * ceil((180 + 2 P dv) / 4)
  * with P = 1 for T = 1, 4 for T <= 4, 8 for T <= 8.  0 for invalid
  * arguments.  Host only.                                                      */
 RSSM_API int64_t gdn_replay_workspace_bytes(const rssm_gdn_dims *dims, int32_t T);
@@ -365,17 +365,13 @@ RSSM_API rssm_status gdn_replay_verify(const rssm_gdn_dims *dims, const rssm_gdn
                               const void *k, const void *v, const float *beta, const float *g, void *y,
                               rssm_stream_t stream);
 
-/* GDN chunked verify with the pending flush fused in: the same outputs and
- * state as gdn_replay_flush followed by gdn_replay_verify.  A sequence whose
- * flag is set has its c = count[b] committed entries folded into S_0
- * (S_0 <- (prod alpha_j) S_0 + sum_j (prod_{i>j} alpha_i) u_j k_j^T) by the
- * launch that streams S_0 for the drafts, from the block it already holds;
- * the round then starts from an empty window at start + c.  A speculative
+/* GDN chunked verify preceded by the pending flush: the same outputs and
+ * state as gdn_replay_flush followed by gdn_replay_verify, issued as those two
+ * calls on the stream.  (A fold inside the verify's S_0 stream was measured
+ * slower than the persistent flush and verify pipelines back to back at
+ * B = 256, Hv = 32, L = 16, T = 4, so no fused launch is kept.)  A speculative
  * round is this call and replay_spec_commit.  Requires st->sync (zero, left
- * zero).  The fused launches apply with a workspace of
- * gdn_replay_workspace_bytes(dims, T) bytes on the tensor-core verify
- * (bf16 inputs, d_k = d_v = 128, 2 <= T); otherwise the call runs the flush
- * and then the verify.  Arguments as gdn_replay_verify.                      */
+ * zero), as gdn_replay_flush.  Workspace and arguments as gdn_replay_verify. */
 RSSM_API rssm_status gdn_replay_verify_fused(const rssm_gdn_dims *dims, const rssm_gdn_replay *st, int32_t T,
                                              const void *q, const void *k, const void *v, const float *beta,
                                              const float *g, void *y, rssm_stream_t stream);

@@ -626,10 +626,7 @@ rssm_status gdn_replay_verify_fused(const rssm_gdn_dims *dims, const rssm_gdn_re
   a.g = g;
   a.y = y;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_gdn(GdnKind::VerifyFused, a, cs);
-  if (e != cudaErrorNotSupported) return cuda_status(e);
-  // outside the fused kernels: the flush, then the verify
-  e = launch_flush(gdn_flush_launch(d, s), cs);
+  cudaError_t e = launch_flush(gdn_flush_launch(d, s), cs);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_gdn(GdnKind::Verify, a, cs));
 }

@@ -524,8 +524,34 @@ __global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) 
   float *sM = reinterpret_cast<float *>(psm + lay.dots);
   float *scoef = reinterpret_cast<float *>(psm + lay.coef) + w * NT * kMaxL;
 
-  // k_e . q_s for every entry e and draft s: pairs spread over the lane groups
-  {
+  // k_e . q_s for every entry e and draft s
+  if constexpr (sizeof(TI) == 2) {
+    // bf16: D[e][s] on the tensor cores, one warp per 16 entries.  Row e of A
+    // is key e (a committed slot or a draft), column s of B is query s; rows
+    // past the last entry and columns past the last draft read entry 0 and
+    // query 0 and are not stored.
+    const int nw = blockDim.x / 32;
+    for (int mt = w; mt * 16 < ne; mt += nw) {
+      const int e = mt * 16 + (lane & 15), ec = e < ne ? e : 0;
+      const TI *key = ec < h ? kring + static_cast<size_t>(wrapL(st + ec, L)) * N : kin + (ec - h) * N;
+      const int sq = lane & 7;
+      const uint32_t aaddr = smem_addr(key + (lane >> 4) * 8);
+      const uint32_t baddr = smem_addr(qin + (sq < T ? sq : 0) * N + ((lane >> 3) & 1) * 8);
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < N / 16; ++kk) {
+        uint32_t af[4], bfr[2];
+        ldsm_x4(af, aaddr + kk * 32);
+        ldsm_x2(bfr, baddr + kk * 32);
+        mma_16816_bf16(c, af, bfr);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int er = mt * 16 + (lane >> 2) + (j >> 1) * 8, sc = 2 * (lane & 3) + (j & 1);
+        if (er < ne && sc < T) sM[sc * kMaxL + er] = c[j];
+      }
+    }
+  } else {
     constexpr int V = LPR >= 4 ? 4 : LPR;
     constexpr int RPW = 32 / LPR;
     const int col = (lane % LPR) * 4;

@@ -6,21 +6,25 @@
 // with the cached corrections u_j and the gates g_j).
 //
 // Items are 64-row halves of the (sequence, head) tiles of flagged sequences
-// (a head of d = 64 rows is one item, one of d = 128 two), spread over the
-// persistent CTAs by their index so that every CTA gets its share.  Roles:
+// (a head of d = 64 rows is one item, one of d = 128 two), numbered in
+// sequence order over the flagged sequences only and dealt round-robin to the
+// persistent CTAs, so that every CTA gets the same share however the flags
+// fall.  Roles:
 //   warp 0     TMA producer: an item's 64 x 128 fp32 rows land in its group's
 //              stage as four 64-row x 32-column boxes in the 128-byte swizzle,
 //              issued as soon as the group has released the stage;
 //   warps 2-17 four worker groups of four warps, taking every fourth item.
-//              While the tile is on its way a group reads the pointers, forms
-//              the decay weights (one warp scan), builds the two operands of
-//              D^T = K (W V)^T in shared memory (keys, exact in bf16, K-major;
-//              each w_j v_j[r] split into three bf16 terms, so the product
-//              keeps fp32 accuracy) and issues the three MMAs (M = 128 state
-//              columns = TMEM lanes, N = 64 rows, K = 48) into its own 64 TMEM
-//              columns; then thread c (state column c) reads D^T[c][0..64)
-//              and writes S_0[r][c] = abar S_0[r][c] + D^T[c][r] from the
-//              landed tile, a warp writing 128 contiguous bytes of a row.
+//              While the tile is on its way a group forms the decay weights
+//              (one warp scan), builds the two operands of D^T = K (W V)^T in
+//              shared memory (keys, exact in bf16, K-major, one copy; each
+//              w_j v_j[r] split into three bf16 terms, so the product keeps
+//              fp32 accuracy) and issues three MMAs (M = 128 state columns =
+//              TMEM lanes, N = 64 rows, K = 16 each, one per term) into its
+//              own 64 TMEM columns; it then loads the keys, vectors and decays
+//              of its next item, and thread c (state column c) reads
+//              D^T[c][0..64) and writes S_0[r][c] = abar S_0[r][c] + D^T[c][r]
+//              from the landed tile, a warp writing 128 contiguous bytes of a
+//              row.
 // A second, one-thread-per-sequence launch resets the pointers of every
 // flagged sequence and clears its flag once all items are folded (no
 // arrival counting inside the pipeline).  Every wait is bounded (RSSM_EBIT_TIMEOUT); a group decides
@@ -44,11 +48,11 @@ constexpr int kFpKE = 16;                                // entries, zero-padded
 constexpr int kFpKT = 3 * kFpKE;                         // split-precision K extent
 constexpr uint32_t kFpBoxBytes = kFpRows * 128;          // 64 rows x 32 fp32: 8 KB
 constexpr uint32_t kFpTileBytes = 4 * kFpBoxBytes;       // 32 KB
-constexpr uint32_t kFpABytes = kFpN * kFpKT * 2;         // keys operand: 12 KB
+constexpr uint32_t kFpABytes = kFpN * kFpKE * 2;         // keys operand (one copy serves the three MMAs): 4 KB
 constexpr uint32_t kFpBBytes = kFpRows * kFpKT * 2;      // weighted-vector operand: 6 KB
 constexpr uint32_t kFpTilesOff = 0;
 constexpr uint32_t kFpOpsOff = kFpTilesOff + kFpGroups * kFpTileBytes;
-constexpr int kFpListMax = 1024;                        // items one CTA may hold (its gids, compacted)
+constexpr int kFpListMax = 1024;                        // items one CTA may hold (its gids, in order)
 constexpr uint32_t kFpListOff = kFpOpsOff + kFpGroups * (kFpABytes + kFpBBytes);
 constexpr uint32_t kFpSmem = kFpListOff + 3 * kFpListMax * 4 + 1024;  // + alignment slack: gid, count, start
 constexpr int kFpThreads = 64 + kFpGroups * 128;
@@ -60,6 +64,10 @@ __device__ __forceinline__ void fp_tma_load(uint32_t dst, const CUtensorMap *map
           dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16_pair(bf16 lo, bf16 hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) | (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
 }
 
 __device__ __forceinline__ float fp_lds(uint32_t a) {
@@ -112,17 +120,20 @@ __global__ void __launch_bounds__(kFpThreads, 1)
     tc05::alloc(&s_tmem, kFpTmemCols);
     tc05::relinquish();
   }
-  // this CTA's items (gid = blockIdx.x + j gridDim.x of flagged sequences),
-  // compacted in order into shared memory once, so that no role walks the
-  // flags with a dependent load per candidate
+  // this CTA's items: the flagged sequences' items numbered t = 0, 1, ... in
+  // sequence order, and this CTA takes t = blockIdx.x + j gridDim.x, so every
+  // CTA gets the same share whichever sequences are flagged.  One pass over the
+  // flags (the pointers read with them) writes the gids and pointers of those
+  // items into shared memory in order.
   int *items = reinterpret_cast<int *>(fp_raw + (base - smem_addr(fp_raw)) + kFpListOff);
   int *item_cnt = items + kFpListMax, *item_st = item_cnt + kFpListMax;
-  const int per_cta = static_cast<int>((total - blockIdx.x + gridDim.x - 1) / gridDim.x);
-  int n_items = 0;
-  for (int j0 = 0; j0 < per_cta; j0 += kFpThreads) {
-    const int jj = j0 + tid;
-    const long gid = blockIdx.x + static_cast<long>(jj) * gridDim.x;
-    const bool f = jj < per_cta && a.flag[gid / per_seq] != 0;
+  int n_items = 0, n_seq = 0;  // items listed so far, flagged sequences seen so far
+  const int grid = static_cast<int>(gridDim.x), bid = static_cast<int>(blockIdx.x);
+  for (int b0 = 0; b0 < a.B; b0 += kFpThreads) {
+    const int b = b0 + tid;
+    const bool inb = b < a.B;
+    const bool f = inb && a.flag[b] != 0;
+    const int cb = inb ? a.count[b] : 0, sb = inb ? a.start[b] : 0;
     const unsigned m = __ballot_sync(kFull, f);
     if (lane == 0) s_wcount[warp] = __popc(m);
     __syncthreads();
@@ -136,17 +147,42 @@ __global__ void __launch_bounds__(kFpThreads, 1)
       s_wcount[kFpThreads / 32] = acc;
     }
     __syncthreads();
-    if (f) items[n_items + s_wcount[warp] + __popc(m & ((1u << lane) - 1u))] = static_cast<int>(gid);
-    n_items += s_wcount[kFpThreads / 32];
+    // sequence number p among the flagged ones; its items t = p per_seq + r
+    const long p = n_seq + s_wcount[warp] + __popc(m & ((1u << lane) - 1u));
+    const int r0 = f ? static_cast<int>(((bid - p * per_seq) % grid + grid) % grid) : per_seq;
+    const int mine = r0 < per_seq ? (per_seq - 1 - r0) / grid + 1 : 0;
+    // exclusive prefix of `mine` over the block, in thread (= sequence) order
+    int inc = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += v;
+    }
+    __syncthreads();  // the flag counts are read
+    if (lane == 31) s_wcount[warp] = inc;
     __syncthreads();
+    if (tid == 0) {
+      int acc = 0;
+      for (int w = 0; w < kFpThreads / 32; ++w) {
+        const int cw = s_wcount[w];
+        s_wcount[w] = acc;
+        acc += cw;
+      }
+      s_wcount[kFpThreads / 32] = acc;
+    }
+    __syncthreads();
+    int pos = n_items + s_wcount[warp] + inc - mine;
+    for (int q = 0; q < mine; ++q, ++pos) {
+      if (pos < kFpListMax) {
+        items[pos] = b * per_seq + r0 + q * grid;
+        item_cnt[pos] = cb;
+        item_st[pos] = sb;
+      }
+    }
+    n_items += s_wcount[kFpThreads / 32];
+    n_seq += __syncthreads_count(f);
   }
-  // and their pointers, all read before any item is folded (every item of a
-  // sequence reads them before the last one resets them)
-  for (int kk = tid; kk < n_items; kk += kFpThreads) {
-    const int b = items[kk] / per_seq;
-    item_cnt[kk] = a.count[b];
-    item_st[kk] = a.start[b];
-  }
+  n_items = min(n_items, kFpListMax);  // no effect: flush_pipe_eligible bounds a CTA's share by kFpListMax
 
   tc05::fence_before_sync();
   __syncthreads();
@@ -180,44 +216,62 @@ __global__ void __launch_bounds__(kFpThreads, 1)
   } else if (warp >= 2) {
     // ---- worker group g: items k = g, g + 4, ... ------------------------------
     const int g = (warp - 2) / 4;
-    const int gt = tid - 64 - g * 128;        // 0..127 within the group
-    const int c = 32 * (warp % 4) + lane;     // state column = TMEM lane this thread reads
-    const int gw = gt >> 5;                   // warp within the group
+    const int gt = tid - 64 - g * 128;         // 0..127 within the group: the A row (state column) it writes
+    const int c = 32 * (warp % 4) + lane;      // state column = TMEM lane this thread reads
+    const int gw = gt >> 5;                    // warp within the group
+    const int vr = gt & (kFpRows - 1), vh = gt >> 6;  // B operand: row vr, entries 8 vh .. 8 vh + 7
     const uint32_t tile = base + kFpTilesOff + g * kFpTileBytes;
     const uint32_t opA = base + kFpOpsOff + g * (kFpABytes + kFpBBytes), opB = opA + kFpABytes;
     unsigned char *pA = fp_raw + (opA - smem_addr(fp_raw));
     unsigned char *pB = fp_raw + (opB - smem_addr(fp_raw));
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(g * kFpRows);
     const uint32_t idesc = tc05::idesc_bf16_f32(kFpN, kFpRows);
-    int j = 0, mj = 0;  // j: this group's items so far, mj: its MMA commits so far
-    for (int k = g; k < n_items; k += kFpGroups) {
-      const int gid = items[k];
-      const int b = gid / per_seq;
-      const int rest = gid - b * per_seq;
+    // an item's loads, issued one item ahead: the keys of state column gt
+    // (bf16 pairs), v_e[vr] for this thread's eight entries, and the log decay
+    // of entry `lane` (the group's first warp)
+    uint32_t kp[kFpKE / 2];
+    float vv[8];
+    float ld = 0.f;
+    auto fetch = [&](int k) {
+      const int gid = items[k], cnt = item_cnt[k], st = item_st[k];
+      const int b = gid / per_seq, rest = gid - b * per_seq;
       const int i = rest / halves, hf = rest - i * halves;
       const size_t bh = static_cast<size_t>(b) * H + i;
       const size_t bg = static_cast<size_t>(b) * a.G + i / HpG;
-      const int cnt = item_cnt[k], st = item_st[k];
       const bool valid = cnt >= 0 && cnt <= L && st >= 0 && st < L;
-      // every load of the item at once: keys (this thread's state column), the
-      // vectors of its rows, the log decays (warp 0)
-      constexpr int kVPer = kFpRows * kFpKE / 128;  // vector values per thread
-      bf16 kv[kFpKE];
-      float vv[kVPer];
-      float ld = 0.f;
-      if (valid) {
-        const bf16 *key = static_cast<const bf16 *>(a.ring_key) + bg * L * kFpN;
+      ld = 0.f;
 #pragma unroll
-        for (int e = 0; e < kFpKE; ++e)
-          kv[e] = (e < cnt) ? key[static_cast<size_t>((st + e) % L) * kFpN + gt] : __float2bfloat16_rn(0.f);
-        const TV *vec = static_cast<const TV *>(a.ring_vec) + bh * L * a.d + hf * kFpRows;
+      for (int e = 0; e < kFpKE / 2; ++e) kp[e] = 0u;
 #pragma unroll
-        for (int u = 0; u < kVPer; ++u) {
-          const int idx = gt + 128 * u, e = idx / kFpRows, r = idx - e * kFpRows;
-          vv[u] = (e < cnt) ? load1(vec + static_cast<size_t>((st + e) % L) * a.d + r) : 0.f;
-        }
-        if (gw == 0 && lane < cnt) ld = a.ring_ld[bh * L + (st + lane) % L];
+      for (int q = 0; q < 8; ++q) vv[q] = 0.f;
+      if (!valid) return;
+      const unsigned short *key = static_cast<const unsigned short *>(a.ring_key) + bg * L * kFpN + gt;
+      int sl = st;
+#pragma unroll
+      for (int e = 0; e < kFpKE; e += 2) {
+        const uint32_t k0 = e < cnt ? key[static_cast<size_t>(sl) * kFpN] : 0u;
+        sl = sl + 1 == L ? 0 : sl + 1;
+        const uint32_t k1 = e + 1 < cnt ? key[static_cast<size_t>(sl) * kFpN] : 0u;
+        sl = sl + 1 == L ? 0 : sl + 1;
+        kp[e / 2] = k0 | (k1 << 16);
       }
+      const TV *vec = static_cast<const TV *>(a.ring_vec) + bh * L * a.d + hf * kFpRows + vr;
+      int sv = (st + 8 * vh) % L;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        vv[q] = 8 * vh + q < cnt ? load1(vec + static_cast<size_t>(sv) * a.d) : 0.f;
+        sv = sv + 1 == L ? 0 : sv + 1;
+      }
+      if (gw == 0 && lane < cnt) ld = a.ring_ld[bh * L + (st + lane) % L];
+    };
+    int j = 0, mj = 0;  // j: this group's items so far, mj: its MMA commits so far
+    if (g < n_items) fetch(g);
+    for (int k = g; k < n_items; k += kFpGroups) {
+      const int gid = items[k], cnt = item_cnt[k], st = item_st[k];
+      const int b = gid / per_seq, rest = gid - b * per_seq;
+      const int i = rest / halves, hf = rest - i * halves;
+      const size_t bh = static_cast<size_t>(b) * H + i;
+      const bool valid = cnt >= 0 && cnt <= L && st >= 0 && st < L;
       if (valid) {
         if (gw == 0) {
           // decay weights over the committed entries, one per lane
@@ -227,42 +281,44 @@ __global__ void __launch_bounds__(kFpThreads, 1)
           s_w[g][lane] = (lane < cnt) ? (a.mamba2 ? ld : 1.f) * expf(ex) : 0.f;
           if (lane == 0) s_abar[g] = expf(tot);
         }
-        // A operand: row = state column gt, K = entries (the keys, three times)
-#pragma unroll
-        for (int e = 0; e < kFpKE; e += 2) {
-          __nv_bfloat162 pr;
-          pr.x = kv[e];
-          pr.y = kv[e + 1];
-#pragma unroll
-          for (int t = 0; t < 3; ++t)
-            *reinterpret_cast<__nv_bfloat162 *>(pA + tc05::kmajor_offset(kFpN, gt, t * kFpKE + e)) = pr;
-        }
+        // A operand: row gt = the keys' column gt over the 16 entries (two
+        // 16-byte units); the three MMAs share it
+        *reinterpret_cast<uint4 *>(pA + tc05::kmajor_offset(kFpN, gt, 0)) = make_uint4(kp[0], kp[1], kp[2], kp[3]);
+        *reinterpret_cast<uint4 *>(pA + tc05::kmajor_offset(kFpN, gt, 8)) = make_uint4(kp[4], kp[5], kp[6], kp[7]);
       }
       // s_w ready; every thread is past the previous item's TMEM reads
       if (named_bar_or(1 + g, 128, *abort != 0)) break;
       if (valid) {
-        // B operand: row r of the item, K = entries: hi(w_e v_e[r]), then mid, then lo
+        // B operand: row vr of the item, K = entries: hi(w_e v_e[r]), then mid, then lo
+        uint32_t t0[4], t1[4], t2[4];
 #pragma unroll
-        for (int u = 0; u < kVPer; ++u) {
-          const int idx = gt + 128 * u, e = idx / kFpRows, r = idx - e * kFpRows;
-          bf16 t0, t1, t2;
-          tc05::split3_bf16(s_w[g][e] * vv[u], t0, t1, t2);
-          *reinterpret_cast<bf16 *>(pB + tc05::kmajor_offset(kFpRows, r, e)) = t0;
-          *reinterpret_cast<bf16 *>(pB + tc05::kmajor_offset(kFpRows, r, kFpKE + e)) = t1;
-          *reinterpret_cast<bf16 *>(pB + tc05::kmajor_offset(kFpRows, r, 2 * kFpKE + e)) = t2;
+        for (int q = 0; q < 8; q += 2) {
+          bf16 h0, m0, l0, h1, m1, l1;
+          tc05::split3_bf16(s_w[g][8 * vh + q] * vv[q], h0, m0, l0);
+          tc05::split3_bf16(s_w[g][8 * vh + q + 1] * vv[q + 1], h1, m1, l1);
+          t0[q / 2] = bf16_pair(h0, h1);
+          t1[q / 2] = bf16_pair(m0, m1);
+          t2[q / 2] = bf16_pair(l0, l1);
         }
+        *reinterpret_cast<uint4 *>(pB + tc05::kmajor_offset(kFpRows, vr, 8 * vh)) = make_uint4(t0[0], t0[1], t0[2], t0[3]);
+        *reinterpret_cast<uint4 *>(pB + tc05::kmajor_offset(kFpRows, vr, kFpKE + 8 * vh)) =
+            make_uint4(t1[0], t1[1], t1[2], t1[3]);
+        *reinterpret_cast<uint4 *>(pB + tc05::kmajor_offset(kFpRows, vr, 2 * kFpKE + 8 * vh)) =
+            make_uint4(t2[0], t2[1], t2[2], t2[3]);
         tc05::fence_proxy_async_smem();
       }
       tc05::fence_before_sync();
       if (named_bar_or(1 + g, 128, false)) break;  // operands in place
       if (valid && gt == 0) {
         tc05::fence_after_sync();
+        const uint64_t adesc = tc05::smem_desc(pA, tc05::kLBO, tc05::kSBO);
         for (int s = 0; s < kFpKT / 16; ++s)
-          tc05::mma_bf16(d_tmem, tc05::smem_desc(pA + static_cast<size_t>(s) * kFpN * 32, tc05::kLBO, tc05::kSBO),
-                         tc05::smem_desc(pB + static_cast<size_t>(s) * kFpRows * 32, tc05::kLBO, tc05::kSBO), idesc,
-                         s > 0);
+          tc05::mma_bf16(d_tmem, adesc, tc05::smem_desc(pB + static_cast<size_t>(s) * kFpRows * 32, tc05::kLBO, tc05::kSBO),
+                         idesc, s > 0);
         tc05::commit(&mma_bar[g]);
       }
+      // the group's next item: its loads overlap this one's MMA and write-back
+      if (k + kFpGroups < n_items) fetch(k + kFpGroups);
       bool failed = valid && !fp_wait(&mma_bar[g], mj & 1, abort);
       if (valid) ++mj;
       failed = failed || !fp_wait(&full[g], j & 1, abort);  // the tile has landed (the stage is this group's)

@@ -430,8 +430,6 @@ cudaError_t launch_gdn_u(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) 
 cudaError_t launch_gdn(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) {
   if ((kind == GdnKind::Decode || kind == GdnKind::Verify) && gdn_split_eligible(kind, a))
     return launch_gdn_split(kind, a, stream);
-  if (kind == GdnKind::VerifyFused)  // only the fused two-launch verify; the caller flushes and verifies otherwise
-    return gdn_split_eligible(kind, a) ? launch_gdn_split(kind, a, stream) : cudaErrorNotSupported;
   if (kind == GdnKind::DecodeFused) return cudaErrorNotSupported;  // caller: decode, then flush
   if (a.in_dtype == RSSM_F32 && a.y_dtype == RSSM_F32) return launch_gdn_u<float, float>(kind, a, stream);
   if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_F32) return launch_gdn_u<bf16, float>(kind, a, stream);

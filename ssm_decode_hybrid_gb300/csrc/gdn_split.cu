@@ -75,10 +75,7 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   constexpr int es = sizeof(TI), eu = sizeof(TU);
   extern __shared__ __align__(128) unsigned char psm[];
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_ptr[4];
-  // a verify with the flush fused in: a flagged sequence folds its committed
-  // entries first and verifies from the emptied window
-  constexpr bool kVFuse = !kDecode && kFuse;
+  __shared__ int s_ptr[2];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int HpK = a.Hv / a.Hk;
   const int b = blockIdx.x / a.Hk, kh = blockIdx.x - b * a.Hk;
@@ -104,12 +101,9 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
       bulk_g2s(psm + lay.q_in + m * N * es, static_cast<const unsigned char *>(a.q) + off, N * es, &bar);
     }
     const int hc = a.count[b], sc = a.start[b];
-    const bool vfold = kVFuse && a.flag[b] != 0;
-    s_ptr[0] = vfold ? 0 : hc;
-    s_ptr[1] = vfold ? ((hc >= 0 && hc <= L && sc >= 0 && sc < L) ? (sc + hc) % L : -1) : sc;
-    s_ptr[2] = vfold ? hc : -1;
-    s_ptr[3] = sc;
-    if (!vfold && hc >= 1 && hc <= L && sc >= 0 && sc < L) {
+    s_ptr[0] = hc;
+    s_ptr[1] = sc;
+    if (hc >= 1 && hc <= L && sc >= 0 && sc < L) {
       const int n1 = min(hc, L - sc), n2 = hc - n1;
       mbar_expect_tx(&bar, static_cast<uint32_t>(hc) * (N * es + (NT > kUGlobalMaxP ? HpK * dv * eu : 0)));
       const unsigned char *gk = static_cast<const unsigned char *>(a.ring_k) + bk * L * N * es;
@@ -148,28 +142,12 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   }
 
   const int h = s_ptr[0], st = s_ptr[1];
-  const int fc = s_ptr[2], fst = s_ptr[3];  // fused verify: fold count (-1: no fold), the window's old start
   const bool ok = kDecode ? (h >= 0 && h < L && st >= 0 && st < L) : (h >= 0 && st >= 0 && st < L && h + T <= L);
   if (!ok) {
     if (lane == 0) reinterpret_cast<int *>(wk)[kGwInfo] = 0;
-    if (tid == 0) set_err(a.err, (kDecode || fc >= 0) ? RSSM_EBIT_COUNT_RANGE : RSSM_EBIT_WINDOW);
+    if (tid == 0) set_err(a.err, kDecode ? RSSM_EBIT_COUNT_RANGE : RSSM_EBIT_WINDOW);
     return;
   }
-  const bool vfold = kVFuse && fc >= 0;
-  if (vfold) {
-    // the fold of the pending flush, this warp's value head:
-    // w^f_j = exp(sum_{j<m<c} g_m), abar_f = exp(sum_{m<c} g_m)
-    const float *fg = reinterpret_cast<const float *>(psm + lay.g_ring) + w * L;
-    const float gl = (lane < fc) ? fg[wrapL(fst + lane, L)] : 0.f;
-    float tot;
-    const float ex = excl_suffix_sum(gl, lane, tot);
-    if (lane < L) wk[kGwW + lane] = (lane < fc) ? expf(ex) : 0.f;
-    if (lane == 0) {
-      wk[kGwAbarFold] = expf(tot);
-      reinterpret_cast<int *>(wk)[kGwFoldCS] = fc | (fst << 8);
-    }
-  }
-  if (kVFuse && w == 0 && lane == 0) reinterpret_cast<int *>(wk)[kGwCtr] = 0;  // the key head's arrival counter
   const TI *kring = reinterpret_cast<const TI *>(psm + lay.k_ring);
   const TU *uring = reinterpret_cast<const TU *>(psm + lay.u_ring) + static_cast<size_t>(w) * L * dv;
   const float *gring = reinterpret_cast<const float *>(psm + lay.g_ring) + w * L;
@@ -258,8 +236,8 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   if (kDecode && kFuse) wk[kGwW + lane] = (lane < h) ? wj * eg0 : (lane == h ? 1.f : 0.f);
   if (lane == 0) {
     wk[kGwAbar] = abar;
-    if (kDecode) wk[kGwAbarFold] = abar * eg0;  // a fused verify's slot holds the pending flush's abar
-    reinterpret_cast<int *>(wk)[kGwInfo] = h | (st << 8) | kInfoValid | ((fold || vfold) ? kInfoFold : 0);
+    wk[kGwAbarFold] = abar * eg0;
+    reinterpret_cast<int *>(wk)[kGwInfo] = h | (st << 8) | kInfoValid | (fold ? kInfoFold : 0);
   }
   __syncwarp();
 
@@ -323,9 +301,7 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   }
 
   // tentative / appended entries: the drafts' k (per key head) and g (per value
-  // head); with a fold pending the streaming kernel writes them once the fold
-  // has read the ring
-  if (vfold) return;
+  // head)
   if (lane < T) a.ring_g[bh * L + checked_slot(wrapL(st + h + lane, L) % L, L, a.err)] = g_m;
   if (w == 0) {
     for (int m = 0; m < T; ++m) {
@@ -634,8 +610,8 @@ cudaError_t launch_gs(const GdnLaunch &a, cudaStream_t stream) {
     return e;
   prep<<<static_cast<unsigned>(a.B) * a.Hk, 32 * HpK, psm, stream>>>(a, stride);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (!kDecode && !kFuse && gdn_verify_pipe_eligible(a)) return launch_gdn_verify_pipe(a, stride, NT, stream);
-  if (!kDecode && gdn_verify_tc_eligible(a)) return launch_gdn_verify_tc(a, stride, NT, kFuse, stream);
+  if (!kDecode && gdn_verify_pipe_eligible(a)) return launch_gdn_verify_pipe(a, stride, NT, stream);
+  if (!kDecode && gdn_verify_tc_eligible(a)) return launch_gdn_verify_tc(a, stride, NT, stream);
   const int nrb = (a.dv + CHUNK - 1) / CHUNK;
   const size_t ssm = GStreamSmem<N, NT>::bytes(kDecode && kFuse, a.L, eu, es);
   auto strm = gdn_stream_kernel<N, NT, kDecode, kFuse, TI, TU, TO>;
@@ -664,10 +640,6 @@ template <int N, typename TU, typename TO>
 cudaError_t launch_gs_kind(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) {
   if (kind == GdnKind::Decode) return launch_gs<N, 1, true, false, TU, TO>(a, stream);
   if (kind == GdnKind::DecodeFused) return launch_gs<N, 1, true, true, TU, TO>(a, stream);
-  if (kind == GdnKind::VerifyFused) {  // the tensor-core stream only (gdn_verify_fused_eligible)
-    if (gdn_window_width(a.T) == 4) return launch_gs<N, 4, false, true, TU, TO>(a, stream);
-    return launch_gs<N, 8, false, true, TU, TO>(a, stream);
-  }
   switch (gdn_window_width(a.T)) {
     case 1: return launch_gs<N, 1, false, false, TU, TO>(a, stream);
     case 4: return launch_gs<N, 4, false, false, TU, TO>(a, stream);
@@ -684,13 +656,9 @@ cudaError_t launch_gs_n(GdnKind kind, const GdnLaunch &a, cudaStream_t stream) {
 }  // namespace
 
 bool gdn_split_eligible(GdnKind kind, const GdnLaunch &a) {
-  if (kind != GdnKind::Decode && kind != GdnKind::DecodeFused && kind != GdnKind::Verify &&
-      kind != GdnKind::VerifyFused)
-    return false;
+  if (kind != GdnKind::Decode && kind != GdnKind::DecodeFused && kind != GdnKind::Verify) return false;
   if (a.in_dtype != RSSM_BF16 || (a.dk != 64 && a.dk != 128)) return false;
-  // the fused verify folds in the tensor-core stream
-  if (kind == GdnKind::VerifyFused && (!gdn_verify_tc_eligible(a) || a.L > 255)) return false;
-  const int T = (kind == GdnKind::Verify || kind == GdnKind::VerifyFused) ? a.T : 1;
+  const int T = kind == GdnKind::Verify ? a.T : 1;
   if (T < 1 || T > kMaxT) return false;
   const int P = gdn_window_width(T);
   const int eu = a.u_dtype == RSSM_BF16 ? 2 : 4;

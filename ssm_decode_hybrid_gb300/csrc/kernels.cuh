@@ -100,7 +100,7 @@ struct GdnLaunch {
   uint64_t wait_ns;    // limit of the precompute kernel's data wait (0: the wait counts as run out)
 };
 
-enum class GdnKind { Baseline, Decode, DecodeFused, Verify, VerifyFused, SnapshotVerify };
+enum class GdnKind { Baseline, Decode, DecodeFused, Verify, SnapshotVerify };
 
 // Window width P of the GDN two-launch kernels for a call with T drafts
 // (T = 1 also covers decode), and the floats of one (sequence, value head)
@@ -111,15 +111,13 @@ __host__ __device__ constexpr int gdn_window_width(int T) { return T <= 1 ? 1 : 
 // gdn_split.cu, read by the streaming kernels), in floats:
 constexpr int kGwAbar = 0;                    // exp(sum_{m<h} g_m)
 constexpr int kGwInfo = 1;                    // int: h | start << 8 | flags
-constexpr int kGwAbarFold = 2;                // the fold's abar (fused decode: abar e^{g_t}; fused verify: the flush's)
-constexpr int kGwFoldCS = 3;                  // int: fused verify: fold count | old start << 8
+constexpr int kGwAbarFold = 2;                // abar e^{g_t} (fused decode's fold); slot 3 unused
 constexpr int kGwW = 4;                       // [kMaxL] fold weights, window order
 constexpr int kGwEG = kGwW + kMaxL;           // [kMaxT] e^{G_m}
 constexpr int kGwBeta = kGwEG + kMaxT;        // [kMaxT] beta_m
 constexpr int kGwA = kGwBeta + kMaxT;         // [kMaxT][kMaxT] A[m][m'], m' < m
 constexpr int kGwY = kGwA + kMaxT * kMaxT;    // [kMaxT][kMaxT] Y[m][m'], m' <= m
-constexpr int kGwCtr = kGwY + kMaxT * kMaxT;  // int: fused verify: head blocks of the key head that staged their fold
-constexpr int kGwBuf = kGwCtr + 4;            // [2P][dv] buffer vectors
+constexpr int kGwBuf = kGwY + kMaxT * kMaxT;  // [2P][dv] buffer vectors
 constexpr int kGdnWorkHeader = kGwBuf;
 __host__ __device__ constexpr int gdn_work_stride_floats(int dv, int P) {
   return (kGdnWorkHeader + 2 * P * dv + 3) & ~3;
@@ -134,9 +132,7 @@ cudaError_t launch_gdn_split(GdnKind kind, const GdnLaunch &a, cudaStream_t stre
 // (verify_tc.cu): dk = dv = 128, bf16 inputs; reads the records the
 // precompute kernel left for window width P.
 bool gdn_verify_tc_eligible(const GdnLaunch &a);
-// fuse_flush: a sequence flagged for a flush has its committed entries folded
-// into S_0 first (gdn_replay_flush, then the verify).
-cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, bool fuse_flush, cudaStream_t stream);
+cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, cudaStream_t stream);
 // The same streaming half as a persistent, warp-specialised TMA + tcgen05
 // pipeline (verify_pipe.cu): dk = dv = 128, bf16 inputs, 2 <= T.
 bool gdn_verify_pipe_eligible(const GdnLaunch &a);

@@ -47,7 +47,6 @@ constexpr int kVtWarps = kVtThreads / 32;
 constexpr int kVtRowsPerThread = kVtRows / kVtWarps;  // 16 rows per warp, one 16-byte unit of each per lane
 
 constexpr int kInfoValid = 1 << 16;
-constexpr int kInfoFold = 1 << 17;
 
 // Shared-memory descriptor of a K-major operand in the 128-byte swizzle
 // layout: 8-row x 128-byte atoms stacked along M/N (sbo = 1024 B); lbo is
@@ -203,85 +202,7 @@ __device__ __forceinline__ void tc_release(const TcBlock &t, int warp) {
   if (warp == 0) tc05::dealloc(t.tmem, kVtTmemCols);
 }
 
-// The fold of a pending flush (gdn_replay_verify_fused) on the block held in
-// registers: S_0 <- abar_f S_0 + sum_{j<c} w^f_j u_j k_j^T with the c
-// committed entries from slot fst, staged through the (still unused) A
-// operand area; S_0 is written back and the block goes on with it.  Then the
-// drafts' entries of the emptied window: this head's g, and the key head's k
-// from the last of its value heads to have staged its fold operands.
-template <typename TI, typename TU>
-__device__ __forceinline__ void tc_fold(TcBlock &t, const GdnLaunch &a, const float *wk, int stride, int b, int i,
-                                        int kh, int st_new, int tid, int warp, int lane) {
-  constexpr int dv = kVtRows, N = kVtK;
-  __shared__ int s_last;
-  const int L = a.L, T = a.T, HpK = a.Hv / a.Hk;
-  const int cs = reinterpret_cast<const int *>(wk)[kGwFoldCS];
-  const int fc = cs & 0xff, fst = (cs >> 8) & 0xff;
-  const size_t bh = static_cast<size_t>(b) * a.Hv + i, bk = static_cast<size_t>(b) * a.Hk + kh;
-  unsigned char *raw = reinterpret_cast<unsigned char *>(__cvta_shared_to_generic(t.base + kVtA));
-  unsigned char *su = raw;                                            // [fc][dv] u
-  unsigned char *sk = raw + static_cast<size_t>(kMaxL) * dv * sizeof(TU);  // [fc][N] keys
-  const unsigned char *gu = static_cast<const unsigned char *>(a.ring_u) + bh * L * dv * sizeof(TU);
-  const unsigned char *gk = static_cast<const unsigned char *>(a.ring_k) + bk * L * N * sizeof(TI);
-  const int urow = dv * sizeof(TU) / 16, krow = N * sizeof(TI) / 16;
-  for (int idx = tid; idx < fc * (urow + krow); idx += kVtThreads) {
-    const int j = idx / (urow + krow), u = idx - j * (urow + krow);
-    const size_t sl = static_cast<size_t>(checked_slot((fst + j) % L, L, a.err));
-    if (u < urow)
-      cp_async16(su + (static_cast<size_t>(j) * urow + u) * 16, gu + (sl * urow + u) * 16);
-    else
-      cp_async16(sk + (static_cast<size_t>(j) * krow + u - urow) * 16, gk + (sl * krow + u - urow) * 16);
-  }
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
-  if (tid == 0) {
-    int *ctr = reinterpret_cast<int *>(a.work + (static_cast<size_t>(b) * a.Hv + kh * HpK) * stride) + kGwCtr;
-    __threadfence();
-    s_last = (atomicAdd(ctr, 1) == HpK - 1) ? 1 : 0;
-    __threadfence();
-  }
-  __syncthreads();
-  for (int m = 0; m < T; ++m) {
-    const int sl = checked_slot((st_new + m) % L, L, a.err);
-    if (tid == 0) a.ring_g[bh * L + sl] = a.g[(static_cast<size_t>(b) * T + m) * a.Hv + i];
-    if (s_last) {
-      const uint32_t *ks = reinterpret_cast<const uint32_t *>(static_cast<const TI *>(a.k) +
-                                                              ((static_cast<size_t>(b) * T + m) * a.Hk + kh) * N);
-      uint32_t *kd = reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_k) + (bk * L + sl) * N);
-      for (int c = tid; c < N * static_cast<int>(sizeof(TI)) / 4; c += kVtThreads) kd[c] = ks[c];
-    }
-  }
-  const float af = wk[kGwAbarFold];
-#pragma unroll
-  for (int j = 0; j < kVtRowsPerThread; ++j) {
-    t.sv[j].x *= af;
-    t.sv[j].y *= af;
-    t.sv[j].z *= af;
-    t.sv[j].w *= af;
-  }
-  const TU *us = reinterpret_cast<const TU *>(su);
-  const TI *ks = reinterpret_cast<const TI *>(sk);
-  for (int e = 0; e < fc; ++e) {
-    const float we = wk[kGwW + e];
-    const float4 kv = load4(ks + static_cast<size_t>(e) * N + 4 * lane);
-#pragma unroll
-    for (int j = 0; j < kVtRowsPerThread; ++j) {
-      const float wu = we * load1(us + static_cast<size_t>(e) * dv + warp + kVtWarps * j);
-      t.sv[j].x = fmaf(wu, kv.x, t.sv[j].x);
-      t.sv[j].y = fmaf(wu, kv.y, t.sv[j].y);
-      t.sv[j].z = fmaf(wu, kv.z, t.sv[j].z);
-      t.sv[j].w = fmaf(wu, kv.w, t.sv[j].w);
-    }
-  }
-  float *S = a.S + bh * dv * N;
-#pragma unroll
-  for (int j = 0; j < kVtRowsPerThread; ++j)
-    stg_stream4(S + static_cast<size_t>(warp + kVtWarps * j) * N + 4 * lane, t.sv[j]);
-  __syncthreads();  // the staging area becomes the A operand
-}
-
-template <typename TI, typename TU, typename TO, bool kFuse>
+template <typename TI, typename TU, typename TO>
 __global__ void __launch_bounds__(kVtThreads, 3) gdn_verify_tc_kernel(GdnLaunch a, int stride, int P) {
   extern __shared__ unsigned char vt_raw[];
   __shared__ __align__(8) uint64_t hi_bar;
@@ -307,30 +228,8 @@ __global__ void __launch_bounds__(kVtThreads, 3) gdn_verify_tc_kernel(GdnLaunch 
     tc_put_x(t, v, u, x);
   }
   const float *wk = a.work + bh * stride;
-  // a block that changes the sequence's state (S_0 by a fold, the pointers and
-  // flag) first makes sure that every group's precompute block finished, so
-  // that a sequence given up keeps its state whole; outputs and drafts are
-  // written whatever the other groups did
-  bool checked = false;
-  if constexpr (kFuse) {
-    // whether the block first folds a pending flush is known from the record
-    pdl_wait();  // the precompute grid has finished: workspace, pointers
-    const int info0 = reinterpret_cast<const int *>(wk)[kGwInfo];
-    __syncthreads();  // the window vectors are in place; the fold stages through the A operand area
-    if ((info0 & kInfoValid) && (info0 & kInfoFold) &&
-        rssm_check(((info0 >> 8) & 0xff) < L && (info0 & 0xff) == 0, a.err) &&
-        sequence_records_valid(a.work + static_cast<size_t>(b) * a.Hv * stride, a.Hk, a.Hv / a.Hk, stride, kGwInfo,
-                               kInfoValid)) {
-      checked = true;
-      if (i == 0 && tid == 0) {  // the flush this round carries out
-        a.start[b] = (info0 >> 8) & 0xff;
-        a.count[b] = 0;
-      }
-      tc_fold<TI, TU>(t, a, wk, stride, b, i, kh, (info0 >> 8) & 0xff, tid, warp, lane);
-    }
-  }
   tc_hi(t, &s_tmem, &hi_bar, tid, warp);
-  if constexpr (!kFuse) pdl_wait();  // the precompute grid has finished: workspace, drafts' k and g, pointers
+  pdl_wait();  // the precompute grid has finished: workspace, drafts' k and g, pointers
   for (int c = tid; c < kGdnWorkHeader; c += kVtThreads) shdr[c] = wk[c];
   bool ok = tc_lo(t, &hi_bar, &mma_bar, tid, warp);
   // the solve's per-row inputs, loaded while the MMAs run
@@ -386,8 +285,8 @@ __global__ void __launch_bounds__(kVtThreads, 3) gdn_verify_tc_kernel(GdnLaunch 
     // (the header is read again: nothing of the solve stays live up to here)
     const int inf = __float_as_int(shdr[kGwInfo]);
     if ((inf & kInfoValid) &&
-        (checked || sequence_records_valid(a.work + static_cast<size_t>(b) * a.Hv * stride, a.Hk, a.Hv / a.Hk, stride,
-                                           kGwInfo, kInfoValid)) &&
+        sequence_records_valid(a.work + static_cast<size_t>(b) * a.Hv * stride, a.Hk, a.Hv / a.Hk, stride, kGwInfo,
+                               kInfoValid) &&
         lane == 0)
       a.flag[b] = ((inf & 0xff) + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
   }
@@ -465,9 +364,9 @@ __global__ void __launch_bounds__(kVtThreads, 3) m2_verify_tc_kernel(M2Launch a,
   tc_release(t, warp);
 }
 
-template <typename TU, typename TO, bool kFuse>
+template <typename TU, typename TO>
 cudaError_t launch_vt(const GdnLaunch &a, int stride, int P, cudaStream_t stream) {
-  auto kern = gdn_verify_tc_kernel<bf16, TU, TO, kFuse>;
+  auto kern = gdn_verify_tc_kernel<bf16, TU, TO>;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kVtSmem))) !=
       cudaSuccess)
@@ -513,17 +412,12 @@ bool gdn_verify_tc_eligible(const GdnLaunch &a) {
          a.B <= 65535 && (reinterpret_cast<uintptr_t>(a.S) & 15u) == 0;
 }
 
-template <bool kFuse>
-cudaError_t launch_vt_f(const GdnLaunch &a, int stride, int P, cudaStream_t stream) {
+cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, cudaStream_t stream) {
   const bool ub = a.u_dtype == RSSM_BF16, yb = a.y_dtype == RSSM_BF16;
-  if (ub && yb) return launch_vt<bf16, bf16, kFuse>(a, stride, P, stream);
-  if (ub) return launch_vt<bf16, float, kFuse>(a, stride, P, stream);
-  if (yb) return launch_vt<float, bf16, kFuse>(a, stride, P, stream);
-  return launch_vt<float, float, kFuse>(a, stride, P, stream);
-}
-
-cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, bool fuse_flush, cudaStream_t stream) {
-  return fuse_flush ? launch_vt_f<true>(a, stride, P, stream) : launch_vt_f<false>(a, stride, P, stream);
+  if (ub && yb) return launch_vt<bf16, bf16>(a, stride, P, stream);
+  if (ub) return launch_vt<bf16, float>(a, stride, P, stream);
+  if (yb) return launch_vt<float, bf16>(a, stride, P, stream);
+  return launch_vt<float, float>(a, stride, P, stream);
 }
 
 }  // namespace rssm

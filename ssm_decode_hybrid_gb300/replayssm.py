@@ -489,8 +489,7 @@ def gdn_replay_verify(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.f
 
 
 def gdn_replay_verify_fused(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32):
-    """gdn_replay_flush, then gdn_replay_verify, with the flush of each flagged
-    sequence folded in by the launch that streams S_0.  Arguments as
+    """gdn_replay_flush, then gdn_replay_verify, in one call.  Arguments as
     gdn_replay_verify."""
     B, Hv, Hk, dk, dv, L = state.shape
     T = v.shape[1]
