@@ -67,12 +67,6 @@ def m2_fused_flush_extra_bytes(s: wl.Mamba2Shape) -> int:
     return 4 * s.H * s.d * s.n
 
 
-def m2_fused_fold_bytes(s: wl.Mamba2Shape, c: int) -> int:
-    """A flush of c entries folded into the next verify's S_0 stream: the S_0
-    write and the entries' read (S_0 itself is read for the verify anyway)."""
-    return 4 * s.H * s.d * s.n + c * m2_entry_bytes(s)
-
-
 def m2_baseline_bytes(s: wl.Mamba2Shape) -> int:
     e = 2 if s.in_dtype == wl.BF16 else 4
     return 8 * s.H * s.d * s.n + s.H * s.d * e + 2 * s.G * s.n * e + s.H * 4 + 4 * s.H * s.d
@@ -529,8 +523,6 @@ def extra_workloads(R, peak) -> dict:
         "spec_round_b512_t4": {
             "workload": m2["workload"], "calls": m2["calls"],
             "timing": m2["timing"], "rounds": m2["rounds"], "ms_per_round": m2["ms_per_round"],
-            "unfused_ms_per_round": m2["unfused_ms_per_round"],
-            "unfused_calls": "replay_spec_verify + replay_spec_commit + replay_flush",
             "gbs": m2["gbs"], "frac": m2["frac_of_peak"], "accepted_tokens_per_s": m2["accepted_tokens_per_s"],
             "snapshot_baseline_ms_per_round": m2["baseline_ms_per_round"],
             "replay_over_snapshot": m2["replay_over_baseline"], "round_over_decode": m2["round_over_decode"],
@@ -1123,17 +1115,13 @@ def suite_sweep(R, peak, steps=None, Ts=range(1, 7), emit=True):
                 y = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
 
                 def rnd(i):
-                    R.replay_spec_verify_fused(st, *inp[i % K], A, y=y)
-                    R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
-
-                def rnd_unfused(i):
                     R.replay_spec_verify(st, *inp[i % K], A, y=y)
                     R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
                     R.replay_flush(st, A)
 
                 vb = lambda h: m2_verify_bytes(shape, h, T)  # noqa: E731
-                fb = lambda c: m2_fused_fold_bytes(shape, c)  # noqa: E731
-                calls = "replay_spec_verify_fused + replay_spec_commit"
+                fb = lambda c: m2_flush_bytes(shape, c)  # noqa: E731
+                calls = "replay_spec_verify + replay_spec_commit + replay_flush"
                 snap_round_bytes = m2_snapshot_verify_bytes(shape, T) * shape.B
                 slot_shape = (shape.B, T + 1, shape.H, shape.d, shape.n)
             else:
@@ -1148,7 +1136,6 @@ def suite_sweep(R, peak, steps=None, Ts=range(1, 7), emit=True):
                     R.replay_spec_commit(accs[i % K], st.count, T, shape.L, st.err)
                     R.gdn_replay_flush(st)
 
-                rnd_unfused = None
                 vb = lambda h: gdn_verify_bytes(shape, h, T)  # noqa: E731
                 fb = lambda c: gdn_flush_bytes(shape, c)  # noqa: E731
                 calls = "gdn_replay_verify + replay_spec_commit + gdn_replay_flush"
@@ -1158,19 +1145,9 @@ def suite_sweep(R, peak, steps=None, Ts=range(1, 7), emit=True):
             acc_h = [a.cpu().numpy() for a in accs]
             ms = _time_graph(rnd, K, W, reps)
             err = int(st.err.item())
-            unfused_ms = None
-            if rnd_unfused is not None:
-                R.replay_flush(st, A)  # the fused rounds leave their last flags pending
-                unfused_ms = _time_graph(rnd_unfused, K, W, reps)
-                err |= int(st.err.item())
             # rounds run: one eager, then W + reps replays of the K captured rounds; the last reps x K are timed
             seq = [acc_h[0]] + [acc_h[i] for _ in range(W + reps) for i in range(K)]
             hs, folds = spec_trace(count0, seq, T, shape.L)
-            if rnd_unfused is not None:
-                # a fused round folds what the previous round flagged, and verifies from
-                # the emptied window; the rounds' fill levels are the same
-                folds = [np.full_like(folds[0], -1)] + folds[:-1]
-                hs = [np.where(f >= 0, 0, h) for h, f in zip(hs, folds)]
             per_h = {x: vb(x) for x in range(shape.L + 1)}
             per_c = {x: fb(x) for x in range(shape.L + 1)}
             nbytes = 0
@@ -1201,7 +1178,6 @@ def suite_sweep(R, peak, steps=None, Ts=range(1, 7), emit=True):
                                  f"GDN layer B={shape.B}, Hv=32, Hk=16, d_k=d_v=128") + f", L=16, T={T}",
                     "T": T, "rounds": reps * K, "timing": f"CUDA graph of {K} rounds", "calls": calls,
                     "ms_per_round": ms, "accepted_tokens_per_s": shape.B * mean_acc / (ms * 1e-3),
-                    "unfused_ms_per_round": unfused_ms,
                     "gbs": gbs, "frac_of_peak": gbs / peak,
                     "decode_step_ms": dec_ms, "decode_gbs": dec_gbs, "round_over_decode": ms / dec_ms,
                     "baseline_ms_per_round": bms, "baseline_decode_step_ms": base_dec_ms,
@@ -1407,11 +1383,10 @@ def suite_kernels(R, peak, steps=None):
     """A few eager calls of every hot kernel at its benchmark workload, one
     JSON line each with the mean milliseconds per call: the command the ncu
     captures of single kernels run (one kernel per capture, selected with
-    -k).  Mamba-2 baseline and fused decode (B = 256), the speculative round
-    at B = 512, T = 4 (verify, commit, flush: the tensor-core flush), the
-    tensor-core Mamba-2 verify (B = 512, T = 6), the round with the flush
-    fused into the verify (B = 512, T = 4), the GDN baseline and fused
-    decode (B = 256) and the GDN T = 4 round (tensor-core verify, flush)."""
+    -k).  Mamba-2 baseline and fused decode (B = 256), the speculative rounds
+    at B = 512 (verify, commit, flush) for T = 4 (CUDA-core verify stream)
+    and T = 6 (tensor-core verify), the GDN baseline and fused decode
+    (B = 256) and the GDN T = 4 round (pipelined tensor-core verify, flush)."""
     import torch
 
     n = steps or 3
@@ -1457,18 +1432,6 @@ def suite_kernels(R, peak, steps=None):
 
         timed(f"m2_spec_round B=512 T={T}", rnd)
         del st
-    T = 4
-    st, A = m2(shape, 16, T)
-    rin = [wl.mamba2_round_device(shape, 80 + i, T, "cuda") for i in range(4)]
-    acc = [wl.accepted_counts_device(shape.B, T, 90 + i, "cuda") for i in range(4)]
-    yv = torch.empty(shape.B, T, shape.H, shape.d, device="cuda")
-
-    def frnd(i):
-        R.replay_spec_verify_fused(st, *rin[i % 4], A, y=yv)
-        R.replay_spec_commit(acc[i % 4], st.count, T, shape.L, st.err)
-
-    timed("m2_spec_round_fused B=512 T=4", frnd)
-    del st
     shape = wl.GDN_LAYER
     t = wl.gdn_state_tensors_device(shape, 13, "cuda")
     st = R.GdnState(t["S0"], t["ring_u"], t["ring_k"], t["ring_g"], t["start"], t["count"], z(shape.B), z(shape.B),

@@ -180,7 +180,7 @@ RSSM_API rssm_status replay_decode_step(const rssm_m2_dims *dims, const rssm_m2_
 RSSM_API int64_t replay_decode_workspace_bytes(const rssm_m2_dims *dims);
 
 /* Bytes of the optional workspace for replay_spec_verify with up to T drafts:
- * B * H * 4 * ceil((48 + P d) / 4) with P = 1 for T = 1, 4 for T <= 4, 8 for
+ * B * H * 4 * ceil((16 + P d) / 4) with P = 1 for T = 1, 4 for T <= 4, 8 for
  * T <= 8.  0 for invalid arguments.  Host only.                               */
 RSSM_API int64_t replay_verify_workspace_bytes(const rssm_m2_dims *dims, int32_t T);
 
@@ -257,20 +257,15 @@ RSSM_API rssm_status replay_spec_verify(const rssm_m2_dims *dims, const rssm_m2_
                                const void *v, const void *k, const void *q, const float *dt,
                                const float *A, void *y, rssm_stream_t stream);
 
-/* Speculative verify with the pending flush fused in ("Algorithm -- speculative
+/* Speculative verify preceded by the pending flush ("Algorithm -- speculative
  * decoding", flush decision: the early flush that the previous round flagged):
- * the same outputs and state as replay_flush followed by replay_spec_verify.
- * A sequence whose flag is set has its c = count[b] committed entries folded
- * into S_0 (S_0 <- abar S_0 + sum_j s_j v_j k_j^T) by the launch that streams
- * S_0 for the drafts, from the tile it already holds; the round then starts
- * from an empty window at start + c (start <- (start + c) mod L, count <- 0),
- * and the flag is set again by the early-flush rule.  So a speculative round
- * is this call and replay_spec_commit, with no separate flush: the flush that
- * round r flags is carried out by round r + 1.  Requires st->sync (zero, left
- * zero).  The fused launches apply with a workspace of
- * replay_verify_workspace_bytes(dims, T) bytes, L a multiple of 4 and the
- * CUDA-core verify stream (T <= 4 at d = 64, n = 128); otherwise the call
- * runs the flush and then the verify.  Arguments as replay_spec_verify.      */
+ * replay_flush then replay_spec_verify, issued as those two calls on the
+ * stream, so that a speculative round is this call and replay_spec_commit and
+ * the flush that round r flags is carried out by round r + 1.  (A fold inside
+ * the verify's S_0 stream doubled that kernel's instructions and measured
+ * slower than the persistent flush pipeline followed by the verify, so no
+ * fused launch is kept.)  Requires st->sync (zero, left zero), as
+ * replay_flush.  Workspace and arguments as replay_spec_verify.              */
 RSSM_API rssm_status replay_spec_verify_fused(const rssm_m2_dims *dims, const rssm_m2_replay *st, int32_t T,
                                               const void *v, const void *k, const void *q, const float *dt,
                                               const float *A, void *y, rssm_stream_t stream);

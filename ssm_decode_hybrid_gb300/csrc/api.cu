@@ -418,10 +418,7 @@ rssm_status replay_spec_verify_fused(const rssm_m2_dims *dims, const rssm_m2_rep
   a.work = s->work;
   a.work_bytes = s->work_bytes;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_m2(M2Kind::VerifyFused, a, cs);
-  if (e != cudaErrorNotSupported) return cuda_status(e);
-  // outside the fused kernels: the flush, then the verify
-  e = launch_flush(m2_flush_launch(d, s, A), cs);
+  cudaError_t e = launch_flush(m2_flush_launch(d, s, A), cs);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_m2(M2Kind::Verify, a, cs));
 }

@@ -385,27 +385,11 @@ cudaError_t launch_split_f(const M2Launch &a, cudaStream_t stream) {
 // The precompute kernel (per sequence and group) forms abar_s and the buffer
 // vectors buf_s[r] = sum_j w_{j,s} (k_j^T q_s) v_j[r] for every draft s; the
 // streaming kernel (per sequence and head) reads S_0 once for all T queries.
-// Workspace record per (sequence, head): abar_s [kMaxT], info, arrival
-// counter, the fold's abar and (count | start << 8), pad, the fold weights
-// [kMaxL], then buf [P][d] (P = 1, 4 or 8 >= T).
-//
-// With the flush fused in (replay_spec_verify_fused: replay_flush, then the
-// verify), a sequence whose flag is set has its c committed entries folded
-// into S_0 by the streaming kernel from the S_0 tile it holds anyway,
-//   S_0 <- abar_f S_0 + sum_{j<c} w^f_j v_j k_j^T,
-// and the round then starts from an empty window at start + c.  The drafts of
-// such a sequence land on ring slots the fold still reads (c + T may exceed
-// L), so the streaming kernel writes them once it has staged its fold
-// operands: each head block its own v and Delta, and the last head block of
-// a group to stage (an arrival counter per group) the group's k.
+// Workspace record per (sequence, head): abar_s [kMaxT], info, pad, then
+// buf [P][d] (P = 1, 4 or 8 >= T).
 // ---------------------------------------------------------------------------
 constexpr int kVwInfo = kMaxT;
-constexpr int kVwCtr = kMaxT + 1;      // int: heads of the group that staged their fold operands
-constexpr int kVwFoldAbar = kMaxT + 2;
-constexpr int kVwFoldCS = kMaxT + 3;   // int: fold count | old start << 8
-constexpr int kVwFoldW = 16;           // [kMaxL] fold weights, window order
 constexpr int kVwBuf = kM2VerifyHeader;
-static_assert(kVwFoldW + kMaxL <= kM2VerifyHeader, "verify record header");
 
 struct VPrepSmem {
   uint32_t k_ring, v_ring, dt_ring, k_in, q_in, v_in, dots, coef, total;
@@ -422,13 +406,13 @@ struct VPrepSmem {
   }
 };
 
-template <int N, int NT, bool kFuse, typename TI>
+template <int N, int NT, typename TI>
 __global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) {
   constexpr int LPR = N / 4;
   constexpr int es = sizeof(TI);
   extern __shared__ __align__(128) unsigned char psm[];
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_ptr[4];
+  __shared__ int s_ptr[2];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int HpG = a.H / a.G;
   const int b = blockIdx.x / a.G, g = blockIdx.x - b * a.G;
@@ -455,14 +439,9 @@ __global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) 
       bulk_g2s(psm + lay.v_in + m * HpG * d * es, static_cast<const unsigned char *>(a.v) + vo, HpG * d * es, &bar);
     }
     const int hc = a.count[b], sc = a.start[b];
-    const bool fold = kFuse && a.flag[b] != 0;
-    // a pending flush: the round starts from an empty window at start + c, and
-    // the fold weights need only the Delta rings (already on their way)
-    s_ptr[0] = fold ? 0 : hc;
-    s_ptr[1] = fold ? ((hc >= 0 && hc <= L && sc >= 0 && sc < L) ? (sc + hc) % L : -1) : sc;
-    s_ptr[2] = fold ? hc : -1;
-    s_ptr[3] = sc;
-    if (!fold && hc >= 1 && hc <= L && sc >= 0 && sc < L) {
+    s_ptr[0] = hc;
+    s_ptr[1] = sc;
+    if (hc >= 1 && hc <= L && sc >= 0 && sc < L) {
       const int n1 = min(hc, L - sc), n2 = hc - n1;
       mbar_expect_tx(&bar, static_cast<uint32_t>(hc) * (N * es + HpG * d * es));
       const unsigned char *gk = static_cast<const unsigned char *>(a.ring_k) + bg * L * N * es;
@@ -494,26 +473,11 @@ __global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) 
     return;
   }
   const int h = s_ptr[0], st = s_ptr[1];
-  const int fc = s_ptr[2], fst = s_ptr[3];  // fold count (-1: no fold) and the window's old start
   if (h < 0 || st < 0 || st >= L || h + T > L) {
     if (lane == 0) reinterpret_cast<int *>(wk)[kVwInfo] = 0;
-    if (tid == 0) set_err(a.err, fc >= 0 ? RSSM_EBIT_COUNT_RANGE : RSSM_EBIT_WINDOW);
+    if (tid == 0) set_err(a.err, RSSM_EBIT_WINDOW);
     return;
   }
-  if (kFuse && fc >= 0) {
-    // the fold of the pending flush, this warp's head:
-    // w^f_j = Delta_j exp(A sum_{j<m<c} Delta_m), abar_f = exp(A sum_{m<c} Delta_m)
-    const float* fdt = reinterpret_cast<const float *>(psm + lay.dt_ring) + w * L;
-    const float ld = (lane < fc) ? fdt[wrapL(fst + lane, L)] : 0.f;
-    float tot;
-    const float ex = excl_suffix_sum(Ai * ld, lane, tot);
-    if (lane < L) wk[kVwFoldW + lane] = (lane < fc) ? ld * expf(ex) : 0.f;
-    if (lane == 0) {
-      wk[kVwFoldAbar] = expf(tot);
-      reinterpret_cast<int *>(wk)[kVwFoldCS] = fc | (fst << 8);
-    }
-  }
-  if (kFuse && lane == 0 && w == 0) reinterpret_cast<int *>(wk)[kVwCtr] = 0;  // the group's arrival counter
   const int ne = h + T;  // committed entries, then the drafts
   const TI *kring = reinterpret_cast<const TI *>(psm + lay.k_ring);
   const TI *kin = reinterpret_cast<const TI *>(psm + lay.k_in);
@@ -577,46 +541,73 @@ __global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) 
       }
     }
   }
-  // decay of this head for each draft s: w_{e,s} = Delta_e exp(A sum_{e<m<p_s} Delta_m)
+  // decay of this head for each draft s: w_{e,s} = Delta_e exp(A sum_{e<m<p_s} Delta_m),
+  // p_s = h + s + 1, from one prefix sum C_e = sum_{m<=e} A Delta_m of entry
+  // `lane`: the exponent is C_{p_s - 1} - C_e and abar_s = exp(C_{p_s - 1})
   const float dd = __shfl_sync(kFull, dt_draft, (lane - h) & 31);
   const float dte = (lane < h) ? sdt[wrapL(st + lane, L)] : (lane < ne ? dd : 0.f);
+  float cs = Ai * dte;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(kFull, cs, o);
+    if (lane >= o) cs += t;
+  }
   __syncthreads();  // sM complete
-  for (int sq = 0; sq < T; ++sq) {
+#pragma unroll
+  for (int sq = 0; sq < NT; ++sq) {
     const int p = h + sq + 1;
-    float tot;
-    const float ex = excl_suffix_sum((lane < p) ? Ai * dte : 0.f, lane, tot);
-    scoef[sq * kMaxL + lane] = (lane < p) ? dte * expf(ex) * sM[sq * kMaxL + lane] : 0.f;
-    if (lane == 0) wk[sq] = expf(tot);
+    const float cp = __shfl_sync(kFull, cs, (p - 1) & 31);
+    if (sq < T) {
+      scoef[lane * NT + sq] = (lane < p) ? dte * expf(cp - cs) * sM[sq * kMaxL + lane] : 0.f;
+      if (lane == 0) wk[sq] = expf(cp);
+    }
   }
   if (lane == 0)
-    reinterpret_cast<int *>(wk)[kVwInfo] = h | (st << 8) | kInfoValid | ((kFuse && fc >= 0) ? kInfoFold : 0);
+    reinterpret_cast<int *>(wk)[kVwInfo] = h | (st << 8) | kInfoValid;
   __syncwarp();
 
-  // buffer vectors of this head, two rows per lane
+  // buffer vectors of this head, two rows per lane: the committed entries from
+  // the ring (slot by slot), then the drafts
   for (int r = 2 * lane; r < d; r += 64) {
     float2 acc[NT];
 #pragma unroll
     for (int sq = 0; sq < NT; ++sq) acc[sq] = make_float2(0.f, 0.f);
-    for (int e = 0; e < ne; ++e) {
-      const float2 v2 = load2((e < h ? vring + static_cast<size_t>(wrapL(st + e, L)) * d
-                                     : vin + static_cast<size_t>((e - h) * HpG + w) * d) + r);
+    auto add = [&](int e, float2 v2) {
+      float c[NT];
+      if constexpr (NT % 4 == 0) {
+#pragma unroll
+        for (int q4 = 0; q4 < NT; q4 += 4) {
+          const float4 c4 = *reinterpret_cast<const float4 *>(scoef + e * NT + q4);
+          c[q4] = c4.x;
+          c[q4 + 1] = c4.y;
+          c[q4 + 2] = c4.z;
+          c[q4 + 3] = c4.w;
+        }
+      } else {
+#pragma unroll
+        for (int sq = 0; sq < NT; ++sq) c[sq] = scoef[e * NT + sq];
+      }
 #pragma unroll
       for (int sq = 0; sq < NT; ++sq) {
-        const float c = scoef[sq * kMaxL + e];
-        acc[sq].x = fmaf(c, v2.x, acc[sq].x);
-        acc[sq].y = fmaf(c, v2.y, acc[sq].y);
+        acc[sq].x = fmaf(c[sq], v2.x, acc[sq].x);
+        acc[sq].y = fmaf(c[sq], v2.y, acc[sq].y);
       }
+    };
+    int sl = st;
+    for (int e = 0; e < h; ++e) {
+      add(e, load2(vring + static_cast<size_t>(sl) * d + r));
+      sl = sl + 1 == L ? 0 : sl + 1;
     }
+    for (int m = 0; m < T; ++m) add(h + m, load2(vin + static_cast<size_t>(m * HpG + w) * d + r));
 #pragma unroll
     for (int sq = 0; sq < NT; ++sq)
       if (sq < T) *reinterpret_cast<float2 *>(wk + kVwBuf + sq * d + r) = acc[sq];
   }
 
-  // the drafts' entries, tentatively, at slots (start + h + m) mod L; with a
-  // fold pending the streaming kernel writes them once the fold has read the ring
-  if (kFuse && fc >= 0) return;
-  for (int m = 0; m < T; ++m) {
-    const int sl = checked_slot((st + h + m) % L, L, a.err);
+  // the drafts' entries, tentatively, at slots (start + h + m) mod L
+  int sd = wrapL(st + h, L);
+  for (int m = 0; m < T; ++m, sd = sd + 1 == L ? 0 : sd + 1) {
+    const int sl = checked_slot(sd, L, a.err);
     uint32_t *rv = reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_v) + (bh * L + sl) * d);
     const uint32_t *sv = reinterpret_cast<const uint32_t *>(vin + static_cast<size_t>(m * HpG + w) * d);
     for (int c = lane; c < d * es / 4; c += 32) rv[c] = sv[c];
@@ -630,12 +621,9 @@ __global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) 
   }
 }
 
-template <int N, int NT, bool kFuse, typename TI, typename TO>
+template <int N, int NT, typename TI, typename TO>
 __global__ void __launch_bounds__(kThreads, NT == 8 ? 2 : 4) m2_vstream_kernel(M2Launch a, int stride) {
   constexpr int LPR = N / 4, RPW = 32 / LPR, RPP = kWarps * RPW;
-  constexpr int es = sizeof(TI);
-  extern __shared__ __align__(16) unsigned char vsm[];  // fold only: [L][d] v slots, [L][N] k slots
-  __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x / a.H, i = blockIdx.x - b * a.H;
   const int d = a.d, L = a.L, T = a.T;
@@ -661,91 +649,7 @@ __global__ void __launch_bounds__(kThreads, NT == 8 ? 2 : 4) m2_vstream_kernel(M
   const int info = reinterpret_cast<const int *>(wk)[kVwInfo];
   const int HpG = a.H / a.G;
   if (!(info & kInfoValid)) return;
-  // a block that changes the sequence's state (S_0 and the ring by a fold, the
-  // pointers and flag) first makes sure that every group's precompute block
-  // finished, so that a sequence given up keeps its state whole
   const float *first = a.work + static_cast<size_t>(b) * a.H * stride;
-  const int st_new = (info >> 8) & 0xff;
-  bool checked = false;
-  if (kFuse && (info & kInfoFold)) {
-    if (!sequence_records_valid(first, a.G, HpG, stride, kVwInfo, kInfoValid)) return;
-    checked = true;
-    const int cs = reinterpret_cast<const int *>(wk)[kVwFoldCS];
-    const int fc = cs & 0xff, fst = (cs >> 8) & 0xff;
-    if (!rssm_check(fc <= L && fst < L && st_new < L, a.err)) return;
-    const size_t bg = static_cast<size_t>(b) * a.G + g;
-    // stage the c committed slots of this head's v ring and the group's k ring
-    unsigned char *sv = vsm;
-    unsigned char *sk = vsm + static_cast<size_t>(L) * d * es;
-    const unsigned char *gv = static_cast<const unsigned char *>(a.ring_v) + bh * L * d * es;
-    const unsigned char *gk = static_cast<const unsigned char *>(a.ring_k) + bg * L * N * es;
-    const int vrow = d * es / 16, krow = N * es / 16;
-    for (int idx = tid; idx < fc * (vrow + krow); idx += kThreads) {
-      const int j = idx / (vrow + krow), u = idx - j * (vrow + krow);
-      const size_t sl = static_cast<size_t>(wrapL(fst + j, L));
-      if (u < vrow)
-        cp_async16(sv + (static_cast<size_t>(j) * vrow + u) * 16, gv + (sl * vrow + u) * 16);
-      else
-        cp_async16(sk + (static_cast<size_t>(j) * krow + u - vrow) * 16, gk + (sl * krow + u - vrow) * 16);
-    }
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
-    if (tid == 0) {
-      // this block has read its fold operands: count it, and let the last of
-      // the group's head blocks overwrite the group's k slots
-      int *ctr = reinterpret_cast<int *>(a.work + (static_cast<size_t>(b) * a.H + g * HpG) * stride) + kVwCtr;
-      __threadfence();
-      s_last = (atomicAdd(ctr, 1) == HpG - 1) ? 1 : 0;
-      __threadfence();
-    }
-    __syncthreads();
-    // the drafts' entries at slots (start + c + m) mod L: this head's v and Delta
-    for (int m = 0; m < T; ++m) {
-      const int sl = checked_slot(wrapL(st_new + m, L), L, a.err);
-      const uint32_t *src =
-          reinterpret_cast<const uint32_t *>(static_cast<const TI *>(a.v) + ((static_cast<size_t>(b) * T + m) * a.H + i) * d);
-      uint32_t *dst = reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_v) + (bh * L + sl) * d);
-      for (int c = tid; c < d * es / 4; c += kThreads) dst[c] = src[c];
-      if (tid == 0) a.ring_dt[bh * L + sl] = a.dt[(static_cast<size_t>(b) * T + m) * a.H + i];
-      if (s_last) {
-        const uint32_t *ks = reinterpret_cast<const uint32_t *>(static_cast<const TI *>(a.k) +
-                                                                ((static_cast<size_t>(b) * T + m) * a.G + g) * N);
-        uint32_t *kd = reinterpret_cast<uint32_t *>(static_cast<TI *>(a.ring_k) + (bg * L + sl) * N);
-        for (int c = tid; c < N * es / 4; c += kThreads) kd[c] = ks[c];
-      }
-    }
-    // S_0 <- abar_f S_0 + sum_j w^f_j v_j k_j^T on the registers, written back
-    const float abf = wk[kVwFoldAbar];
-#pragma unroll
-    for (int pp = 0; pp < kSPass; ++pp) {
-      s[pp].x *= abf;
-      s[pp].y *= abf;
-      s[pp].z *= abf;
-      s[pp].w *= abf;
-    }
-    const TI *vst = reinterpret_cast<const TI *>(sv);
-    const TI *kst = reinterpret_cast<const TI *>(sk);
-    for (int j = 0; j < fc; ++j) {
-      const float4 kv = load4(kst + static_cast<size_t>(j) * N + col);
-      const float wj = wk[kVwFoldW + j];
-#pragma unroll
-      for (int pp = 0; pp < kSPass; ++pp) {
-        const int r = row0 + pp * RPP;
-        const float wv = (r < d) ? wj * load1(vst + static_cast<size_t>(j) * d + r) : 0.f;
-        s[pp].x = fmaf(wv, kv.x, s[pp].x);
-        s[pp].y = fmaf(wv, kv.y, s[pp].y);
-        s[pp].z = fmaf(wv, kv.z, s[pp].z);
-        s[pp].w = fmaf(wv, kv.w, s[pp].w);
-      }
-    }
-    float *S0w = a.S + bh * d * N;
-#pragma unroll
-    for (int pp = 0; pp < kSPass; ++pp) {
-      const int r = row0 + pp * RPP;
-      if (r < d) stg_stream4(S0w + static_cast<size_t>(r) * N + col, s[pp]);
-    }
-  }
 
   // S_0 q_s, PB passes x NT drafts reduced together; the reducing lane writes y
   static_assert(NT <= LPR, "drafts per lane group");
@@ -766,23 +670,19 @@ __global__ void __launch_bounds__(kThreads, NT == 8 ? 2 : 4) m2_vstream_kernel(M
     if ((lane % SPAN) == 0 && r < d && sq < T)
       store1(y + ((static_cast<size_t>(b) * T + sq) * a.H + i) * d + r, fmaf(wk[sq], x[0], wk[kVwBuf + sq * d + r]));
   }
-  if (i == 0 && warp == 0 && (checked || sequence_records_valid(first, a.G, HpG, stride, kVwInfo, kInfoValid)) &&
-      lane == 0) {
+  // the flag, once every group's precompute block of the sequence finished,
+  // so that a sequence given up keeps its state whole
+  if (i == 0 && warp == 0 && sequence_records_valid(first, a.G, HpG, stride, kVwInfo, kInfoValid) && lane == 0)
     a.flag[b] = ((info & 0xff) + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
-    if (kFuse && (info & kInfoFold)) {  // the flush this round carried out
-      a.start[b] = st_new;
-      a.count[b] = 0;
-    }
-  }
 }
 
-template <int N, int NT, bool kFuse, typename TI, typename TO>
+template <int N, int NT, typename TI, typename TO>
 cudaError_t launch_vsplit(const M2Launch &a, cudaStream_t stream) {
   constexpr int es = sizeof(TI);
   const int HpG = a.H / a.G;
   const int stride = m2_verify_stride_floats(a.d, NT);
   const size_t psm = VPrepSmem(a.L, N, a.d, HpG, NT, es).total;
-  auto prep = m2_vprep_kernel<N, NT, kFuse, TI>;
+  auto prep = m2_vprep_kernel<N, NT, TI>;
   cudaError_t e;
   if (psm > 48 * 1024 &&
       (e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psm))) !=
@@ -790,17 +690,13 @@ cudaError_t launch_vsplit(const M2Launch &a, cudaStream_t stream) {
     return e;
   prep<<<static_cast<unsigned>(a.B) * a.G, 32 * HpG, psm, stream>>>(a, stride);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (!kFuse && m2_verify_tc_eligible(a)) return launch_m2_verify_tc(a, stride, stream);
-  const size_t ssm = kFuse ? static_cast<size_t>(a.L) * (a.d + N) * es : 0;
-  auto strm = m2_vstream_kernel<N, NT, kFuse, TI, TO>;
-  if (ssm > 48 * 1024 &&
-      (e = cudaFuncSetAttribute(strm, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm))) !=
-          cudaSuccess)
-    return e;
+  if (m2_verify_pipe_eligible(a)) return launch_m2_verify_pipe(a, stride, stream);
+  if (m2_verify_tc_eligible(a)) return launch_m2_verify_tc(a, stride, stream);
+  auto strm = m2_vstream_kernel<N, NT, TI, TO>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.H);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = ssm;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -810,31 +706,23 @@ cudaError_t launch_vsplit(const M2Launch &a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, strm, a, stride);
 }
 
-template <int N, bool kFuse, typename TI, typename TO>
+template <int N, typename TI, typename TO>
 cudaError_t launch_vsplit_t(const M2Launch &a, cudaStream_t stream) {
   switch (gdn_window_width(a.T)) {
-    case 1: return launch_vsplit<N, 1, kFuse, TI, TO>(a, stream);
-    case 4: return launch_vsplit<N, 4, kFuse, TI, TO>(a, stream);
-    default: return launch_vsplit<N, 8, kFuse, TI, TO>(a, stream);
+    case 1: return launch_vsplit<N, 1, TI, TO>(a, stream);
+    case 4: return launch_vsplit<N, 4, TI, TO>(a, stream);
+    default: return launch_vsplit<N, 8, TI, TO>(a, stream);
   }
 }
 
-template <bool kFuse, typename TI, typename TO>
+template <typename TI, typename TO>
 cudaError_t launch_vsplit_n(const M2Launch &a, cudaStream_t stream) {
   switch (a.n) {
-    case 32: return launch_vsplit_t<32, kFuse, TI, TO>(a, stream);
-    case 64: return launch_vsplit_t<64, kFuse, TI, TO>(a, stream);
-    case 128: return launch_vsplit_t<128, kFuse, TI, TO>(a, stream);
+    case 32: return launch_vsplit_t<32, TI, TO>(a, stream);
+    case 64: return launch_vsplit_t<64, TI, TO>(a, stream);
+    case 128: return launch_vsplit_t<128, TI, TO>(a, stream);
   }
   return cudaErrorInvalidValue;
-}
-
-template <bool kFuse>
-cudaError_t launch_vsplit_f(const M2Launch &a, cudaStream_t stream) {
-  if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_F32) return launch_vsplit_n<kFuse, bf16, float>(a, stream);
-  if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_BF16) return launch_vsplit_n<kFuse, bf16, bf16>(a, stream);
-  if (a.in_dtype == RSSM_F32 && a.y_dtype == RSSM_F32) return launch_vsplit_n<kFuse, float, float>(a, stream);
-  return launch_vsplit_n<kFuse, float, bf16>(a, stream);
 }
 
 }  // namespace
@@ -853,14 +741,11 @@ bool m2_verify_split_eligible(const M2Launch &a) {
          a16(a.S) && a16(a.ring_v) && a16(a.ring_k) && a16(a.ring_dt) && a16(a.v) && a16(a.k) && a16(a.q);
 }
 
-bool m2_verify_fused_eligible(const M2Launch &a) {
-  const int es = a.in_dtype == RSSM_BF16 ? 2 : 4;
-  return m2_verify_split_eligible(a) && !m2_verify_tc_eligible(a) && a.L <= 255 &&
-         static_cast<size_t>(a.L) * (a.d + a.n) * es <= 96u * 1024u;
-}
-
-cudaError_t launch_m2_verify_split(const M2Launch &a, bool fuse_flush, cudaStream_t stream) {
-  return fuse_flush ? launch_vsplit_f<true>(a, stream) : launch_vsplit_f<false>(a, stream);
+cudaError_t launch_m2_verify_split(const M2Launch &a, cudaStream_t stream) {
+  if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_F32) return launch_vsplit_n<bf16, float>(a, stream);
+  if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_BF16) return launch_vsplit_n<bf16, bf16>(a, stream);
+  if (a.in_dtype == RSSM_F32 && a.y_dtype == RSSM_F32) return launch_vsplit_n<float, float>(a, stream);
+  return launch_vsplit_n<float, bf16>(a, stream);
 }
 
 bool m2_decode_split_eligible(const M2Launch &a) {

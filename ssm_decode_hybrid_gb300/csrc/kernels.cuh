@@ -43,7 +43,7 @@ struct M2Launch {
 // rounded up to 16 bytes.
 __host__ __device__ constexpr int work_stride_floats(int d, int L) { return (4 + L + d + 3) & ~3; }
 
-enum class M2Kind { Baseline, Decode, DecodeFused, Verify, VerifyFused, SnapshotVerify };
+enum class M2Kind { Baseline, Decode, DecodeFused, Verify, SnapshotVerify };
 
 cudaError_t launch_m2(M2Kind kind, const M2Launch &a, cudaStream_t stream);
 
@@ -57,21 +57,21 @@ bool m2_decode_split_eligible(const M2Launch &a);
 cudaError_t launch_m2_decode_split(const M2Launch &a, bool fuse_flush, cudaStream_t stream);
 // Speculative verify through the caller's workspace (decode_split.cu): a
 // precompute kernel per (sequence, group), then a kernel streaming S_0 per
-// (sequence, head) for all T drafts.  Record per (sequence, head): a 48-float
-// header (abar_s, info, the fold of a pending flush: its abar, count, start
-// and up to kMaxL weights), then P buffer vectors of d rows, P = 1, 4 or 8 >= T.
-constexpr int kM2VerifyHeader = 48;
+// (sequence, head) for all T drafts.  Record per (sequence, head): a 16-float
+// header (abar_s, info), then P buffer vectors of d rows, P = 1, 4 or 8 >= T.
+constexpr int kM2VerifyHeader = 16;
 __host__ __device__ constexpr int m2_verify_stride_floats(int d, int P) { return (kM2VerifyHeader + P * d + 3) & ~3; }
 bool m2_verify_split_eligible(const M2Launch &a);
-// fuse_flush: a sequence flagged for a flush has its committed entries folded
-// into S_0 by the streaming kernel first (replay_flush, then the verify); only
-// on the CUDA-core stream (m2_verify_fused_eligible).
-bool m2_verify_fused_eligible(const M2Launch &a);
-cudaError_t launch_m2_verify_split(const M2Launch &a, bool fuse_flush, cudaStream_t stream);
+cudaError_t launch_m2_verify_split(const M2Launch &a, cudaStream_t stream);
 // Its streaming half on the tensor cores (verify_tc.cu): n = 128, d = 64,
 // two heads of a group per block, bf16 inputs, T >= 5.
 bool m2_verify_tc_eligible(const M2Launch &a);
 cudaError_t launch_m2_verify_tc(const M2Launch &a, int stride, cudaStream_t stream);
+// The same streaming half as the persistent TMA + tcgen05 pipeline
+// (verify_pipe.cu): n = 128, d = 64, two heads of a group per item, bf16
+// inputs, 2 <= T.
+bool m2_verify_pipe_eligible(const M2Launch &a);
+cudaError_t launch_m2_verify_pipe(const M2Launch &a, int stride, cudaStream_t stream);
 // One CTA per (sequence, head) with every load issued up front (decode_flat.cu).
 bool m2_decode_flat_eligible(const M2Launch &a);
 cudaError_t launch_m2_decode_flat(const M2Launch &a, bool fuse_flush, cudaStream_t stream);

@@ -384,9 +384,7 @@ cudaError_t launch_m2_t(M2Kind kind, const M2Launch &a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_m2(M2Kind kind, const M2Launch &a, cudaStream_t stream) {
-  if (kind == M2Kind::Verify && m2_verify_split_eligible(a)) return launch_m2_verify_split(a, false, stream);
-  if (kind == M2Kind::VerifyFused)  // only the fused two-launch verify; the caller flushes and verifies otherwise
-    return m2_verify_fused_eligible(a) ? launch_m2_verify_split(a, true, stream) : cudaErrorNotSupported;
+  if (kind == M2Kind::Verify && m2_verify_split_eligible(a)) return launch_m2_verify_split(a, stream);
   if ((kind == M2Kind::Decode || kind == M2Kind::DecodeFused) && m2_decode_split_eligible(a))
     return launch_m2_decode_split(a, kind == M2Kind::DecodeFused, stream);
   if ((kind == M2Kind::Decode || kind == M2Kind::DecodeFused) && m2_decode_flat_eligible(a))

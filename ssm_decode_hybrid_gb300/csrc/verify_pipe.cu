@@ -1,15 +1,22 @@
-// GDN chunked speculative verify, the S_0 stream as a persistent,
-// warp-specialised TMA + tcgen05 pipeline (sm_103a).
+// Speculative verify, the S_0 stream as a persistent, warp-specialised
+// TMA + tcgen05 pipeline (sm_103a), for both families.
 //
-// "ReplaySSM: Cache SSM Inputs, Not State" -- appendix "GDN: speculative
-// decoding": per (sequence, value head) the checkpoint meets the window's 2T
-// vectors once, Z = S_0 [k_1 .. k_T, q_1 .. q_T], and every output row follows
-// from its row of Z and the terms the precompute kernel of gdn_split.cu left
-// in the workspace (the solve is the one of verify_tc.cu).
+// "ReplaySSM: Cache SSM Inputs, Not State" -- "Algorithm -- speculative
+// decoding" and the appendix "GDN: speculative decoding": per item the
+// checkpoint meets the window's vectors once, Z = S_0 X, and every output row
+// follows from its row of Z and the terms the precompute kernel left in the
+// workspace.
+//   GDN:     an item is a (sequence, value head): 128 rows (d_v) x 128
+//            columns (d_k); X = [k_1 .. k_T, q_1 .. q_T] of its key head; each
+//            row is solved as verify_tc.cu does (gdn_split.cu's records).
+//   Mamba-2: an item is two heads of one group of a sequence: 2 x 64 rows
+//            (d) x 128 columns (n); X = [q_1 .. q_T] of the group; row r of
+//            head i gives y_s[r] = abar_s Z[r][s] + buf_s[r] (decode_split.cu's
+//            records).
 //
-// One CTA per SM walks the (sequence, value head) items of the grid.  Each
-// item's 128 x 128 fp32 block is four 128-row x 32-column chunks.  Roles:
-//   warp 0     TMA producer: each chunk lands in a stage of a five-stage ring,
+// One CTA per SM walks the items of the grid.  Each item's 128 x 128 fp32
+// block is four 128-row x 32-column chunks.  Roles:
+//   warp 0     TMA producer: each chunk lands in a stage of a six-stage ring,
 //              already in the 128-byte-swizzled K-major layout of the MMA's A
 //              operand (one cp.async.bulk.tensor box of 16 KB);
 //   warps 2-3  split: lo = S - tf32(S) of each landed chunk into the stage's
@@ -18,13 +25,13 @@
 //              hi + lo carries S to about 2^-21), and the item's window
 //              vectors (bf16, exact in tf32) into one of two B-operand slots;
 //   warp 1     MMA issuer: per chunk four tf32 MMAs on hi and four on lo
-//              (M = 128 rows, N = 16 vectors, K = 8) into one of two TMEM
+//              (M = 128 rows, N = 16 vectors, K = 8) into one of four TMEM
 //              accumulators; a commit frees the stage once they have read it;
 //   warps 4-19 epilogue, four groups of four warps taking every fourth item,
 //              each with its own TMEM accumulator: once an item's accumulator
 //              is complete, thread r of its group reads row r (tcgen05.ld) and
-//              solves it as verify_tc.cu does (four groups, so that the loads
-//              of the solve's inputs of several items are in flight at once).
+//              finishes it (four groups, so that the loads of the rows' inputs
+//              of several items are in flight at once).
 // So the S_0 loads of later items are always in flight while earlier items
 // are split, multiplied and solved; no thread holds S_0 in registers.
 // Every wait is bounded (RSSM_EBIT_TIMEOUT); after one runs out each role
@@ -33,6 +40,8 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "kernels.cuh"
 #include "tc05.cuh"
 
@@ -40,13 +49,14 @@ namespace rssm {
 
 namespace {
 
-constexpr int kPvStages = 5;
-constexpr int kPvRows = 128;                        // dv: MMA M, TMEM lanes
-constexpr int kPvK = 128;                           // dk
+constexpr int kPvStages = 6;
+constexpr int kPvRows = 128;                        // rows of an item: MMA M, TMEM lanes
+constexpr int kPvK = 128;                           // columns of S_0 (d_k, n)
+constexpr int kPvM2Rows = 64;                       // Mamba-2 head dimension d (two heads per item)
 constexpr int kPvChunks = 4;                        // 32-column chunks of a row
 constexpr uint32_t kPvChunkBytes = kPvRows * 128;   // 16 KB: one TMA box
-constexpr uint32_t kPvStageBytes = 2 * kPvChunkBytes;  // hi, lo
-constexpr int kPvN = 16;                            // 8 key columns, 8 query columns
+constexpr uint32_t kPvStageBytes = 2 * kPvChunkBytes;  // hi (the landed chunk), lo
+constexpr int kPvN = 16;                            // GDN: 8 key, 8 query columns; Mamba-2: 8 query columns, 8 zero
 constexpr uint32_t kPvXChunkBytes = kPvN * 128;     // 2 KB
 constexpr uint32_t kPvXBytes = kPvChunks * kPvXChunkBytes;  // 8 KB per slot
 constexpr uint32_t kPvStagesOff = 0;
@@ -54,6 +64,7 @@ constexpr uint32_t kPvXOff = kPvStagesOff + kPvStages * kPvStageBytes;
 constexpr uint32_t kPvHdrOff = kPvXOff + 2 * kPvXBytes;
 constexpr int kPvGroups = 4;                        // epilogue groups of 128 threads
 constexpr uint32_t kPvSmem = kPvHdrOff + kPvGroups * kGdnWorkHeader * 4 + 1024;  // + alignment slack
+static_assert(kM2VerifyHeader <= kGdnWorkHeader, "record header staging");
 constexpr int kPvThreads = 128 + kPvGroups * 128;
 constexpr uint32_t kPvTmemCols = kPvGroups * 16;    // one accumulator of 16 columns per group
 constexpr int kInfoValid = 1 << 16;
@@ -134,9 +145,27 @@ struct PvBars {
   uint64_t drain;             // every MMA issued has completed (commit)
 };
 
-template <typename TI, typename TU, typename TO>
+// Items of each family, and where vector v (row v of X) of item `it` comes
+// from (nullptr: a zero row).
+__device__ __forceinline__ int pv_items(const GdnLaunch &a) { return a.B * a.Hv; }
+__device__ __forceinline__ int pv_items(const M2Launch &a) { return a.B * (a.H / 2); }
+template <typename TI>
+__device__ __forceinline__ const TI *pv_vector(const GdnLaunch &a, int it, int v) {
+  const int b = it / a.Hv, kh = (it - b * a.Hv) / (a.Hv / a.Hk), m = v & 7;
+  if (m >= a.T) return nullptr;
+  return static_cast<const TI *>(v < 8 ? a.k : a.q) + ((static_cast<size_t>(b) * a.T + m) * a.Hk + kh) * kPvK;
+}
+template <typename TI>
+__device__ __forceinline__ const TI *pv_vector(const M2Launch &a, int it, int v) {
+  const int hp = a.H / 2, b = it / hp, g = 2 * (it - b * hp) / (a.H / a.G);
+  if (v >= a.T) return nullptr;
+  return static_cast<const TI *>(a.q) + ((static_cast<size_t>(b) * a.T + v) * a.G + g) * kPvK;
+}
+
+template <typename LaunchT, typename TI, typename TU, typename TO>
 __global__ void __launch_bounds__(kPvThreads, 1)
-    gdn_verify_pipe_kernel(const __grid_constant__ CUtensorMap s0map, GdnLaunch a, int stride, int P) {
+    verify_pipe_kernel(const __grid_constant__ CUtensorMap s0map, LaunchT a, int stride, int P) {
+  constexpr bool kM2 = std::is_same<LaunchT, M2Launch>::value;
   extern __shared__ unsigned char pv_raw[];
   __shared__ PvBars bars;
   __shared__ uint32_t s_tmem;
@@ -144,8 +173,7 @@ __global__ void __launch_bounds__(kPvThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = (smem_addr(pv_raw) + 1023u) & ~1023u;
   const int T = a.T, L = a.L;
-  const int HpK = a.Hv / a.Hk;
-  const int items = a.B * a.Hv;
+  const int items = pv_items(a);
   volatile int *abort = &s_abort;
 
   if (tid == 0) {
@@ -236,14 +264,11 @@ __global__ void __launch_bounds__(kPvThreads, 1)
     constexpr int kXUnits = kPvN * (kPvK / 4) / 64;  // 16-byte units of the vectors per thread
     uint2 xr[kXUnits];
     auto load_x = [&](int it) {
-      const int b = it / a.Hv, kh = (it - b * a.Hv) / HpK;
 #pragma unroll
       for (int j = 0; j < kXUnits; ++j) {
-        const int idx = ct + 64 * j, v = idx / (kPvK / 4), u = idx % (kPvK / 4), m = v & 7;
-        xr[j] = make_uint2(0u, 0u);
-        if (m < T)
-          xr[j] = *reinterpret_cast<const uint2 *>(static_cast<const TI *>(v < 8 ? a.k : a.q) +
-                                                   ((static_cast<size_t>(b) * T + m) * a.Hk + kh) * kPvK + 4 * u);
+        const int idx = ct + 64 * j, v = idx / (kPvK / 4), u = idx % (kPvK / 4);
+        const TI *src = pv_vector<TI>(a, it, v);
+        xr[j] = src != nullptr ? *reinterpret_cast<const uint2 *>(src + 4 * u) : make_uint2(0u, 0u);
       }
     };
     static_assert(sizeof(TI) == 2, "bf16 window vectors");
@@ -252,8 +277,8 @@ __global__ void __launch_bounds__(kPvThreads, 1)
     for (int it = blockIdx.x; it < items && !*abort; it += gridDim.x, ++k) {
       const int sl = k & 1;
       if (!pv_wait(&bars.xempty[sl], ((k >> 1) & 1) ^ 1, abort)) break;
-      // vector v: key v (v < 8) or query v - 8, zero past T; 16-byte unit u of
-      // chunk u / 8 at atom v / 8, row v % 8, unit (u % 8) ^ (v % 8); bf16 to fp32 is exact
+      // vector v (pv_vector); 16-byte unit u of chunk u / 8 at atom v / 8,
+      // row v % 8, unit (u % 8) ^ (v % 8); bf16 to fp32 is exact
       const uint32_t xb = base + kPvXOff + sl * kPvXBytes;
 #pragma unroll
       for (int j = 0; j < kXUnits; ++j) {
@@ -288,70 +313,109 @@ __global__ void __launch_bounds__(kPvThreads, 1)
       if (!ok) break;
     }
   } else {
-    // ---- epilogue: group g solves items k = g, g + 4, ...; thread r row r -------
+    // ---- epilogue: group g finishes items k = g, g + 4, ...; thread r row r ----
     const int g = (warp - 4) / 4;   // group
-    const int r = (tid - 128) % 128;  // TMEM lane, state row
+    const int r = (tid - 128) % 128;  // TMEM lane, row of the item
     const int ew = warp % 4;          // this warp reads TMEM lanes 32 ew .. 32 ew + 31
-    float *shdr = reinterpret_cast<float *>(pv_raw + (base - smem_addr(pv_raw)) + kPvHdrOff) + g * kGdnWorkHeader;
-    pdl_wait();  // the precompute grid has finished: workspace, drafts' k and g, pointers
+    pdl_wait();  // the precompute grid has finished: workspace, drafts' entries, pointers
     // the group's 128 threads take every decision to stop together (named
     // barriers with an OR), since a named barrier has no time limit
     int k = g;
     for (int it = blockIdx.x + g * gridDim.x; it < items; it += kPvGroups * gridDim.x, k += kPvGroups) {
-      const int b = it / a.Hv, i = it - b * a.Hv;
-      const size_t bh = static_cast<size_t>(b) * a.Hv + i;
-      const float *wk = a.work + bh * stride;
-      if (named_bar_or(1 + 2 * g, 128, *abort != 0)) break;  // the previous item's header is no longer read
-      for (int c = r; c < kGdnWorkHeader; c += 128) shdr[c] = wk[c];
-      float pk[kMaxT], pq[kMaxT], pv[kMaxT];
+      if constexpr (kM2) {
+        const int hp = a.H / 2, b = it / hp, i = 2 * (it - b * hp) + (r >> 6), row = r & (kPvM2Rows - 1);
+        const float *wk = a.work + (static_cast<size_t>(b) * a.H + i) * stride;
+        if (named_bar_or(1 + 2 * g, 128, *abort != 0)) break;
+        // this row's terms: abar_s, buf_s[row] and the record's info, loaded
+        // while the MMAs run
+        float ab[kMaxT], buf[kMaxT];
 #pragma unroll
-      for (int m = 0; m < kMaxT; ++m) {
-        pk[m] = pq[m] = pv[m] = 0.f;
-        if (m < T) {
-          pk[m] = wk[kGwBuf + m * kPvRows + r];
-          pq[m] = wk[kGwBuf + (P + m) * kPvRows + r];  // the record holds P key vectors, then the queries
-          pv[m] = load1(static_cast<const TI *>(a.v) + ((static_cast<size_t>(b) * T + m) * a.Hv + i) * kPvRows + r);
-        }
-      }
-      const bool failed = !pv_wait(&bars.afull[g], (k / kPvGroups) & 1, abort);
-      if (named_bar_or(2 + 2 * g, 128, failed)) break;  // the header is in place; the accumulator is complete
-      tc05::fence_after_sync();
-      float z[16];
-      pv_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(g * kPvN), z);
-      tc05::fence_before_sync();
-      mbar_arrive(&bars.aempty[g]);
-      const int info = __float_as_int(shdr[kGwInfo]);
-      if ((info & kInfoValid) && rssm_check(((info >> 8) & 0xff) < L && (info & 0xff) + T <= L, a.err)) {
-        const int h = info & 0xff, st = (info >> 8) & 0xff;
-        const float abar = shdr[kGwAbar];
-        TO *y = static_cast<TO *>(a.y);
-        TU *ru = static_cast<TU *>(a.ring_u) + bh * L * kPvRows;
-        float u[kMaxT];
-#pragma unroll
-        for (int m = 0; m < kMaxT; ++m) {
-          u[m] = 0.f;
-          if (m < T) {
-            const size_t tvm = (static_cast<size_t>(b) * T + m) * a.Hv + i;
-            const float Shk = fmaf(abar, z[m], pk[m]);
-            const float Shq = fmaf(abar, z[8 + m], pq[m]);
-            const float eG = shdr[kGwEG + m];
-            float um = shdr[kGwBeta + m] * (pv[m] - eG * Shk);
-#pragma unroll
-            for (int mp = 0; mp < m; ++mp) um = fmaf(-shdr[kGwA + m * kMaxT + mp], u[mp], um);
-            u[m] = um;
-            float ym = eG * Shq;
-#pragma unroll
-            for (int mp = 0; mp <= m; ++mp) ym = fmaf(shdr[kGwY + m * kMaxT + mp], u[mp], ym);
-            store1(y + tvm * kPvRows + r, ym);
-            store1(ru + static_cast<size_t>(checked_slot((st + h + m) % L, L, a.err)) * kPvRows + r, um);
+        for (int s2 = 0; s2 < kMaxT; ++s2) {
+          ab[s2] = buf[s2] = 0.f;
+          if (s2 < T) {
+            ab[s2] = wk[s2];
+            buf[s2] = wk[kM2VerifyHeader + s2 * kPvM2Rows + row];
           }
         }
+        const int info = reinterpret_cast<const int *>(wk)[kMaxT];
+        const bool failed = !pv_wait(&bars.afull[g], (k / kPvGroups) & 1, abort);
+        if (named_bar_or(2 + 2 * g, 128, failed)) break;  // the accumulator is complete
+        tc05::fence_after_sync();
+        float z[16];
+        pv_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(g * kPvN), z);
+        tc05::fence_before_sync();
+        mbar_arrive(&bars.aempty[g]);
+        if (info & kInfoValid) {
+          TO *y = static_cast<TO *>(a.y);
+#pragma unroll
+          for (int s2 = 0; s2 < kMaxT; ++s2)
+            if (s2 < T)
+              store1(y + ((static_cast<size_t>(b) * T + s2) * a.H + i) * kPvM2Rows + row, fmaf(ab[s2], z[s2], buf[s2]));
+        }
         // the flag, once every group's precompute block of the sequence finished
-        if (i == 0 && ew == 0 &&
-            sequence_records_valid(a.work + static_cast<size_t>(b) * a.Hv * stride, a.Hk, HpK, stride, kGwInfo,
-                                   kInfoValid) &&
-            lane == 0)
-          a.flag[b] = (h + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
+        if (i == 0 && ew == 0) {
+          const float *first = a.work + static_cast<size_t>(b) * a.H * stride;
+          if ((info & kInfoValid) && sequence_records_valid(first, a.G, a.H / a.G, stride, kMaxT, kInfoValid) &&
+              lane == 0)
+            a.flag[b] = ((info & 0xff) + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
+        }
+      } else {
+        const int b = it / a.Hv, i = it - b * a.Hv;
+        const size_t bh = static_cast<size_t>(b) * a.Hv + i;
+        const float *wk = a.work + bh * stride;
+        float *shdr = reinterpret_cast<float *>(pv_raw + (base - smem_addr(pv_raw)) + kPvHdrOff) + g * kGdnWorkHeader;
+        if (named_bar_or(1 + 2 * g, 128, *abort != 0)) break;  // the previous item's header is no longer read
+        for (int c = r; c < kGdnWorkHeader; c += 128) shdr[c] = wk[c];
+        float pk[kMaxT], pq[kMaxT], pv[kMaxT];
+#pragma unroll
+        for (int m = 0; m < kMaxT; ++m) {
+          pk[m] = pq[m] = pv[m] = 0.f;
+          if (m < T) {
+            pk[m] = wk[kGwBuf + m * kPvRows + r];
+            pq[m] = wk[kGwBuf + (P + m) * kPvRows + r];  // the record holds P key vectors, then the queries
+            pv[m] = load1(static_cast<const TI *>(a.v) + ((static_cast<size_t>(b) * T + m) * a.Hv + i) * kPvRows + r);
+          }
+        }
+        const bool failed = !pv_wait(&bars.afull[g], (k / kPvGroups) & 1, abort);
+        if (named_bar_or(2 + 2 * g, 128, failed)) break;  // the header is in place; the accumulator is complete
+        tc05::fence_after_sync();
+        float z[16];
+        pv_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(g * kPvN), z);
+        tc05::fence_before_sync();
+        mbar_arrive(&bars.aempty[g]);
+        const int info = __float_as_int(shdr[kGwInfo]);
+        if ((info & kInfoValid) && rssm_check(((info >> 8) & 0xff) < L && (info & 0xff) + T <= L, a.err)) {
+          const int h = info & 0xff, st = (info >> 8) & 0xff;
+          const float abar = shdr[kGwAbar];
+          TO *y = static_cast<TO *>(a.y);
+          TU *ru = static_cast<TU *>(a.ring_u) + bh * L * kPvRows;
+          float u[kMaxT];
+#pragma unroll
+          for (int m = 0; m < kMaxT; ++m) {
+            u[m] = 0.f;
+            if (m < T) {
+              const size_t tvm = (static_cast<size_t>(b) * T + m) * a.Hv + i;
+              const float Shk = fmaf(abar, z[m], pk[m]);
+              const float Shq = fmaf(abar, z[8 + m], pq[m]);
+              const float eG = shdr[kGwEG + m];
+              float um = shdr[kGwBeta + m] * (pv[m] - eG * Shk);
+#pragma unroll
+              for (int mp = 0; mp < m; ++mp) um = fmaf(-shdr[kGwA + m * kMaxT + mp], u[mp], um);
+              u[m] = um;
+              float ym = eG * Shq;
+#pragma unroll
+              for (int mp = 0; mp <= m; ++mp) ym = fmaf(shdr[kGwY + m * kMaxT + mp], u[mp], ym);
+              store1(y + tvm * kPvRows + r, ym);
+              store1(ru + static_cast<size_t>(checked_slot((st + h + m) % L, L, a.err)) * kPvRows + r, um);
+            }
+          }
+          // the flag, once every group's precompute block of the sequence finished
+          if (i == 0 && ew == 0 &&
+              sequence_records_valid(a.work + static_cast<size_t>(b) * a.Hv * stride, a.Hk, a.Hv / a.Hk, stride,
+                                     kGwInfo, kInfoValid) &&
+              lane == 0)
+            a.flag[b] = (h + 2 * T > L) ? 1 : 0;  // early flush, one window ahead
+        }
       }
     }
   }
@@ -373,27 +437,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <typename TU, typename TO>
-cudaError_t launch_pv(const GdnLaunch &a, int stride, int P, cudaStream_t stream) {
+// S_0 as a 2-D fp32 tensor: 128 columns, `rows` rows; boxes of 128 rows x 32
+// columns (128 bytes) in the 128-byte swizzle.
+bool pv_map(CUtensorMap *map, float *S, long long rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (enc == nullptr) return cudaErrorNotSupported;
-  // S_0 as a 2-D fp32 tensor: 128 columns (d_k), B Hv 128 rows; boxes of
-  // 128 rows x 32 columns (128 bytes) in the 128-byte swizzle
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kPvK), static_cast<cuuint64_t>(a.B) * a.Hv * kPvRows};
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kPvK), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kPvK) * 4};
   const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kPvRows)};
   const cuuint32_t estr[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.S, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-      CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  auto kern = gdn_verify_pipe_kernel<bf16, TU, TO>;
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, S, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <typename LaunchT, typename TU, typename TO>
+cudaError_t launch_pv(const LaunchT &a, const CUtensorMap &map, int items, int stride, int P, cudaStream_t stream) {
+  auto kern = verify_pipe_kernel<LaunchT, bf16, TU, TO>;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kPvSmem))) !=
       cudaSuccess)
     return e;
-  const int items = a.B * a.Hv;
   const int grid = items < sm_count() ? items : sm_count();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -417,11 +481,30 @@ bool gdn_verify_pipe_eligible(const GdnLaunch &a) {
 }
 
 cudaError_t launch_gdn_verify_pipe(const GdnLaunch &a, int stride, int P, cudaStream_t stream) {
+  CUtensorMap map;
+  if (!pv_map(&map, a.S, static_cast<long long>(a.B) * a.Hv * kPvRows)) return cudaErrorInvalidValue;
+  const int items = a.B * a.Hv;
   const bool ub = a.u_dtype == RSSM_BF16, yb = a.y_dtype == RSSM_BF16;
-  if (ub && yb) return launch_pv<bf16, bf16>(a, stride, P, stream);
-  if (ub) return launch_pv<bf16, float>(a, stride, P, stream);
-  if (yb) return launch_pv<float, bf16>(a, stride, P, stream);
-  return launch_pv<float, float>(a, stride, P, stream);
+  if (ub && yb) return launch_pv<GdnLaunch, bf16, bf16>(a, map, items, stride, P, stream);
+  if (ub) return launch_pv<GdnLaunch, bf16, float>(a, map, items, stride, P, stream);
+  if (yb) return launch_pv<GdnLaunch, float, bf16>(a, map, items, stride, P, stream);
+  return launch_pv<GdnLaunch, float, float>(a, map, items, stride, P, stream);
+}
+
+bool m2_verify_pipe_eligible(const M2Launch &a) {
+  // two heads of one group per item; up to four queries the CUDA-core stream
+  // is faster (it reads S_0 at a higher fraction of the bandwidth)
+  return a.n == kPvK && a.d == kPvM2Rows && a.in_dtype == RSSM_BF16 && a.H % 2 == 0 && (a.H / a.G) % 2 == 0 &&
+         a.T >= 5 && a.T <= kMaxT && static_cast<long long>(a.B) * a.H * kPvM2Rows < (1ll << 31) &&
+         (reinterpret_cast<uintptr_t>(a.S) & 15u) == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_m2_verify_pipe(const M2Launch &a, int stride, cudaStream_t stream) {
+  CUtensorMap map;
+  if (!pv_map(&map, a.S, static_cast<long long>(a.B) * a.H * kPvM2Rows)) return cudaErrorInvalidValue;
+  const int items = a.B * (a.H / 2);
+  if (a.y_dtype == RSSM_BF16) return launch_pv<M2Launch, float, bf16>(a, map, items, stride, 0, stream);
+  return launch_pv<M2Launch, float, float>(a, map, items, stride, 0, stream);
 }
 
 }  // namespace rssm

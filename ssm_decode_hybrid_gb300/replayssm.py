@@ -395,8 +395,7 @@ def replay_spec_verify(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch
 
 
 def replay_spec_verify_fused(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
-    """replay_flush, then replay_spec_verify, with the flush of each flagged
-    sequence folded in by the launch that streams S_0.  Arguments as
+    """replay_flush, then replay_spec_verify, in one call.  Arguments as
     replay_spec_verify."""
     B, H, G, d, n, L = state.shape
     T = v.shape[1]

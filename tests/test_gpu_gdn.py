@@ -297,14 +297,14 @@ def run_verify_fused(shape, T, rounds, seed, sample=None, workspace_T=8):
 @pytest.mark.parametrize("T", [1, 2, 4, 6, 8])
 def test_chunked_verify_fused_parity(T, workspace_T):
     """gdn_replay_verify_fused == gdn_replay_flush + gdn_replay_verify, over
-    rounds whose early flushes fold windows that the next drafts overwrite;
-    T = 1 and the one-launch path take the unfused fallback."""
+    rounds whose early flushes empty windows whose slots the next drafts
+    overwrite; pipelined (T >= 2), CUDA-core (T = 1) and one-launch verify."""
     shape = wl.GdnShape(B=8, Hv=8, Hk=4, dk=128, dv=128, L=16, in_dtype=wl.BF16)
     run_verify_fused(shape, T, rounds=12, seed=340 + T, workspace_T=workspace_T)
 
 
 def test_chunked_verify_fused_dtypes_and_window_equal_to_ring():
-    # bf16 u and bf16 keys in the fold; T = L = 4: every round folds what it committed
+    # bf16 u and bf16 keys in the flush; T = L = 4: every round flushes what it committed
     run_verify_fused(wl.GdnShape(B=4, Hv=4, Hk=2, dk=128, dv=128, L=8, in_dtype=wl.BF16, u_dtype=wl.BF16), 4,
                      rounds=10, seed=350)
     run_verify_fused(wl.GdnShape(B=5, Hv=4, Hk=4, dk=128, dv=128, L=4, in_dtype=wl.BF16), 4, rounds=8, seed=351)
@@ -312,6 +312,7 @@ def test_chunked_verify_fused_dtypes_and_window_equal_to_ring():
 
 def test_chunked_verify_fused_full_batch_sampled():
     """The GDN layer at its own size (B = 256, Hv = 32, Hk = 16, T = 4, L = 16),
-    verify with the flush fused in + commit, 16 rounds, eight sampled sequences."""
+    the pending flush, the verify and the commit, 16 rounds, eight sampled
+    sequences."""
     run_verify_fused(wl.GDN_LAYER, 4, rounds=16, seed=wl.SEED_GDN + 60,
                      sample=[0, 1, 63, 128, 200, 230, 254, 255], workspace_T=4)

@@ -457,14 +457,15 @@ def run_spec_fused(shape, T, rounds, seed, sample=None, workspace=True):
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 6])
 def test_spec_verify_fused_parity(T, workspace):
     """replay_spec_verify_fused == replay_flush + replay_spec_verify, over
-    rounds whose early flushes fold windows that the next drafts overwrite
-    (c + T > L); T = 6 and the one-launch path take the unfused fallback."""
+    rounds whose early flushes empty windows whose slots the next drafts
+    overwrite (c + T > L); two-launch (T <= 4 CUDA-core and T = 6 tensor-core
+    streams) and one-launch verify."""
     shape = wl.Mamba2Shape(B=12, H=8, G=2, d=64, n=128, L=16, in_dtype=wl.BF16)
     run_spec_fused(shape, T, rounds=14, seed=140 + T, workspace=workspace)
 
 
 def test_spec_verify_fused_small_shapes():
-    # fp32 inputs with n = 32, ragged heads; T = L (every round folds what it committed)
+    # fp32 inputs with n = 32, ragged heads; T = L (every round flushes what it committed)
     run_spec_fused(wl.Mamba2Shape(B=4, H=6, G=3, d=20, n=32, L=8, in_dtype=wl.F32), 3, rounds=10, seed=141)
     run_spec_fused(wl.Mamba2Shape(B=5, H=8, G=2, d=64, n=128, L=4, in_dtype=wl.BF16), 4, rounds=8, seed=142)
     run_spec_fused(wl.Mamba2Shape(B=4, H=8, G=1, d=48, n=64, L=12, in_dtype=wl.BF16), 4, rounds=10, seed=143)
@@ -472,7 +473,7 @@ def test_spec_verify_fused_small_shapes():
 
 def test_spec_fused_full_batch_sampled():
     """The speculative workload at its own size: B = 512, T = 4, L = 16,
-    accepted ~ U{0..4}, verify with the flush fused in + commit, 24 rounds;
+    accepted ~ U{0..4}, the pending flush, the verify and the commit, 24 rounds;
     ten sampled sequences against the oracle."""
     run_spec_fused(wl.SPEC_MAMBA2, 4, rounds=24, seed=wl.SEED_SPEC,
                    sample=[0, 1, 100, 255, 256, 311, 400, 480, 510, 511])
