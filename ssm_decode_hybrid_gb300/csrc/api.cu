@@ -314,7 +314,7 @@ rssm_status replay_decode_step_fused(const rssm_m2_dims *dims, const rssm_m2_rep
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_m2(M2Kind::DecodeFused, a, cs);
   if (e != cudaErrorNotSupported) return cuda_status(e);
-  // shapes outside the pipelined kernel: the decode step, then the flush
+  // shapes outside the fused kernels: the decode step, then the flush
   e = launch_m2(M2Kind::Decode, a, cs);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_flush(m2_flush_launch(d, s, A), cs));

@@ -158,9 +158,44 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   float *scoef = reinterpret_cast<float *>(psm + lay.coef) + w * NV * kMaxL;
 
   // dots of every key (committed j < h, then drafts m) with every window vector
-  // x_v (v < NT: k_v, v >= NT: q_{v-NT}); pairs spread over the lane groups,
-  // V of them reduced together
-  {
+  // x_v (v < NT: k_v, v >= NT: q_{v-NT}), zero for v past the drafts
+  if constexpr (sizeof(TI) == 2) {
+    // bf16: D[e][v] on the tensor cores (m16n8k16, fp32 out), one warp per
+    // tile of 16 keys x 8 vectors.  Rows past the last key and vectors past
+    // the last draft read key 0 and vector 0 and store zero or nothing.
+    const int nw = blockDim.x / 32;
+    const int ne = h + T, mt_n = (ne + 15) / 16, nt_n = (NV + 7) / 8;
+    for (int t = w; t < mt_n * nt_n; t += nw) {
+      const int mt = t / nt_n, nt = t - mt * nt_n;
+      const int e = mt * 16 + (lane & 15), ec = e < ne ? e : 0;
+      const TI *key = ec < h ? kring + static_cast<size_t>(wrapL(st + ec, L)) * N : kin + (ec - h) * N;
+      const int v = nt * 8 + (lane & 7), mv = v < NT ? v : v - NT;
+      const TI *xv = (v < NV && mv < T) ? (v < NT ? kin : qin) + mv * N : kin;
+      const uint32_t aaddr = smem_addr(key + (lane >> 4) * 8);
+      const uint32_t baddr = smem_addr(xv + ((lane >> 3) & 1) * 8);
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < N / 16; ++kk) {
+        uint32_t af[4], bfr[2];
+        ldsm_x4(af, aaddr + kk * 32);
+        ldsm_x2(bfr, baddr + kk * 32);
+        mma_16816_bf16(c, af, bfr);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int er = mt * 16 + (lane >> 2) + (j >> 1) * 8, vc = nt * 8 + 2 * (lane & 3) + (j & 1);
+        const int mvc = vc < NT ? vc : vc - NT;
+        if (er < ne && vc < NV) {
+          const float x = mvc < T ? c[j] : 0.f;
+          if (er < h)
+            sD[vc * kMaxL + er] = x;
+          else
+            sK[(er - h) * NV + vc] = x;
+        }
+      }
+    }
+  } else {
+    // pairs spread over the lane groups, V of them reduced together
     constexpr int V = LPR >= 4 ? 4 : LPR;
     constexpr int RPW = 32 / LPR;
     const int col = (lane % LPR) * 4;

@@ -47,10 +47,6 @@ enum class M2Kind { Baseline, Decode, DecodeFused, Verify, SnapshotVerify };
 
 cudaError_t launch_m2(M2Kind kind, const M2Launch &a, cudaStream_t stream);
 
-// Persistent bulk-copy pipelined decode step (decode_pipe.cu).  Eligible when
-// every bulk copy is 16-byte sized and aligned; `launched` reports whether the
-// kernel ran (false: the caller falls back to the per-head kernel).
-bool m2_decode_pipe_eligible(const M2Launch &a);
 // Two launches through the caller's workspace (decode_split.cu): a precompute
 // kernel per (sequence, group), then a kernel streaming S_0 per (sequence, head).
 bool m2_decode_split_eligible(const M2Launch &a);
@@ -73,11 +69,11 @@ cudaError_t launch_m2_verify_tc(const M2Launch &a, int stride, cudaStream_t stre
 bool m2_verify_pipe_eligible(const M2Launch &a);
 cudaError_t launch_m2_verify_pipe(const M2Launch &a, int stride, cudaStream_t stream);
 // One CTA per (sequence, head) with every load issued up front (decode_flat.cu).
+// fuse_flush (here and in launch_m2_decode_split): a sequence whose buffer
+// fills is folded into S_0 in the same launch (count and flag end at 0)
+// instead of being flagged for replay_flush.
 bool m2_decode_flat_eligible(const M2Launch &a);
 cudaError_t launch_m2_decode_flat(const M2Launch &a, bool fuse_flush, cudaStream_t stream);
-// fuse_flush: a sequence whose buffer fills is folded into S_0 in the same
-// launch (count and flag end at 0) instead of being flagged for replay_flush.
-cudaError_t launch_m2_decode_pipe(const M2Launch &a, bool fuse_flush, cudaStream_t stream, bool *launched);
 cudaError_t launch_replay_commit(int B, int T, int L, const int32_t *accepted, int32_t *count, int32_t *err,
                                  cudaStream_t stream);
 cudaError_t launch_snapshot_commit(int B, int T, const int32_t *accepted, int32_t *cur, int32_t *err,

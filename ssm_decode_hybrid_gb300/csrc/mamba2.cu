@@ -389,11 +389,6 @@ cudaError_t launch_m2(M2Kind kind, const M2Launch &a, cudaStream_t stream) {
     return launch_m2_decode_split(a, kind == M2Kind::DecodeFused, stream);
   if ((kind == M2Kind::Decode || kind == M2Kind::DecodeFused) && m2_decode_flat_eligible(a))
     return launch_m2_decode_flat(a, kind == M2Kind::DecodeFused, stream);
-  if ((kind == M2Kind::Decode || kind == M2Kind::DecodeFused) && m2_decode_pipe_eligible(a)) {
-    bool launched = false;
-    const cudaError_t e = launch_m2_decode_pipe(a, kind == M2Kind::DecodeFused, stream, &launched);
-    if (e != cudaSuccess || launched) return e;
-  }
   if (kind == M2Kind::DecodeFused) return cudaErrorNotSupported;  // caller: decode, then flush
   if (a.in_dtype == RSSM_F32 && a.y_dtype == RSSM_F32) return launch_m2_t<float, float>(kind, a, stream);
   if (a.in_dtype == RSSM_BF16 && a.y_dtype == RSSM_F32) return launch_m2_t<bf16, float>(kind, a, stream);
