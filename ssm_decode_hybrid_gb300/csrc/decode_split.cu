@@ -88,7 +88,15 @@ __global__ void __launch_bounds__(1024) m2_prep_kernel(M2Launch a, int stride) {
     bulk_g2s(psm + lay.v_ring, cv + h0 * L * d * es, lay.v_in - lay.v_ring, &bar);
     bulk_g2s(psm + lay.v_in, static_cast<const unsigned char *>(a.v) + h0 * d * es, lay.dt_ring - lay.v_in, &bar);
     bulk_g2s(psm + lay.dt_ring, a.ring_dt + h0 * L, lay.coef - lay.dt_ring, &bar);
-    s_ptr[0] = a.count[b];  // after the copies are issued: the two latencies overlap
+  }
+  // This grid may start while the previous step's streaming grid finishes (it
+  // is launched with programmatic serialisation, and that grid lets it start
+  // once all its blocks are past their own wait on the previous precompute):
+  // the rings and inputs copied above are final by then, but the pointers and
+  // the workspace records are not, so everything below waits for that grid.
+  pdl_wait();
+  if (tid == 0) {
+    s_ptr[0] = a.count[b];
     s_ptr[1] = a.start[b];
   }
   // the streaming kernel may start its S_0 loads now; it waits for this grid
@@ -236,6 +244,10 @@ __global__ void __launch_bounds__(kThreads, 4) m2_stream_kernel(M2Launch a, int 
   const size_t bg = static_cast<size_t>(b) * a.G + g;
   const float4 q4 = load4(static_cast<const TI *>(a.q) + bg * N + col);
   pdl_wait();  // the precompute grid has finished: workspace, ring and pointers are final
+  // the next step's precompute may start its ring copies once every block is
+  // past this wait (it waits for this grid before it touches the pointers or
+  // the workspace)
+  pdl_launch_dependents();
   const int info = reinterpret_cast<const int *>(wk)[1];
   const float abar = wk[0];
   if (!(info & kInfoValid)) return;
@@ -337,23 +349,31 @@ cudaError_t launch_split_n(const M2Launch &a, cudaStream_t stream) {
       (e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psm))) !=
           cudaSuccess)
     return e;
-  prep<<<static_cast<unsigned>(a.B) * a.G, 32 * HpG, psm, stream>>>(a, stride);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // programmatic dependent launches: the precompute's ring copies overlap the
+  // previous step's S_0 stream tail, and this step's S_0 stream the
+  // precompute's tail
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pcfg = {};
+  pcfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.G);
+  pcfg.blockDim = dim3(32 * HpG);
+  pcfg.dynamicSmemBytes = psm;
+  pcfg.stream = stream;
+  pcfg.attrs = attr;
+  pcfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&pcfg, prep, a, stride)) != cudaSuccess) return e;
   const size_t ssm = kFuse ? static_cast<size_t>(a.L) * (a.d + N) * es : 0;
   auto strm = m2_stream_kernel<N, kFuse, TI, TO>;
   if (ssm > 48 * 1024 &&
       (e = cudaFuncSetAttribute(strm, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm))) !=
           cudaSuccess)
     return e;
-  // programmatic dependent launch: the S_0 stream overlaps the precompute's tail
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.H);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = ssm;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, strm, a, stride);
