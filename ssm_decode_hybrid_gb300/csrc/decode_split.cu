@@ -79,29 +79,32 @@ __global__ void __launch_bounds__(1024) m2_prep_kernel(M2Launch a, int stride) {
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar, lay.copied);
+    mbar_arrive_expect_tx(&bar, lay.copied);  // the rings now, this step's inputs after the wait
     const unsigned char *ck = static_cast<const unsigned char *>(a.ring_k);
     const unsigned char *cv = static_cast<const unsigned char *>(a.ring_v);
     bulk_g2s(psm + lay.k_ring, ck + bg * L * N * es, lay.k_in - lay.k_ring, &bar);
-    bulk_g2s(psm + lay.k_in, static_cast<const unsigned char *>(a.k) + bg * N * es, N * es, &bar);
-    bulk_g2s(psm + lay.q_in, static_cast<const unsigned char *>(a.q) + bg * N * es, N * es, &bar);
     bulk_g2s(psm + lay.v_ring, cv + h0 * L * d * es, lay.v_in - lay.v_ring, &bar);
-    bulk_g2s(psm + lay.v_in, static_cast<const unsigned char *>(a.v) + h0 * d * es, lay.dt_ring - lay.v_in, &bar);
     bulk_g2s(psm + lay.dt_ring, a.ring_dt + h0 * L, lay.coef - lay.dt_ring, &bar);
   }
   // This grid may start while the previous step's streaming grid finishes (it
   // is launched with programmatic serialisation, and that grid lets it start
   // once all its blocks are past their own wait on the previous precompute):
-  // the rings and inputs copied above are final by then, but the pointers and
-  // the workspace records are not, so everything below waits for that grid.
+  // the rings copied above are final by then (only precompute grids write
+  // them), but the pointers and the workspace records are not, nor need the
+  // step's inputs be (the caller may pass that grid's output), so everything
+  // below waits for that grid.
   pdl_wait();
-  if (tid == 0) {
-    s_ptr[0] = a.count[b];
-    s_ptr[1] = a.start[b];
-  }
   // the streaming kernel may start its S_0 loads now; it waits for this grid
   // before it reads the workspace
   pdl_launch_dependents();
+  if (tid == 0) {
+    // this step's k, q and v, in flight together with the pointer reads
+    bulk_g2s(psm + lay.k_in, static_cast<const unsigned char *>(a.k) + bg * N * es, N * es, &bar);
+    bulk_g2s(psm + lay.q_in, static_cast<const unsigned char *>(a.q) + bg * N * es, N * es, &bar);
+    bulk_g2s(psm + lay.v_in, static_cast<const unsigned char *>(a.v) + h0 * d * es, lay.dt_ring - lay.v_in, &bar);
+    s_ptr[0] = a.count[b];
+    s_ptr[1] = a.start[b];
+  }
   const float dt_in = a.dt[bh];
   const float Ai = a.A[i];
   float *wk = a.work + bh * stride;

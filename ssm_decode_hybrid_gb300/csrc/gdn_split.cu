@@ -90,11 +90,24 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
-    // the g rings and this step's k, q first; then, once the pointers are in,
+    // the g rings first; then this step's k, q and, once the pointers are in,
     // only the committed slots of the k and u rings (they sit at their own
     // slot positions in shared memory)
     mbar_expect_tx(&bar, (lay.k_in - lay.g_ring) + 2u * T * N * es);
     bulk_g2s(psm + lay.g_ring, a.ring_g + h0 * L, lay.k_in - lay.g_ring, &bar);
+  }
+  // This grid may start while the previous call's streaming grid finishes (it
+  // is launched with programmatic serialisation, and a streaming grid lets it
+  // start once all its blocks are past their own wait on their precompute):
+  // the g rings are final by then (only precompute grids write them), but the
+  // pointers, the u ring and the workspace records are not, nor need the
+  // inputs be (the caller may pass that grid's output), so everything below
+  // waits for that grid.
+  pdl_wait();
+  // the streaming kernel may start its S_0 loads now; it waits for this grid
+  // before it reads the workspace
+  pdl_launch_dependents();
+  if (tid == 0) {
     for (int m = 0; m < T; ++m) {
       const size_t off = ((static_cast<size_t>(b) * T + m) * a.Hk + kh) * N * es;
       bulk_g2s(psm + lay.k_in + m * N * es, static_cast<const unsigned char *>(a.k) + off, N * es, &bar);
@@ -119,9 +132,6 @@ __global__ void __launch_bounds__(1024) gdn_prep_kernel(GdnLaunch a, int stride)
     }
     mbar_arrive(&bar);
   }
-  // the streaming kernel may start its S_0 loads now; it waits for this grid
-  // before it reads the workspace
-  pdl_launch_dependents();
   const size_t tv = (static_cast<size_t>(b) * T + (lane < T ? lane : 0)) * a.Hv + i;  // draft `lane` of this head
   const float g_m = (lane < T) ? a.g[tv] : 0.f;
   const float beta_m = (lane < T) ? a.beta[tv] : 0.f;
@@ -458,6 +468,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : (NT == 8 ? 1 : 2)) gdn
                     ((static_cast<size_t>(b) * T + mv) * a.Hk + kh) * N + col);
   }
   pdl_wait();  // the precompute grid has finished: workspace, drafts' k and g, pointers
+  // the next call's precompute may start its first copies once every block is
+  // past this wait (it waits for this grid before it reads anything this grid
+  // writes)
+  pdl_launch_dependents();
   // this thread's row of the solve, and the header, fetched before they are needed
   float pk[NT], pq[NT], pv[NT];
   const int rs = r_base + tid;
@@ -643,29 +657,33 @@ cudaError_t launch_gs(const GdnLaunch &a, cudaStream_t stream) {
       (e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(psm))) !=
           cudaSuccess)
     return e;
-  prep<<<static_cast<unsigned>(a.B) * a.Hk, 32 * HpK, psm, stream>>>(a, stride);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // programmatic dependent launches: the precompute's first copies overlap the
+  // previous streaming grid's tail, and the S_0 stream the precompute's tail
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pcfg = {};
+  pcfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.Hk);
+  pcfg.blockDim = dim3(32 * HpK);
+  pcfg.dynamicSmemBytes = psm;
+  pcfg.stream = stream;
+  pcfg.attrs = attr;
+  pcfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&pcfg, prep, a, stride)) != cudaSuccess) return e;
   if (!kDecode && gdn_verify_pipe_eligible(a)) return launch_gdn_verify_pipe(a, stride, NT, stream);
   if (!kDecode && gdn_verify_tc_eligible(a)) return launch_gdn_verify_tc(a, stride, NT, stream);
   const int nrb = (a.dv + CHUNK - 1) / CHUNK;
   const size_t ssm = GStreamSmem<N, NT>::bytes(kDecode && kFuse, a.L, eu, es);
   auto strm = gdn_stream_kernel<N, NT, kDecode, kFuse, TI, TU, TO>;
-  static std::atomic<size_t> configured{0};
-  if (ssm > 48 * 1024 && ssm > configured.load()) {
-    if ((e = cudaFuncSetAttribute(strm, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm))) !=
-        cudaSuccess)
-      return e;
-    configured.store(ssm);
-  }
-  // programmatic dependent launch: the S_0 stream overlaps the precompute's tail
+  if (ssm > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(strm, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm))) !=
+          cudaSuccess)
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nrb), static_cast<unsigned>(a.Hv), static_cast<unsigned>(a.B));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = ssm;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, strm, a, stride);

@@ -316,3 +316,32 @@ def test_chunked_verify_fused_full_batch_sampled():
     sequences."""
     run_verify_fused(wl.GDN_LAYER, 4, rounds=16, seed=wl.SEED_GDN + 60,
                      sample=[0, 1, 63, 128, 200, 230, 254, 255], workspace_T=4)
+
+
+def test_fused_decode_output_feeds_next_step():
+    """Each step's y (bf16) is the next step's v, passed as the same device
+    buffer, so the next step's precompute (which may start during the previous
+    S_0 stream) must read its inputs only after that grid has finished.
+    Batch 64, 20 steps; the oracle gets the GPU's y as its next v."""
+    R = rs()
+    shape = wl.GdnShape(B=64, Hv=32, Hk=16, dk=128, dv=128, L=8, in_dtype=wl.BF16)
+    seed = 271
+    init = wl.gdn_init(shape, seed)
+    idx = np.array([0, 1, 31, 32, 63])
+    state = gdn_state(init, 1)
+    orc = oracle_replay(init, idx)
+    st0 = wl.gdn_step(shape, seed, 0)
+    bufs = [dev(st0.v, torch.bfloat16).reshape(shape.B, shape.Hv, shape.dv),
+            torch.empty(shape.B, shape.Hv, shape.dv, dtype=torch.bfloat16, device="cuda")]
+    for t in range(20):
+        st = wl.gdn_step(shape, seed, t)
+        q, k, _, beta, g = gdn_step_dev(st, shape.in_dtype)
+        v_in, y = bufs[t % 2], bufs[(t + 1) % 2]
+        v_host = host(v_in.float()).reshape(np.asarray(st.v).shape)
+        R.gdn_replay_decode_fused(state, q, k, v_in, beta, g, y=y)
+        y_ref = orc.decode_step(take(st.q, idx), take(st.k, idx), take(v_host, idx), take(st.beta, idx),
+                                take(st.g, idx))
+        orc.flush()
+        assert_close(y[idx], y_ref, 1e-2, 1e-3, what=f"step {t}: y")
+    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0

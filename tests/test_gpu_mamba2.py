@@ -477,3 +477,33 @@ def test_spec_fused_full_batch_sampled():
     ten sampled sequences against the oracle."""
     run_spec_fused(wl.SPEC_MAMBA2, 4, rounds=24, seed=wl.SEED_SPEC,
                    sample=[0, 1, 100, 255, 256, 311, 400, 480, 510, 511])
+
+
+def test_fused_decode_output_feeds_next_step():
+    """Each step's y (bf16) is the next step's v, passed as the same device
+    buffer: the next step's precompute may start during the previous step's
+    S_0 stream (programmatic dependent launch), so it must read its inputs
+    only after that grid has finished.  Batch 128 (4096 streaming blocks, a
+    tail the next precompute overlaps), 20 steps; the oracle gets the GPU's y
+    as its next v."""
+    R = rs()
+    shape = wl.Mamba2Shape(B=128, H=32, G=8, d=64, n=128, L=8, in_dtype=wl.BF16)
+    seed = 171
+    init = wl.mamba2_init(shape, seed)
+    idx = np.array([0, 1, 50, 64, 100, 127])
+    state = m2_state(init)
+    orc = oracle_replay(init, idx)
+    A = dev(init.A)
+    st0 = wl.mamba2_step(shape, seed, 0)
+    bufs = [dev(st0.v, torch.bfloat16), torch.empty(shape.B, shape.H, shape.d, dtype=torch.bfloat16, device="cuda")]
+    for t in range(20):
+        st = wl.mamba2_step(shape, seed, t)
+        _, k, q, dt = m2_step_dev(st, shape.in_dtype)
+        v_in, y = bufs[t % 2], bufs[(t + 1) % 2]
+        v_host = host(v_in.float())
+        R.replay_decode_step_fused(state, v_in, k, q, dt, A, y=y)
+        y_ref = orc.decode_step(take(v_host, idx), take(st.k, idx), take(st.q, idx), take(st.dt, idx))
+        orc.flush()
+        assert_close(y[idx], y_ref, 1e-2, 1e-3, what=f"step {t}: y")
+    assert_close(state.S0[idx], orc.S0, what="final S0")
+    assert int(host(state.err)[0]) == 0
