@@ -120,6 +120,11 @@ __global__ void __launch_bounds__(kFpThreads, 1)
     tc05::alloc(&s_tmem, kFpTmemCols);
     tc05::relinquish();
   }
+  // launched with programmatic serialisation: the flags, pointers, rings and
+  // S_0 are read only once the previous grid has completed; the pointer reset
+  // that follows may be scheduled at once (it waits for this grid)
+  pdl_wait();
+  pdl_launch_dependents();
   // this CTA's items: the flagged sequences' items numbered t = 0, 1, ... in
   // sequence order, and this CTA takes t = blockIdx.x + j gridDim.x, so every
   // CTA gets the same share whichever sequences are flagged.  One pass over the
@@ -376,6 +381,7 @@ PFN_cuTensorMapEncodeTiled_v12000 fp_encode_fn() {
 // count <- 0, flag <- 0 (a sequence whose pointers were out of range was not
 // folded and keeps them; the fold set RSSM_EBIT_COUNT_RANGE).
 __global__ void fp_reset_kernel(int B, int L, int32_t *start, int32_t *count, int32_t *flag) {
+  pdl_wait();  // every item of the flush is folded
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B || flag[b] == 0) return;
   const int c = count[b], st = start[b];
@@ -410,10 +416,24 @@ cudaError_t launch_fp(const FlushLaunch &a, cudaStream_t stream) {
   const long items = static_cast<long>(a.B) * a.H * halves;
   const int sms = a.num_sms > 0 ? a.num_sms : sm_count();
   const int grid = items < sms ? static_cast<int>(items) : sms;
-  kern<<<grid, kFpThreads, kFpSmem, stream>>>(map, a, halves);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  fp_reset_kernel<<<(a.B + 255) / 256, 256, 0, stream>>>(a.B, a.L, a.start, a.count, a.flag);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kFpThreads);
+  cfg.dynamicSmemBytes = kFpSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, kern, map, a, halves)) != cudaSuccess) return e;
+  cudaLaunchConfig_t rcfg = {};
+  rcfg.gridDim = dim3(static_cast<unsigned>((a.B + 255) / 256));
+  rcfg.blockDim = dim3(256);
+  rcfg.stream = stream;
+  rcfg.attrs = attr;
+  rcfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&rcfg, fp_reset_kernel, a.B, a.L, a.start, a.count, a.flag);
 }
 
 }  // namespace

@@ -320,6 +320,9 @@ __global__ void __launch_bounds__(kThreads) m2_snapshot_verify_kernel(M2Launch a
 // Commit kernels (one thread per sequence)
 // ---------------------------------------------------------------------------
 __global__ void replay_commit_kernel(int B, int T, int L, const int32_t *accepted, int32_t *count, int32_t *err) {
+  // launched with programmatic serialisation: scheduled while the previous
+  // grid finishes, it reads nothing before that grid has completed
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int acc = accepted[b], c = count[b];
@@ -399,8 +402,16 @@ cudaError_t launch_m2(M2Kind kind, const M2Launch &a, cudaStream_t stream) {
 
 cudaError_t launch_replay_commit(int B, int T, int L, const int32_t *accepted, int32_t *count, int32_t *err,
                                  cudaStream_t stream) {
-  replay_commit_kernel<<<(B + 255) / 256, 256, 0, stream>>>(B, T, L, accepted, count, err);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((B + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, replay_commit_kernel, B, T, L, accepted, count, err);
 }
 
 cudaError_t launch_snapshot_commit(int B, int T, const int32_t *accepted, int32_t *cur, int32_t *err,

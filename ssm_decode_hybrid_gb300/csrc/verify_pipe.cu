@@ -16,24 +16,29 @@
 //
 // One CTA per SM walks the items of the grid.  Each item's 128 x 128 fp32
 // block is four 128-row x 32-column chunks.  Roles:
-//   warp 0     TMA producer: each chunk lands in a stage of a six-stage ring,
-//              already in the 128-byte-swizzled K-major layout of the MMA's A
-//              operand (one cp.async.bulk.tensor box of 16 KB);
-//   warps 2-3  split: lo = S - tf32(S) of each landed chunk into the stage's
-//              second half (the tensor core reads fp32 as tf32 by dropping the
-//              low 13 mantissa bits, so hi is the landed chunk itself and
-//              hi + lo carries S to about 2^-21), and the item's window
-//              vectors (bf16, exact in tf32) into one of two B-operand slots;
+//   warp 0     TMA producer: each chunk lands in a stage of an eight-stage
+//              ring (one cp.async.bulk.tensor box of 16 KB, 128-byte
+//              swizzle);
+//   warps 2-5  convert: thread r (TMEM lane r) reads row r of each landed
+//              chunk (eight conflict-free 16-byte loads), frees the stage, and
+//              writes hi = tf32(S) and lo = S - hi of the row into one of four
+//              A-operand slots in tensor memory (tcgen05.st; the tensor core
+//              reads fp32 as tf32 by dropping the low 13 mantissa bits, and
+//              hi + lo carries S to about 2^-21); it also stages the item's
+//              window vectors (bf16, exact in tf32) into one of two B-operand
+//              slots in shared memory;
 //   warp 1     MMA issuer: per chunk four tf32 MMAs on hi and four on lo
-//              (M = 128 rows, N = 16 vectors, K = 8) into one of four TMEM
-//              accumulators; a commit frees the stage once they have read it;
-//   warps 4-19 epilogue, four groups of four warps taking every fourth item,
+//              (M = 128 rows, N = 16 vectors, K = 8; A from tensor memory, B
+//              from shared memory) into one of four TMEM accumulators; a
+//              commit frees the A slot once they have read it;
+//   warps 6-21 epilogue, four groups of four warps taking every fourth item,
 //              each with its own TMEM accumulator: once an item's accumulator
 //              is complete, thread r of its group reads row r (tcgen05.ld) and
 //              finishes it (four groups, so that the loads of the rows' inputs
 //              of several items are in flight at once).
 // So the S_0 loads of later items are always in flight while earlier items
-// are split, multiplied and solved; no thread holds S_0 in registers.
+// are converted, multiplied and solved.  Shared memory carries each chunk
+// twice (the copy in, one read); the tensor cores read S_0 from tensor memory.
 // Every wait is bounded (RSSM_EBIT_TIMEOUT); after one runs out each role
 // stops at its next wait, in-flight copies are drained and TMEM is released.
 #include <cudaTypedefs.h>
@@ -49,13 +54,14 @@ namespace rssm {
 
 namespace {
 
-constexpr int kPvStages = 6;
+constexpr int kPvStages = 8;
+constexpr int kPvTSlots = 4;                        // A-operand slots in tensor memory (hi and lo of one chunk)
 constexpr int kPvRows = 128;                        // rows of an item: MMA M, TMEM lanes
 constexpr int kPvK = 128;                           // columns of S_0 (d_k, n)
 constexpr int kPvM2Rows = 64;                       // Mamba-2 head dimension d (two heads per item)
 constexpr int kPvChunks = 4;                        // 32-column chunks of a row
 constexpr uint32_t kPvChunkBytes = kPvRows * 128;   // 16 KB: one TMA box
-constexpr uint32_t kPvStageBytes = 2 * kPvChunkBytes;  // hi (the landed chunk), lo
+constexpr uint32_t kPvStageBytes = kPvChunkBytes;
 constexpr int kPvN = 16;                            // GDN: 8 key, 8 query columns; Mamba-2: 8 query columns, 8 zero
 constexpr uint32_t kPvXChunkBytes = kPvN * 128;     // 2 KB
 constexpr uint32_t kPvXBytes = kPvChunks * kPvXChunkBytes;  // 8 KB per slot
@@ -65,8 +71,11 @@ constexpr uint32_t kPvHdrOff = kPvXOff + 2 * kPvXBytes;
 constexpr int kPvGroups = 4;                        // epilogue groups of 128 threads
 constexpr uint32_t kPvSmem = kPvHdrOff + kPvGroups * kGdnWorkHeader * 4 + 1024;  // + alignment slack
 static_assert(kM2VerifyHeader <= kGdnWorkHeader, "record header staging");
-constexpr int kPvThreads = 128 + kPvGroups * 128;
-constexpr uint32_t kPvTmemCols = kPvGroups * 16;    // one accumulator of 16 columns per group
+constexpr int kPvThreads = 64 + 128 + kPvGroups * 128;
+constexpr uint32_t kPvAccCols = kPvGroups * 16;     // one accumulator of 16 columns per group
+constexpr uint32_t kPvTSlotCols = 64;               // hi: 32 columns (K = 32 fp32), lo: 32
+constexpr uint32_t kPvTmemCols = 512;               // >= kPvAccCols + kPvTSlots * kPvTSlotCols, a power of two
+static_assert(kPvAccCols + kPvTSlots * kPvTSlotCols <= kPvTmemCols, "tensor memory budget");
 constexpr int kInfoValid = 1 << 16;
 
 // kind::tf32, fp32 accumulator, A and B tf32, both K-major, M = 128, N = 16.
@@ -80,12 +89,23 @@ __device__ __forceinline__ uint64_t pv_desc(uint32_t saddr) {
          (1ull << 46) | (2ull << 61);
 }
 
-__device__ __forceinline__ void pv_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, bool accumulate) {
+// D (TMEM) += A (TMEM: lane = row, one column per K element) x B (shared memory).
+__device__ __forceinline__ void pv_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, bool accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kPvIdesc), "r"(accumulate ? 1u : 0u)
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(kPvIdesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
+// 16 columns of this warp's 32 TMEM lanes from registers (thread = lane).
+__device__ __forceinline__ void pv_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 
@@ -136,9 +156,10 @@ __device__ __forceinline__ bool pv_wait(uint64_t *bar, uint32_t parity, volatile
 
 struct PvBars {
   uint64_t full[kPvStages];   // TMA landed (tx bytes)
-  uint64_t conv[kPvStages];   // lo written (64 split threads)
-  uint64_t empty[kPvStages];  // MMAs have read the stage (commit)
-  uint64_t xfull[2];          // window vectors written (64 split threads)
+  uint64_t empty[kPvStages];  // the stage is read (the 128 convert threads)
+  uint64_t tfull[kPvTSlots];  // hi and lo of a chunk in tensor memory (the 128 convert threads)
+  uint64_t tempty[kPvTSlots]; // MMAs have read the A slot (commit)
+  uint64_t xfull[2];          // window vectors written (the 128 convert threads)
   uint64_t xempty[2];         // MMAs of the slot's item done (commit)
   uint64_t afull[kPvGroups];  // accumulator complete (commit)
   uint64_t aempty[kPvGroups]; // accumulator read (the group's 128 threads)
@@ -180,11 +201,14 @@ __global__ void __launch_bounds__(kPvThreads, 1)
     s_abort = 0;
     for (int s = 0; s < kPvStages; ++s) {
       mbar_init(&bars.full[s], 1);
-      mbar_init(&bars.conv[s], 64);
-      mbar_init(&bars.empty[s], 1);
+      mbar_init(&bars.empty[s], 128);
+    }
+    for (int t = 0; t < kPvTSlots; ++t) {
+      mbar_init(&bars.tfull[t], 128);
+      mbar_init(&bars.tempty[t], 1);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars.xfull[x], 64);
+      mbar_init(&bars.xfull[x], 128);
       mbar_init(&bars.xempty[x], 1);
     }
     for (int g = 0; g < kPvGroups; ++g) {
@@ -234,19 +258,19 @@ __global__ void __launch_bounds__(kPvThreads, 1)
         const uint32_t xb = base + kPvXOff + sl * kPvXBytes;
         bool ok = true;
         for (int c = 0; c < kPvChunks; ++c, ++q) {
-          const int s = q % kPvStages;
-          if (!pv_wait(&bars.conv[s], (q / kPvStages) & 1, abort)) {
+          const int t = q % kPvTSlots;
+          if (!pv_wait(&bars.tfull[t], (q / kPvTSlots) & 1, abort)) {
             ok = false;
             break;
           }
           tc05::fence_after_sync();
-          const uint32_t hi = base + kPvStagesOff + s * kPvStageBytes, lo = hi + kPvChunkBytes;
+          const uint32_t hi = tmem + kPvAccCols + static_cast<uint32_t>(t) * kPvTSlotCols, lo = hi + 32;
 #pragma unroll
           for (int s2 = 0; s2 < 4; ++s2)
-            pv_mma(d, pv_desc(hi + s2 * 32), pv_desc(xb + c * kPvXChunkBytes + s2 * 32), c > 0 || s2 > 0);
+            pv_mma_ts(d, hi + 8 * s2, pv_desc(xb + c * kPvXChunkBytes + s2 * 32), c > 0 || s2 > 0);
 #pragma unroll
-          for (int s2 = 0; s2 < 4; ++s2) pv_mma(d, pv_desc(lo + s2 * 32), pv_desc(xb + c * kPvXChunkBytes + s2 * 32), true);
-          tc05::commit(&bars.empty[s]);
+          for (int s2 = 0; s2 < 4; ++s2) pv_mma_ts(d, lo + 8 * s2, pv_desc(xb + c * kPvXChunkBytes + s2 * 32), true);
+          tc05::commit(&bars.tempty[t]);
         }
         if (!ok) break;
         tc05::commit(&bars.afull[ag]);
@@ -256,17 +280,20 @@ __global__ void __launch_bounds__(kPvThreads, 1)
       tc05::commit(&bars.drain);
       mbar_wait(&bars.drain, 0);
     }
-  } else if (warp < 4) {
-    // ---- split: lo of each landed chunk, and the window vectors ---------------
-    // The next item's vectors are loaded into registers while the current
-    // item's chunks are split, so that the split never waits on global memory.
-    const int ct = tid - 64;  // 0..63
-    constexpr int kXUnits = kPvN * (kPvK / 4) / 64;  // 16-byte units of the vectors per thread
+  } else if (warp < 6) {
+    // ---- convert: hi and lo of each landed chunk into tensor memory, and the
+    // window vectors.  The next item's vectors are loaded into registers
+    // while the current item's chunks are converted, so that this role never
+    // waits on global memory.
+    const int ct = tid - 64;                       // 0..127
+    const int r = 32 * (warp & 3) + lane;          // the TMEM lane (row) this thread writes
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    constexpr int kXUnits = kPvN * (kPvK / 4) / 128;  // 16-byte units of the vectors per thread
     uint2 xr[kXUnits];
     auto load_x = [&](int it) {
 #pragma unroll
       for (int j = 0; j < kXUnits; ++j) {
-        const int idx = ct + 64 * j, v = idx / (kPvK / 4), u = idx % (kPvK / 4);
+        const int idx = ct + 128 * j, v = idx / (kPvK / 4), u = idx % (kPvK / 4);
         const TI *src = pv_vector<TI>(a, it, v);
         xr[j] = src != nullptr ? *reinterpret_cast<const uint2 *>(src + 4 * u) : make_uint2(0u, 0u);
       }
@@ -282,7 +309,7 @@ __global__ void __launch_bounds__(kPvThreads, 1)
       const uint32_t xb = base + kPvXOff + sl * kPvXBytes;
 #pragma unroll
       for (int j = 0; j < kXUnits; ++j) {
-        const int idx = ct + 64 * j, v = idx / (kPvK / 4), u = idx % (kPvK / 4);
+        const int idx = ct + 128 * j, v = idx / (kPvK / 4), u = idx % (kPvK / 4);
         const int cc = u >> 3, lu = u & 7;
         const float4 x = make_float4(__uint_as_float(xr[j].x << 16), __uint_as_float(xr[j].x & 0xffff0000u),
                                      __uint_as_float(xr[j].y << 16), __uint_as_float(xr[j].y & 0xffff0000u));
@@ -290,33 +317,49 @@ __global__ void __launch_bounds__(kPvThreads, 1)
       }
       tc05::fence_proxy_async_smem();
       mbar_arrive(&bars.xfull[sl]);
-      if (it + static_cast<int>(gridDim.x) < items) load_x(it + gridDim.x);  // in flight during the splits
+      if (it + static_cast<int>(gridDim.x) < items) load_x(it + gridDim.x);  // in flight during the conversions
       bool ok = true;
       for (int c = 0; c < kPvChunks; ++c, ++q) {
-        const int s = q % kPvStages;
-        if (!pv_wait(&bars.full[s], (q / kPvStages) & 1, abort)) {
+        const int s = q % kPvStages, t = q % kPvTSlots;
+        if (!pv_wait(&bars.full[s], (q / kPvStages) & 1, abort) ||
+            !pv_wait(&bars.tempty[t], ((q / kPvTSlots) & 1) ^ 1, abort)) {
           ok = false;
           break;
         }
-        const uint32_t hi = base + kPvStagesOff + s * kPvStageBytes, lo = hi + kPvChunkBytes;
-        // elementwise, so the swizzle of the layout does not matter
-#pragma unroll 4
-        for (int u = ct; u < static_cast<int>(kPvChunkBytes / 16); u += 64) {
-          float4 x;
-          pv_lds4(hi + u * 16, x);
-          pv_sts4(lo + u * 16, make_float4(x.x - pv_trunc(x.x), x.y - pv_trunc(x.y), x.z - pv_trunc(x.z),
-                                           x.w - pv_trunc(x.w)));
+        // row r of the chunk: 16-byte unit u at r * 128 + ((u ^ (r % 8)) << 4) in the swizzled box
+        const uint32_t row = base + kPvStagesOff + s * kPvStageBytes + r * 128;
+        const uint32_t ta = tmem + lane_base + kPvAccCols + static_cast<uint32_t>(t) * kPvTSlotCols;
+        tc05::fence_after_sync();  // after the wait on tempty: the MMAs that read this slot are complete
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float4 x;
+            pv_lds4(row + (((4 * half + u) ^ (r & 7)) << 4), x);
+            const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float h = pv_trunc(xs[e]);
+              hi[4 * u + e] = __float_as_uint(h);
+              lo[4 * u + e] = __float_as_uint(xs[e] - h);
+            }
+          }
+          pv_st16(ta + 16 * half, hi);
+          pv_st16(ta + 32 + 16 * half, lo);
         }
-        tc05::fence_proxy_async_smem();
-        mbar_arrive(&bars.conv[s]);
+        mbar_arrive(&bars.empty[s]);  // the stage is read: the producer may refill it
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc05::fence_before_sync();
+        mbar_arrive(&bars.tfull[t]);
       }
       if (!ok) break;
     }
   } else {
     // ---- epilogue: group g finishes items k = g, g + 4, ...; thread r row r ----
-    const int g = (warp - 4) / 4;   // group
-    const int r = (tid - 128) % 128;  // TMEM lane, row of the item
+    const int g = (warp - 6) / 4;     // group
     const int ew = warp % 4;          // this warp reads TMEM lanes 32 ew .. 32 ew + 31
+    const int r = 32 * ew + lane;     // TMEM lane, row of the item
     pdl_wait();  // the precompute grid has finished: workspace, drafts' entries, pointers
     // the group's 128 threads take every decision to stop together (named
     // barriers with an OR), since a named barrier has no time limit
