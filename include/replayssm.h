@@ -13,7 +13,11 @@
  *    non-zero status nothing was launched.
  *  - Calls are asynchronous on the caller's stream and never synchronise.
  *    Pass a cudaStream_t (NULL = the legacy default stream).  The calling
- *    thread's current CUDA device must own every pointer.
+ *    thread's current CUDA device must own every pointer.  Consecutive calls
+ *    on one stream may overlap on the GPU (programmatic dependent launch),
+ *    but a call reads nothing the previous call writes before the previous
+ *    call's kernels have completed, so one call's output may be passed as the
+ *    next call's input.
  *  - The caller owns all memory.  Every pointer is a DEVICE pointer,
  *    contiguous, row-major in the documented layout.  S, S0, snapshot slots,
  *    k, q and ring_k must be 16-byte aligned; every other array must be

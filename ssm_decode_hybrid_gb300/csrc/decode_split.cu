@@ -714,7 +714,6 @@ cudaError_t launch_vsplit(const M2Launch &a, cudaStream_t stream) {
   prep<<<static_cast<unsigned>(a.B) * a.G, 32 * HpG, psm, stream>>>(a, stride);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (m2_verify_pipe_eligible(a)) return launch_m2_verify_pipe(a, stride, stream);
-  if (m2_verify_tc_eligible(a)) return launch_m2_verify_tc(a, stride, stream);
   auto strm = m2_vstream_kernel<N, NT, TI, TO>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.B) * a.H);

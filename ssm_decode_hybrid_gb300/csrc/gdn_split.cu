@@ -671,7 +671,6 @@ cudaError_t launch_gs(const GdnLaunch &a, cudaStream_t stream) {
   pcfg.numAttrs = 1;
   if ((e = cudaLaunchKernelEx(&pcfg, prep, a, stride)) != cudaSuccess) return e;
   if (!kDecode && gdn_verify_pipe_eligible(a)) return launch_gdn_verify_pipe(a, stride, NT, stream);
-  if (!kDecode && gdn_verify_tc_eligible(a)) return launch_gdn_verify_tc(a, stride, NT, stream);
   const int nrb = (a.dv + CHUNK - 1) / CHUNK;
   const size_t ssm = GStreamSmem<N, NT>::bytes(kDecode && kFuse, a.L, eu, es);
   auto strm = gdn_stream_kernel<N, NT, kDecode, kFuse, TI, TU, TO>;

@@ -59,13 +59,9 @@ constexpr int kM2VerifyHeader = 16;
 __host__ __device__ constexpr int m2_verify_stride_floats(int d, int P) { return (kM2VerifyHeader + P * d + 3) & ~3; }
 bool m2_verify_split_eligible(const M2Launch &a);
 cudaError_t launch_m2_verify_split(const M2Launch &a, cudaStream_t stream);
-// Its streaming half on the tensor cores (verify_tc.cu): n = 128, d = 64,
-// two heads of a group per block, bf16 inputs, T >= 5.
-bool m2_verify_tc_eligible(const M2Launch &a);
-cudaError_t launch_m2_verify_tc(const M2Launch &a, int stride, cudaStream_t stream);
-// The same streaming half as the persistent TMA + tcgen05 pipeline
+// Its streaming half as the persistent TMA + tcgen05 pipeline
 // (verify_pipe.cu): n = 128, d = 64, two heads of a group per item, bf16
-// inputs, 2 <= T.
+// inputs, 5 <= T (fewer queries stay on the CUDA-core stream).
 bool m2_verify_pipe_eligible(const M2Launch &a);
 cudaError_t launch_m2_verify_pipe(const M2Launch &a, int stride, cudaStream_t stream);
 // One CTA per (sequence, head) with every load issued up front (decode_flat.cu).
@@ -124,13 +120,10 @@ __host__ __device__ constexpr int gdn_work_stride_floats(int dv, int P) {
 // value head, row block).  kind: Decode, DecodeFused or Verify.
 bool gdn_split_eligible(GdnKind kind, const GdnLaunch &a);
 cudaError_t launch_gdn_split(GdnKind kind, const GdnLaunch &a, cudaStream_t stream);
-// The streaming half of the two-launch GDN verify on the tensor cores
-// (verify_tc.cu): dk = dv = 128, bf16 inputs; reads the records the
-// precompute kernel left for window width P.
-bool gdn_verify_tc_eligible(const GdnLaunch &a);
-cudaError_t launch_gdn_verify_tc(const GdnLaunch &a, int stride, int P, cudaStream_t stream);
-// The same streaming half as a persistent, warp-specialised TMA + tcgen05
-// pipeline (verify_pipe.cu): dk = dv = 128, bf16 inputs, 2 <= T.
+// The streaming half of the two-launch GDN verify as a persistent,
+// warp-specialised TMA + tcgen05 pipeline (verify_pipe.cu): dk = dv = 128,
+// bf16 inputs, 2 <= T; it reads the records the precompute kernel left for
+// window width P.
 bool gdn_verify_pipe_eligible(const GdnLaunch &a);
 cudaError_t launch_gdn_verify_pipe(const GdnLaunch &a, int stride, int P, cudaStream_t stream);
 

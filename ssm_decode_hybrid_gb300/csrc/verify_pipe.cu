@@ -8,7 +8,8 @@
 // workspace.
 //   GDN:     an item is a (sequence, value head): 128 rows (d_v) x 128
 //            columns (d_k); X = [k_1 .. k_T, q_1 .. q_T] of its key head; each
-//            row is solved as verify_tc.cu does (gdn_split.cu's records).
+//            row follows from the chunked T x T solve whose terms
+//            gdn_split.cu's precompute left in the record.
 //   Mamba-2: an item is two heads of one group of a sequence: 2 x 64 rows
 //            (d) x 128 columns (n); X = [q_1 .. q_T] of the group; row r of
 //            head i gives y_s[r] = abar_s Z[r][s] + buf_s[r] (decode_split.cu's
