@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(1024) m2_vprep_kernel(M2Launch a, int stride) 
 }
 
 template <int N, int NT, typename TI, typename TO>
-__global__ void __launch_bounds__(kThreads, NT == 8 ? 2 : 4) m2_vstream_kernel(M2Launch a, int stride) {
+__global__ void __launch_bounds__(kThreads, NT == 8 ? 2 : (NT == 1 ? 5 : 4)) m2_vstream_kernel(M2Launch a, int stride) {
   constexpr int LPR = N / 4, RPW = 32 / LPR, RPP = kWarps * RPW;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x / a.H, i = blockIdx.x - b * a.H;
