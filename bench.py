@@ -468,21 +468,23 @@ def run_gpu(args):
 
     def inputs_ahead(t0):
         # steps t0 and t0 + 1 find their inputs in place
-        for j in range(2):
-            staging[(t0 + j) % 2].copy_(host_packed[(t0 + j) % POOL], non_blocking=True)
-        for e in copied:
-            e.record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_stream(stream)  # earlier steps are done with both buffers
+            for j in range(2):
+                staging[(t0 + j) % 2].copy_(host_packed[(t0 + j) % POOL], non_blocking=True)
+                copied[(t0 + j) % 2].record(copy_stream)
 
     def e2e_step(st, t):
+        # called with the copy stream current, so that the copies need no
+        # stream switch; the decode call names the compute stream
         i = t % 2
         stream.wait_event(copied[i])  # step t's inputs have landed; step t - 2's y was read
-        R.replay_decode_step_fused(st, *staged[i], A, y=ys[i])
+        R.replay_decode_step_fused(st, *staged[i], A, y=ys[i], stream=stream)
         computed.record(stream)
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(computed)
-            y_host[i].copy_(ys[i], non_blocking=True)
-            staging[i].copy_(host_packed[(t + 2) % POOL], non_blocking=True)
-            copied[i].record(copy_stream)
+        copy_stream.wait_event(computed)
+        y_host[i].copy_(ys[i], non_blocking=True)
+        staging[i].copy_(host_packed[(t + 2) % POOL], non_blocking=True)
+        copied[i].record(copy_stream)
 
     def serial_step(st, t):
         staging[0].copy_(host_packed[t % POOL], non_blocking=True)
@@ -494,8 +496,9 @@ def run_gpu(args):
     fields = [f.name for f in dataclasses.fields(state) if getattr(state, f.name) is not None]
     twins = [dataclasses.replace(state, **{f: getattr(state, f).clone() for f in fields}) for _ in range(2)]
     inputs_ahead(0)
-    for t in range(4):
-        e2e_step(twins[0], t)
+    with torch.cuda.stream(copy_stream):
+        for t in range(4):
+            e2e_step(twins[0], t)
     stream.wait_stream(copy_stream)
     torch.cuda.synchronize()
     last = [y_host[0].clone(), y_host[1].clone()]  # steps 2 and 3
@@ -516,8 +519,9 @@ def run_gpu(args):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for t in range(Ke):
-            step(state, first + t)
+        with torch.cuda.stream(copy_stream if overlapped else stream):
+            for t in range(Ke):
+                step(state, first + t)
         stream.wait_stream(copy_stream)
         e1.record(stream)
         torch.cuda.synchronize()
@@ -525,8 +529,9 @@ def run_gpu(args):
 
     Wu = max(W, 16)
     inputs_ahead(0)
-    for t in range(Wu):
-        e2e_step(state, t)
+    with torch.cuda.stream(copy_stream):
+        for t in range(Wu):
+            e2e_step(state, t)
     stream.wait_stream(copy_stream)
     e2e_ms = e2e_window(e2e_step, Wu, True)
     e2e_value = whole_job_throughput(shape.B * Ke, world, e2e_ms)

@@ -3,8 +3,9 @@ step of the decode path runs in the library's CUDA kernels.
 
 Tensors must be CUDA tensors on the current device, contiguous, in the
 layouts documented in ``include/replayssm.h``.  Calls are asynchronous on
-torch's current stream.  A missing library raises at import time; a non-zero
-status raises ``ReplaySSMError``.
+torch's current stream, or on the ``torch.cuda.Stream`` passed as ``stream=``.
+A missing library raises at import time; a non-zero status raises
+``ReplaySSMError``.
 """
 from __future__ import annotations
 
@@ -143,8 +144,8 @@ def _ptr(t: torch.Tensor | None):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _stream():
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+def _stream(stream=None):
+    return ctypes.c_void_p((torch.cuda.current_stream() if stream is None else stream).cuda_stream)
 
 
 def _dt(t: torch.Tensor) -> int:
@@ -330,7 +331,7 @@ def _out(y, shape, dtype, device):
     return y
 
 
-def ssm_state_update_baseline(S, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+def ssm_state_update_baseline(S, v, k, q, dt, A, y=None, y_dtype=torch.float32, stream=None):
     """Baseline decode step: S <- a S + dt v k^T in place, returns y = S q."""
     _f32(S, "S")
     B, H, d, n = S.shape
@@ -338,32 +339,33 @@ def ssm_state_update_baseline(S, v, k, q, dt, A, y=None, y_dtype=torch.float32):
     y = _out(y, (B, H, d), y_dtype, S.device)
     dims = M2Dims(B, H, G, d, n, 1, _dt(v), _dt(y))
     _check(LIB.ssm_state_update_baseline(ctypes.byref(dims), _ptr(S), _ptr(v), _ptr(k), _ptr(q), _ptr(dt), _ptr(A),
-                                         _ptr(y), _stream()), "ssm_state_update_baseline")
+                                         _ptr(y), _stream(stream)), "ssm_state_update_baseline")
     return y
 
 
-def replay_decode_step(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+def replay_decode_step(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32, stream=None):
     B, H, G, d, n, L = state.shape
     y = _out(y, (B, H, d), y_dtype, state.S0.device)
     dims = state.dims(y.dtype)
     st = state.struct()
     _check(LIB.replay_decode_step(ctypes.byref(dims), ctypes.byref(st), _ptr(v), _ptr(k), _ptr(q), _ptr(dt), _ptr(A),
-                                  _ptr(y), _stream()), "replay_decode_step")
+                                  _ptr(y), _stream(stream)), "replay_decode_step")
     return y
 
 
-def replay_decode_step_fused(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+def replay_decode_step_fused(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32, stream=None):
     """Decode step with the full-buffer flush in the same launch."""
     B, H, G, d, n, L = state.shape
     y = _out(y, (B, H, d), y_dtype, state.S0.device)
     dims = state.dims(y.dtype)
     st = state.struct()
     _check(LIB.replay_decode_step_fused(ctypes.byref(dims), ctypes.byref(st), _ptr(v), _ptr(k), _ptr(q), _ptr(dt),
-                                        _ptr(A), _ptr(y), _stream()), "replay_decode_step_fused")
+                                        _ptr(A), _ptr(y), _stream(stream)), "replay_decode_step_fused")
     return y
 
 
-def replay_decode_step_fused_noalloc(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+def replay_decode_step_fused_noalloc(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32,
+                                     stream=None):
     """replay_decode_step_fused with the library's own workspace (state.work is
     not used); allocates nothing when y is given."""
     B, H, G, d, n, L = state.shape
@@ -371,18 +373,18 @@ def replay_decode_step_fused_noalloc(state: Mamba2State, v, k, q, dt, A, y=None,
     dims = state.dims(y.dtype)
     st = state.struct()
     _check(LIB.replay_decode_step_fused_noalloc(ctypes.byref(dims), ctypes.byref(st), _ptr(v), _ptr(k), _ptr(q),
-                                                _ptr(dt), _ptr(A), _ptr(y), _stream()),
+                                                _ptr(dt), _ptr(A), _ptr(y), _stream(stream)),
            "replay_decode_step_fused_noalloc")
     return y
 
 
-def replay_flush(state: Mamba2State, A):
+def replay_flush(state: Mamba2State, A, stream=None):
     dims = state.dims()
     st = state.struct()
-    _check(LIB.replay_flush(ctypes.byref(dims), ctypes.byref(st), _ptr(A), _stream()), "replay_flush")
+    _check(LIB.replay_flush(ctypes.byref(dims), ctypes.byref(st), _ptr(A), _stream(stream)), "replay_flush")
 
 
-def replay_spec_verify(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+def replay_spec_verify(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32, stream=None):
     """v [B,T,H,d]; k, q [B,T,G,n]; dt [B,T,H]; returns y [B,T,H,d]."""
     B, H, G, d, n, L = state.shape
     T = v.shape[1]
@@ -390,11 +392,11 @@ def replay_spec_verify(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch
     dims = state.dims(y.dtype)
     st = state.struct()
     _check(LIB.replay_spec_verify(ctypes.byref(dims), ctypes.byref(st), T, _ptr(v), _ptr(k), _ptr(q), _ptr(dt),
-                                  _ptr(A), _ptr(y), _stream()), "replay_spec_verify")
+                                  _ptr(A), _ptr(y), _stream(stream)), "replay_spec_verify")
     return y
 
 
-def replay_spec_verify_fused(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32):
+def replay_spec_verify_fused(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype=torch.float32, stream=None):
     """replay_flush, then replay_spec_verify, in one call.  Arguments as
     replay_spec_verify."""
     B, H, G, d, n, L = state.shape
@@ -403,18 +405,18 @@ def replay_spec_verify_fused(state: Mamba2State, v, k, q, dt, A, y=None, y_dtype
     dims = state.dims(y.dtype)
     st = state.struct()
     _check(LIB.replay_spec_verify_fused(ctypes.byref(dims), ctypes.byref(st), T, _ptr(v), _ptr(k), _ptr(q),
-                                        _ptr(dt), _ptr(A), _ptr(y), _stream()), "replay_spec_verify_fused")
+                                        _ptr(dt), _ptr(A), _ptr(y), _stream(stream)), "replay_spec_verify_fused")
     return y
 
 
-def replay_spec_commit(accepted, count, T: int, L: int, err=None):
+def replay_spec_commit(accepted, count, T: int, L: int, err=None, stream=None):
     _i32(accepted, "accepted")
     _i32(count, "count")
-    _check(LIB.replay_spec_commit(count.shape[0], T, L, _ptr(accepted), _ptr(count), _ptr(err), _stream()),
+    _check(LIB.replay_spec_commit(count.shape[0], T, L, _ptr(accepted), _ptr(count), _ptr(err), _stream(stream)),
            "replay_spec_commit")
 
 
-def ssm_spec_verify_baseline(slots, cur, v, k, q, dt, A, y=None, err=None, y_dtype=torch.float32):
+def ssm_spec_verify_baseline(slots, cur, v, k, q, dt, A, y=None, err=None, y_dtype=torch.float32, stream=None):
     """slots [B,T+1,H,d,n] f32; cur [B] i32; inputs as replay_spec_verify."""
     _f32(slots, "slots")
     B, T1, H, d, n = slots.shape
@@ -423,12 +425,12 @@ def ssm_spec_verify_baseline(slots, cur, v, k, q, dt, A, y=None, err=None, y_dty
     y = _out(y, (B, T, H, d), y_dtype, slots.device)
     dims = M2Dims(B, H, G, d, n, 1, _dt(v), _dt(y))
     _check(LIB.ssm_spec_verify_baseline(ctypes.byref(dims), T, _ptr(slots), _ptr(cur), _ptr(v), _ptr(k), _ptr(q),
-                                        _ptr(dt), _ptr(A), _ptr(y), _ptr(err), _stream()), "ssm_spec_verify_baseline")
+                                        _ptr(dt), _ptr(A), _ptr(y), _ptr(err), _stream(stream)), "ssm_spec_verify_baseline")
     return y
 
 
-def ssm_spec_commit_baseline(accepted, cur, T: int, err=None):
-    _check(LIB.ssm_spec_commit_baseline(cur.shape[0], T, _ptr(accepted), _ptr(cur), _ptr(err), _stream()),
+def ssm_spec_commit_baseline(accepted, cur, T: int, err=None, stream=None):
+    _check(LIB.ssm_spec_commit_baseline(cur.shape[0], T, _ptr(accepted), _ptr(cur), _ptr(err), _stream(stream)),
            "ssm_spec_commit_baseline")
 
 
@@ -437,45 +439,45 @@ def ssm_spec_commit_baseline(accepted, cur, T: int, err=None):
 # ---------------------------------------------------------------------------
 
 
-def gdn_state_update_baseline(S, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+def gdn_state_update_baseline(S, q, k, v, beta, g, y=None, y_dtype=torch.float32, stream=None):
     _f32(S, "S")
     B, Hv, dv, dk = S.shape
     Hk = k.shape[1]
     y = _out(y, (B, Hv, dv), y_dtype, S.device)
     dims = GdnDims(B, Hv, Hk, dk, dv, 1, _dt(k), F32, _dt(y))
     _check(LIB.gdn_state_update_baseline(ctypes.byref(dims), _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
-                                         _ptr(y), _stream()), "gdn_state_update_baseline")
+                                         _ptr(y), _stream(stream)), "gdn_state_update_baseline")
     return y
 
 
-def gdn_replay_decode(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+def gdn_replay_decode(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32, stream=None):
     B, Hv, Hk, dk, dv, L = state.shape
     y = _out(y, (B, Hv, dv), y_dtype, state.S0.device)
     dims = state.dims(y.dtype)
     st = state.struct()
     _check(LIB.gdn_replay_decode(ctypes.byref(dims), ctypes.byref(st), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
-                                 _ptr(y), _stream()), "gdn_replay_decode")
+                                 _ptr(y), _stream(stream)), "gdn_replay_decode")
     return y
 
 
-def gdn_replay_decode_fused(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+def gdn_replay_decode_fused(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32, stream=None):
     """GDN decode step with the full-buffer flush in the same launches."""
     B, Hv, Hk, dk, dv, L = state.shape
     y = _out(y, (B, Hv, dv), y_dtype, state.S0.device)
     dims = state.dims(y.dtype)
     st = state.struct()
     _check(LIB.gdn_replay_decode_fused(ctypes.byref(dims), ctypes.byref(st), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
-                                       _ptr(g), _ptr(y), _stream()), "gdn_replay_decode_fused")
+                                       _ptr(g), _ptr(y), _stream(stream)), "gdn_replay_decode_fused")
     return y
 
 
-def gdn_replay_flush(state: GdnState):
+def gdn_replay_flush(state: GdnState, stream=None):
     dims = state.dims()
     st = state.struct()
-    _check(LIB.gdn_replay_flush(ctypes.byref(dims), ctypes.byref(st), _stream()), "gdn_replay_flush")
+    _check(LIB.gdn_replay_flush(ctypes.byref(dims), ctypes.byref(st), _stream(stream)), "gdn_replay_flush")
 
 
-def gdn_replay_verify(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+def gdn_replay_verify(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32, stream=None):
     """q, k [B,T,Hk,dk]; v [B,T,Hv,dv]; beta, g [B,T,Hv]; returns y [B,T,Hv,dv]."""
     B, Hv, Hk, dk, dv, L = state.shape
     T = v.shape[1]
@@ -483,11 +485,11 @@ def gdn_replay_verify(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.f
     dims = state.dims(y.dtype)
     st = state.struct()
     _check(LIB.gdn_replay_verify(ctypes.byref(dims), ctypes.byref(st), T, _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
-                                 _ptr(g), _ptr(y), _stream()), "gdn_replay_verify")
+                                 _ptr(g), _ptr(y), _stream(stream)), "gdn_replay_verify")
     return y
 
 
-def gdn_replay_verify_fused(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32):
+def gdn_replay_verify_fused(state: GdnState, q, k, v, beta, g, y=None, y_dtype=torch.float32, stream=None):
     """gdn_replay_flush, then gdn_replay_verify, in one call.  Arguments as
     gdn_replay_verify."""
     B, Hv, Hk, dk, dv, L = state.shape
@@ -496,11 +498,11 @@ def gdn_replay_verify_fused(state: GdnState, q, k, v, beta, g, y=None, y_dtype=t
     dims = state.dims(y.dtype)
     st = state.struct()
     _check(LIB.gdn_replay_verify_fused(ctypes.byref(dims), ctypes.byref(st), T, _ptr(q), _ptr(k), _ptr(v),
-                                       _ptr(beta), _ptr(g), _ptr(y), _stream()), "gdn_replay_verify_fused")
+                                       _ptr(beta), _ptr(g), _ptr(y), _stream(stream)), "gdn_replay_verify_fused")
     return y
 
 
-def gdn_spec_verify_baseline(slots, cur, q, k, v, beta, g, y=None, err=None, y_dtype=torch.float32):
+def gdn_spec_verify_baseline(slots, cur, q, k, v, beta, g, y=None, err=None, y_dtype=torch.float32, stream=None):
     _f32(slots, "slots")
     B, T1, Hv, dv, dk = slots.shape
     T = T1 - 1
@@ -508,12 +510,12 @@ def gdn_spec_verify_baseline(slots, cur, q, k, v, beta, g, y=None, err=None, y_d
     y = _out(y, (B, T, Hv, dv), y_dtype, slots.device)
     dims = GdnDims(B, Hv, Hk, dk, dv, 1, _dt(k), F32, _dt(y))
     _check(LIB.gdn_spec_verify_baseline(ctypes.byref(dims), T, _ptr(slots), _ptr(cur), _ptr(q), _ptr(k), _ptr(v),
-                                        _ptr(beta), _ptr(g), _ptr(y), _ptr(err), _stream()),
+                                        _ptr(beta), _ptr(g), _ptr(y), _ptr(err), _stream(stream)),
            "gdn_spec_verify_baseline")
     return y
 
 
-def conv_state_update(state, u, weight, bias, dx: int, dbc: int, silu: bool = True, out=None):
+def conv_state_update(state, u, weight, bias, dx: int, dbc: int, silu: bool = True, out=None, stream=None):
     """Convolution-state decode step: state [B][dx+2dbc][W-1] (updated in
     place), u [B][dx+2dbc] (same dtype, bf16 or f32), weight f32 [dx+2dbc][W],
     bias f32 [dx+2dbc] or None.  Returns (x [B][dx], b [B][dbc], c [B][dbc])
@@ -528,7 +530,7 @@ def conv_state_update(state, u, weight, bias, dx: int, dbc: int, silu: bool = Tr
         out = tuple(torch.empty(B, n, dtype=state.dtype, device=state.device) for n in (dx, dbc, dbc))
     dims = ConvDims(B, dx, dbc, Wm1 + 1, _dt(state), 1 if silu else 0)
     _check(LIB.conv_state_update(ctypes.byref(dims), _ptr(state), _ptr(u), _ptr(weight), _ptr(bias),
-                                 *(_ptr(t) if t.numel() else None for t in out), _stream()), "conv_state_update")
+                                 *(_ptr(t) if t.numel() else None for t in out), _stream(stream)), "conv_state_update")
     return out
 
 
@@ -541,12 +543,12 @@ def layout_sizes(dims) -> Layout:
     return out
 
 
-def read_error(err: torch.Tensor) -> int:
-    """The sticky device error word, read on torch's current stream (this
-    waits for the stream)."""
+def read_error(err: torch.Tensor, stream=None) -> int:
+    """The sticky device error word, read on torch's current stream or on
+    `stream` (this waits for that stream)."""
     _i32(err, "err")
     v = ctypes.c_int32(0)
-    _check(LIB.rssm_read_error(_ptr(err), ctypes.byref(v), _stream()), "rssm_read_error")
+    _check(LIB.rssm_read_error(_ptr(err), ctypes.byref(v), _stream(stream)), "rssm_read_error")
     return int(v.value)
 
 

@@ -507,3 +507,31 @@ def test_fused_decode_output_feeds_next_step():
         assert_close(y[idx], y_ref, 1e-2, 1e-3, what=f"step {t}: y")
     assert_close(state.S0[idx], orc.S0, what="final S0")
     assert int(host(state.err)[0]) == 0
+
+
+def test_decode_runs_on_the_stream_passed():
+    """stream= puts the call on that stream: while torch's current stream is
+    still busy (a bounded sleep kernel), the output read back on the named
+    stream is already the full result, equal to the same step on the current
+    stream."""
+    R = rs()
+    shape = wl.Mamba2Shape(B=8, H=4, G=2, d=64, n=128, L=8, in_dtype=wl.BF16)
+    seed = 23
+    init = wl.mamba2_init(shape, seed)
+    ref, out = m2_state(init), m2_state(init)
+    A = dev(init.A)
+    inp = m2_step_dev(wl.mamba2_step(shape, seed, 0), shape.in_dtype)
+    y_ref = R.replay_decode_step_fused(ref, *inp, A)
+    y = torch.full_like(y_ref, float("nan"))
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    torch.cuda._sleep(400_000_000)  # keeps the current stream busy for about 0.2 s
+    R.replay_decode_step_fused(out, *inp, A, y=y, stream=side)
+    with torch.cuda.stream(side):
+        y_side = y.cpu()  # a copy on `side`, which waits for `side` only
+    busy = not torch.cuda.current_stream().query()
+    torch.cuda.synchronize()
+    assert busy, "the current stream finished before the read: the check says nothing"
+    assert torch.equal(y_side, y_ref.cpu())
+    for f in ("S0", "ring_v", "ring_k", "ring_dt", "start", "count", "flag"):
+        assert torch.equal(getattr(out, f), getattr(ref, f)), f
