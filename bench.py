@@ -456,34 +456,44 @@ def run_gpu(args):
     host_packed = [packed_host(h) for h in host_in]
     for h, p in zip(host_in, host_packed):
         assert all(torch.equal(a, b) for a, b in zip(h, typed_views(p))), "packed inputs equal the step's inputs"
-    staging = [torch.empty(h2d, dtype=torch.uint8, device=dev) for _ in range(2)]
+    NB, G = 8, 4  # staging and y buffers; the compute stream waits for G steps' copies at once
+    staging = [torch.empty(h2d, dtype=torch.uint8, device=dev) for _ in range(NB)]
     staged = [typed_views(b) for b in staging]
-    ys = [y, torch.empty_like(y)]
-    y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
+    ys = [y] + [torch.empty_like(y) for _ in range(NB - 1)]
+    y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(NB)]
     d2h = y_host[0].numel() * y_host[0].element_size()
     copy_stream = torch.cuda.Stream(device=dev)
     computed = torch.cuda.Event()
-    copied = [torch.cuda.Event() for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(NB)]
+    origin = [0]  # the first step after the last inputs_ahead: wait groups start there
     Ke = args.e2e_steps  # its own count: a 20-step window is too short to average the host's per-call costs
 
     def inputs_ahead(t0):
-        # steps t0 and t0 + 1 find their inputs in place
+        # steps t0 .. t0 + NB - 1 find their inputs in place
+        origin[0] = t0
         with torch.cuda.stream(copy_stream):
-            copy_stream.wait_stream(stream)  # earlier steps are done with both buffers
-            for j in range(2):
-                staging[(t0 + j) % 2].copy_(host_packed[(t0 + j) % POOL], non_blocking=True)
-                copied[(t0 + j) % 2].record(copy_stream)
+            copy_stream.wait_stream(stream)  # earlier steps are done with every buffer
+            for j in range(NB):
+                staging[(t0 + j) % NB].copy_(host_packed[(t0 + j) % POOL], non_blocking=True)
+                copied[(t0 + j) % NB].record(copy_stream)
 
     def e2e_step(st, t):
         # called with the copy stream current, so that the copies need no
-        # stream switch; the decode call names the compute stream
-        i = t % 2
-        stream.wait_event(copied[i])  # step t's inputs have landed; step t - 2's y was read
+        # stream switch; the decode call names the compute stream.  A wait on
+        # the compute stream between two decode calls costs the programmatic
+        # overlap of one step's S_0 stream with the next step's precompute
+        # (about 2.5 us), so the compute stream waits once every G steps, for
+        # the next G steps' inputs (copied NB - G or more steps earlier) and for
+        # the reads of the y buffers those steps overwrite.
+        i = t % NB
+        if (t - origin[0]) % G == 0:
+            for j in range(G):
+                stream.wait_event(copied[(t + j) % NB])
         R.replay_decode_step_fused(st, *staged[i], A, y=ys[i], stream=stream)
         computed.record(stream)
         copy_stream.wait_event(computed)
         y_host[i].copy_(ys[i], non_blocking=True)
-        staging[i].copy_(host_packed[(t + 2) % POOL], non_blocking=True)
+        staging[i].copy_(host_packed[(t + NB) % POOL], non_blocking=True)
         copied[i].record(copy_stream)
 
     def serial_step(st, t):
@@ -491,22 +501,23 @@ def run_gpu(args):
         R.replay_decode_step_fused(st, *staged[0], A, y=ys[0])
         y_host[0].copy_(ys[0], non_blocking=True)
 
-    # four overlapped steps (no synchronisation between them) leave the state
-    # and the last two outputs of four serial steps, bit for bit
+    # 2 NB overlapped steps (no synchronisation between them, every buffer used
+    # twice) leave the state and the last NB outputs of as many serial steps,
+    # bit for bit
     fields = [f.name for f in dataclasses.fields(state) if getattr(state, f.name) is not None]
     twins = [dataclasses.replace(state, **{f: getattr(state, f).clone() for f in fields}) for _ in range(2)]
     inputs_ahead(0)
     with torch.cuda.stream(copy_stream):
-        for t in range(4):
+        for t in range(2 * NB):
             e2e_step(twins[0], t)
     stream.wait_stream(copy_stream)
     torch.cuda.synchronize()
-    last = [y_host[0].clone(), y_host[1].clone()]  # steps 2 and 3
-    for t in range(4):
+    last = [y_host[t % NB].clone() for t in range(NB, 2 * NB)]
+    for t in range(2 * NB):
         serial_step(twins[1], t)
         torch.cuda.synchronize()
-        if t >= 2:
-            assert torch.equal(last[t - 2], y_host[0]), "overlapped copies changed a step's output"
+        if t >= NB:
+            assert torch.equal(last[t - NB], y_host[0]), "overlapped copies changed a step's output"
     for f in fields:
         assert torch.equal(getattr(twins[0], f), getattr(twins[1], f)) or f == "work", f"overlapped copies changed {f}"
     del twins
@@ -586,7 +597,8 @@ def run_gpu(args):
                     "steps": Ke, "ms_per_step": e2e_ms / Ke,
                     "calls": "each step from the host: replay_decode_step_fused on the compute stream; one H2D "
                              "copy of a later step's packed v/k/q/dt and one D2H copy of y on a copy stream, "
-                             "overlapping the neighbouring steps' kernels (double-buffered)",
+                             "overlapping other steps' kernels (8 staging and y buffers; the compute stream "
+                             "waits for the copies once every 4 steps)",
                     "serial": {"value": e2e_serial_value, "ms_per_step": e2e_serial_ms / Ke,
                                "calls": "the same steps with both copies on the compute stream, in order"}},
             "gpu_launches": LAUNCHES_PER_STEP * K,
