@@ -47,6 +47,30 @@ def test_binding_covers_exports():
     assert R.LIB.rssm_status_string(-2) == b"unsupported shape or dtype"
 
 
+def test_every_launching_call_takes_a_stream():
+    """Every binding call that passes a stream to the library accepts
+    stream= (default None: torch's current stream), and the calls the
+    library exposes with a stream argument are all covered."""
+    import inspect
+
+    _lib_path()
+    from ssm_decode_hybrid_gb300 import replayssm as R
+
+    src = inspect.getsource(R)
+    callers = set(re.findall(r"^def (\w+)\(", src, flags=re.M)) - {"_stream"}
+    with_stream = {n for n in callers if "_stream(stream)" in inspect.getsource(getattr(R, n))}
+    assert "replay_decode_step_fused" in with_stream and "gdn_replay_verify" in with_stream
+    for name in with_stream:
+        p = inspect.signature(getattr(R, name)).parameters
+        assert "stream" in p and p["stream"].default is None, name
+    assert not re.search(r"(?<![\w.])_stream\(\)", src), "a call still takes torch's current stream only"
+    header = open(HEADER).read()
+    takes_stream = set(re.findall(r"^RSSM_API\s+[\w\s\*]+?\b(\w+)\s*\([^;]*?rssm_stream_t", header, flags=re.M | re.S))
+    wrapped = {"rssm_read_error": "read_error"}
+    for sym in takes_stream:
+        assert wrapped.get(sym, sym) in with_stream, f"{sym} takes a stream but its binding has no stream="
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="host-validation test uses fake device pointers; CPU only")
 def test_host_validation_rejects_bad_arguments():
     _lib_path()
